@@ -1,0 +1,433 @@
+"""Benchmark: fp9 MoE-layer decode on one GB300 (DeepSeek-V3 MoE layer, bsz 1).
+
+A step is one MoE-layer forward (router, fused fp9 expert kernel, combine)
+for one batch of synthetic tokens, on one of several resident layers in
+turn, so every step streams its 446 MB of fp9 expert weights from HBM
+(4 layers x 12.7 GB rotate; no weight is re-read within 3 steps, far more
+than the 129 MB L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+the host cores instead (one token through one expert FFN per step, scaled
+to MoE-layer tokens/s). Multi-GPU runs are independent replicas (the path
+has no exchange step), launched one rank per GPU by torchrun.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fp9 MoE-layer decode tok/s (bsz 1/2) & weight-stream HBM GB/s vs GB300 peak"
+FP9_BYTES_PER_WEIGHT = 9.0 / 8.0
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--bsz", type=int, default=1)
+    p.add_argument("--layers", type=int, default=4, help="resident layers rotated per step")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="skip the bsz-2 / dense side runs")
+    p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ clock sampler
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- native bench
+
+def _native(args):
+    import torch
+    import torch.distributed as dist
+
+    from fp9_weight_expert_gb300 import Workspace, binding, build_lib, layers, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if rank == 0:
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    binding.load()
+
+    shape = synth.DSV3
+    H, I, bsz = shape.hidden, shape.inter, args.bsz
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def make_layer(l):
+        L = layers.MoELayer(H, I, shape.n_experts, shape.n_groups, shape.topk_groups, shape.topk,
+                            shape.n_shared, shape.route_scale, dev)
+        kinds = (synth.ROUTED, synth.SHARED)
+        L.fill(lambda b, k, m: synth.ffn_weight(shape, I, H, synth.seed_for(1000 + rank, l, kinds[b], k, m), dev),
+               synth.normal((shape.n_experts, H), shape.router_std,
+                            synth.seed_for(1000 + rank, l, synth.ROUTER), dev), status)
+        return L
+
+    t0 = time.time()
+    Ls = [make_layer(l) for l in range(args.layers)]
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("packing failed: " + binding.status_str(int(status.item())))
+    setup_s = time.time() - t0
+
+    n_tok = 64
+    xs = synth.tokens(n_tok * bsz, H, synth.seed_for(2000 + rank, 0, synth.TOKENS), dev).view(n_tok, bsz, H)
+    y = torch.empty((bsz, H), dtype=torch.float32, device=dev)
+    K, W = args.steps, args.warmup
+    ids = torch.empty((K, bsz, shape.topk), dtype=torch.int32, device=dev)
+    ws = Workspace.for_moe(Ls[0], bsz, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ids_out=None):
+        binding.fp9_moe_forward(Ls[i % len(Ls)], xs[i % n_tok], y, ws.tensor, status, ids_out)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        binding.fp9_profile_events(ev_k[i][0], ev_k[i][1])
+        step(W + i, ids[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    binding.fp9_profile_events(None, None)
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.1)
+    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status: " + binding.status_str(int(status.item())))
+
+    elapsed_ms = start.elapsed_time(stop)
+    kern_ms = [a.elapsed_time(b) for a, b in ev_k]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # union of experts streamed per step: distinct routed ids + shared
+    idc = ids.cpu()
+    units = [len(set(idc[i].flatten().tolist())) + shape.n_shared for i in range(K)]
+    unit_bytes = 3 * I * H * FP9_BYTES_PER_WEIGHT
+    weight_bytes = [u * unit_bytes for u in units]
+    mean_kern_s = sum(kern_ms) / K / 1e3
+    kernel_gbs = (sum(weight_bytes) / K) / mean_kern_s / 1e9
+    step_gbs = sum(weight_bytes) / (elapsed_ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+
+    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of y, per step
+    Ke = min(K, 500)
+    xh = torch.empty((n_tok, bsz, H), dtype=torch.float32).pin_memory()
+    xh.copy_(xs.cpu())
+    yh = torch.empty((bsz, H), dtype=torch.float32).pin_memory()
+    xd = torch.empty((bsz, H), dtype=torch.float32, device=dev)
+    for i in range(3):
+        xd.copy_(xh[i % n_tok], non_blocking=True)
+        binding.fp9_moe_forward(Ls[i % len(Ls)], xd, y, ws.tensor, status)
+        yh.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_e = time.perf_counter()
+    for i in range(Ke):
+        xd.copy_(xh[i % n_tok], non_blocking=True)
+        binding.fp9_moe_forward(Ls[i % len(Ls)], xd, y, ws.tensor, status)
+        yh.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t_e
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    extra = {}
+    if not args.no_extra and world == 1:
+        extra = _side_runs(Ls, ws, status, dev, shape)
+
+    if rank != 0:
+        return None
+    value = world * bsz * K / (elapsed_ms / 1e3)
+    clocks = sampler.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(elapsed_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights packed to fp9 on the GPU, N(0,1) tokens)",
+        "config": {
+            "workload": "one DeepSeek-V3 MoE layer, bsz 1: hidden 7168, 256 routed experts "
+                        "(8 groups x 32, top-4 groups, top-8) + 1 shared, intermediate 2048, fp9 weights",
+            "bsz": bsz,
+            "resident_layers": len(Ls),
+            "l2": "inputs larger than L2: 4 resident layers (12.7 GB each) rotate, each step streams "
+                  f"{sum(weight_bytes) / K / 1e6:.1f} MB of fp9 weights",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "fp9::expert_kernel",
+            "achieved": round(kernel_gbs, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(kernel_gbs / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": round(sum(weight_bytes) / K),
+            "kernel_us": round(mean_kern_s * 1e6, 2),
+        },
+        "weight_stream_gbs_per_step": round(step_gbs, 1),
+        "us_per_layer": round(elapsed_ms / K * 1e3, 2),
+        "e2e": {
+            "value": round(world * bsz * Ke / e2e_s, 2),
+            "unit": "tok/s",
+            "h2d_bytes_per_step": bsz * H * 4,
+            "d2h_bytes_per_step": bsz * H * 4,
+            "steps": Ke,
+        },
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "setup_s": round(setup_s, 1),
+    }
+    if extra:
+        out["extra"] = extra
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = _cpu_baseline(mode="layer")
+    return out
+
+
+def _side_runs(Ls, ws, status, dev, shape):
+    """bsz 2 on the same layers (weight-stream GB/s of the union of experts)."""
+    import torch
+
+    from fp9_weight_expert_gb300 import Workspace, binding, synth
+    res = {}
+    for bsz in (2,):
+        K = 400
+        xs = synth.tokens(64 * bsz, shape.hidden, synth.seed_for(3000, bsz, synth.TOKENS), dev).view(64, bsz, -1)
+        y = torch.empty((bsz, shape.hidden), device=dev)
+        ids = torch.empty((K, bsz, shape.topk), dtype=torch.int32, device=dev)
+        w2 = Workspace.for_moe(Ls[0], bsz, dev)
+        for i in range(10):
+            binding.fp9_moe_forward(Ls[i % len(Ls)], xs[i % 64], y, w2.tensor, status)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(K):
+            binding.fp9_moe_forward(Ls[i % len(Ls)], xs[i % 64], y, w2.tensor, status, ids[i])
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        idc = ids.cpu()
+        units = sum(len(set(idc[i].flatten().tolist())) + shape.n_shared for i in range(K))
+        gbs = units * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT / (ms / 1e3) / 1e9
+        res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
+                            "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
+    return res
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def _cpu_baseline(mode: str, steps: int = 0, warmup: int = 0):
+    """Runs the oracle in a fresh single-threaded process (no CUDA) and
+    returns its timing record."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample", f"{mode}:{steps}:{warmup}"]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _cpu_sample_worker(spec: str):
+    """Oracle timing, CPU only. mode 'layer': one token through one full
+    DeepSeek-V3 MoE layer (router + 8 routed + 1 shared expert FFN).
+    mode 'expert': per step one token through one of its 9 expert FFNs."""
+    import numpy as np
+
+    import oracle as O
+    from fp9_weight_expert_gb300 import synth
+
+    mode, steps, warmup = spec.split(":")
+    steps, warmup = int(steps), int(warmup)
+    shape = synth.DSV3
+    H, I = shape.hidden, shape.inter
+    wr = synth.normal((shape.n_experts, H), shape.router_std, synth.seed_for(5000, 0, synth.ROUTER)).numpy()
+    x = synth.tokens(1, H, synth.seed_for(5000, 0, synth.TOKENS)).numpy()
+    t0 = time.perf_counter()
+    ids, w = O.route(x, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
+    t_router = time.perf_counter() - t0
+
+    def planes(kind, k):
+        out = []
+        for m in range(3):
+            body, sign, _ = O.fp9_pack(synth.ffn_weight(shape, I, H, synth.seed_for(5000, 0, kind, k, m)).numpy())
+            out += [body, sign]
+        return tuple(out)
+
+    experts = [(synth.ROUTED, int(e), float(wt)) for e, wt in zip(ids[0], w[0])] + [(synth.SHARED, 0, 1.0)]
+    if mode == "layer":
+        cache = {k: planes(kind, k) for kind, k, _ in experts if kind == synth.ROUTED}
+        shared = [planes(synth.SHARED, 0)]
+        t0 = time.perf_counter()
+        y = O.moe(x, wr, lambda e: cache[e], shared, shape.n_groups, shape.topk_groups, shape.topk,
+                  shape.route_scale)
+        dt = time.perf_counter() - t0
+        assert np.isfinite(y).all()
+        print(json.dumps({"value": round(1.0 / dt, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                          "seconds": round(dt, 3),
+                          "sample": "one token through one DeepSeek-V3 MoE layer (router over 256 experts, "
+                                    "8 routed + 1 shared expert FFN, fp64 numpy oracle, 1 thread)"}))
+        return
+    n = min(len(experts), steps + warmup)
+    cache = [planes(kind, k) for kind, k, _ in experts[:n]]
+    times = []
+    for i in range(warmup + steps):
+        kind, k, wt = experts[i % n]
+        t0 = time.perf_counter()
+        yk = wt * O.dense_ffn(x, cache[i % n])
+        times.append(time.perf_counter() - t0)
+        assert np.isfinite(yk).all()
+    t_exp = statistics.mean(times[warmup:]) if steps else statistics.mean(times)
+    per_layer = t_router + len(experts) * t_exp
+    print(json.dumps({"value": round(1.0 / per_layer, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                      "seconds_per_expert": round(t_exp, 4), "router_seconds": round(t_router, 4),
+                      "seconds_per_step": round(t_exp, 4),
+                      "sample": "per step one token through one of its 9 expert FFNs of a DeepSeek-V3 MoE "
+                                "layer (fp64 numpy oracle, 1 thread); MoE-layer tok/s = "
+                                "1 / (router + 9 x mean expert time)"}))
+
+
+def _reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    rec = _cpu_baseline(mode="expert", steps=args.steps, warmup=args.warmup)
+    if "error" in rec:
+        return {"impl": "reference", "unavailable": "oracle run failed: " + rec["error"][-200:]}
+    v = rec["value"]
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "tok/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(rec["seconds_per_step"] * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "one DeepSeek-V3 MoE layer, bsz 1 (CPU oracle, sampled per expert)",
+                   "bsz": 1},
+        "cpu_baseline": rec,
+        "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = _args()
+    if args.cpu_sample:
+        _cpu_sample_worker(args.cpu_sample)
+        return
+    out = _reference(args) if args.impl == "reference" else _native(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

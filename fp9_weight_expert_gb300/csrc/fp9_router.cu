@@ -1,0 +1,356 @@
+// Router: fp32 logits x . W_g, sigmoid, group-limited top-k, normalised and
+// scaled weights; then the job list for the fused expert kernel.
+//
+// The pages fix top_k = 8 experts per token ([MTP-9.2], "第 9 章 MTP1
+// dual-lane overlap", section 9.2); the grouping (8 groups of 32, top-4
+// groups ranked by the sum of their two best scores) is the DeepSeek-V3 gate.
+//
+// One launch: every CTA computes the logits of kRouterRows experts for all
+// tokens; the last CTA to finish (a self-resetting atomicInc ticket, no
+// waiting) reads all logits back and does the selection and the job build.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "fp9_device.cuh"
+#include "fp9_host.h"
+#include "fp9_plan.h"
+#include "fp9moe.h"
+
+namespace fp9 {
+
+constexpr int kRouterThreads = 256;
+constexpr int kRouterRows = 2;
+constexpr int kMaxEntries = FP9_MAX_BSZ * FP9_MAX_TOPK;  // 128 (token, expert) pairs
+static_assert(kMaxEntries <= kRouterThreads, "one thread per routed pair");
+
+struct RouterArgs {
+    const float* x;      // [bsz, H]
+    const float* wr;     // [E, H]
+    int32_t bsz, E, H, n_groups, topk_groups, topk, n_shared;
+    float scale;
+    Control* ctl;
+    float* logits;       // [bsz, E]
+    int32_t* ids_ws;     // [bsz, topk]
+    float* w_ws;         // [bsz, topk]
+    int32_t* ids_out;    // optional
+    float* w_out;        // optional
+    Job* jobs;           // [jmax]
+};
+
+// Argmax over a warp of (value, index) pairs: larger value wins, ties go to
+// the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, m);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, m);
+        if (ov > v || (ov == v && oi < idx)) {
+            v = ov;
+            idx = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// Selection for token t by one warp. `s` holds the token's E sigmoid
+// scores (NaN already replaced by -inf so that the choice stays defined).
+__device__ void select_token(const RouterArgs& a, const float* s, int t, int lane) {
+    const int gsize = a.E / a.n_groups;
+    // group scores: sum of the two largest members (the one member if gsize == 1)
+    float gscore = -INFINITY;
+    if (lane < a.n_groups) {
+        float m1 = -INFINITY, m2 = -INFINITY;
+        for (int i = 0; i < gsize; ++i) {
+            const float v = s[lane * gsize + i];
+            if (v > m1) {
+                m2 = m1;
+                m1 = v;
+            } else if (v > m2) {
+                m2 = v;
+            }
+        }
+        gscore = (gsize == 1) ? m1 : m1 + m2;
+    }
+    uint32_t kept = 0;  // bit g set when group g is kept
+    for (int r = 0; r < a.topk_groups; ++r) {
+        float v = -INFINITY;
+        int idx = INT_MAX;
+        if (lane < a.n_groups && !((kept >> lane) & 1u)) {
+            v = gscore;
+            idx = lane;
+        }
+        warp_argmax(v, idx);
+        kept |= 1u << idx;
+    }
+    // experts e = lane + 32 * j; chosen bits per lane
+    uint32_t taken = 0;
+    const int per_lane = (a.E + 31) / 32;
+    float sum = 0.0f;
+    int my_id = 0;
+    float my_s = 0.0f;
+    for (int k = 0; k < a.topk; ++k) {
+        float v = -INFINITY;
+        int idx = INT_MAX;
+        for (int j = 0; j < per_lane; ++j) {
+            const int e = lane + 32 * j;
+            if (e < a.E && ((kept >> (e / gsize)) & 1u) && !((taken >> j) & 1u)) {
+                if (better(s[e], e, v, idx)) {
+                    v = s[e];
+                    idx = e;
+                }
+            }
+        }
+        warp_argmax(v, idx);
+        if ((idx & 31) == lane) taken |= 1u << (idx / 32);
+        sum += v;  // identical on every lane, added in rank order
+        if (lane == k) {
+            my_id = idx;
+            my_s = v;
+        }
+    }
+    if (lane < a.topk) {
+        const float w = my_s / sum * a.scale;
+        a.ids_ws[t * a.topk + lane] = my_id;
+        a.w_ws[t * a.topk + lane] = w;
+        if (a.ids_out) a.ids_out[t * a.topk + lane] = my_id;
+        if (a.w_out) a.w_out[t * a.topk + lane] = w;
+    }
+}
+
+// Job list: shared experts first (tokens in pairs, weight 1), then routed
+// experts in ascending id, each with its tokens in ascending order, in
+// groups of up to two.
+__device__ void build_jobs(const RouterArgs& a, int tid) {
+    __shared__ int32_t s_in[kMaxEntries];
+    __shared__ int32_t s_key[kMaxEntries];
+    __shared__ float s_w[kMaxEntries];
+    __shared__ int32_t s_start[kMaxEntries];
+    const int P = a.bsz * a.topk;
+    int32_t key = INT_MAX;
+    float w = 0.0f;
+    if (tid < P) {
+        const int t = tid / a.topk;
+        key = a.ids_ws[tid] * FP9_MAX_BSZ + t;  // unique: a token picks an expert once
+        w = a.w_ws[tid];
+        s_in[tid] = key;
+    }
+    __syncthreads();
+    if (tid < P) {  // counting sort of the unique keys
+        int rank = 0;
+        for (int q = 0; q < P; ++q) rank += (s_in[q] < key) ? 1 : 0;
+        s_key[rank] = key;
+        s_w[rank] = w;
+    }
+    __syncthreads();
+    int is_start = 0;
+    int e = 0;
+    if (tid < P) {
+        e = s_key[tid] / FP9_MAX_BSZ;
+        int pos = 0;
+        for (int q = 0; q < tid; ++q) pos += (s_key[q] / FP9_MAX_BSZ == e) ? 1 : 0;
+        is_start = (pos % kTokensPerJob == 0) ? 1 : 0;
+        s_start[tid] = is_start;
+    }
+    __syncthreads();
+    const int pairs = (a.bsz + kTokensPerJob - 1) / kTokensPerJob;
+    const int nshared_jobs = a.n_shared * pairs;
+    if (tid < P && is_start) {
+        int before = 0;
+        for (int q = 0; q < tid; ++q) before += s_start[q];
+        Job j;
+        j.bank = 0;
+        j.expert = e;
+        j.pad0 = 0;
+        j.tok[0] = s_key[tid] % FP9_MAX_BSZ;
+        j.w[0] = s_w[tid];
+        const bool two = (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
+        j.ntok = two ? 2 : 1;
+        j.tok[1] = two ? s_key[tid + 1] % FP9_MAX_BSZ : j.tok[0];
+        j.w[1] = two ? s_w[tid + 1] : 0.0f;
+        a.jobs[nshared_jobs + before] = j;
+    }
+    if (tid < nshared_jobs) {
+        const int sh = tid / pairs, pr = tid % pairs;
+        Job j;
+        j.bank = 1;
+        j.expert = sh;
+        j.pad0 = 0;
+        j.tok[0] = 2 * pr;
+        j.ntok = (2 * pr + 1 < a.bsz) ? 2 : 1;
+        j.tok[1] = (j.ntok == 2) ? 2 * pr + 1 : 2 * pr;
+        j.w[0] = 1.0f;
+        j.w[1] = (j.ntok == 2) ? 1.0f : 0.0f;
+        a.jobs[tid] = j;
+    }
+    if (tid == 0) {
+        int starts = 0;
+        for (int q = 0; q < P; ++q) starts += s_start[q];
+        a.ctl->njobs = nshared_jobs + starts;
+    }
+}
+
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
+    extern __shared__ float s_scores[];  // [bsz, E] in the last CTA
+    __shared__ float s_red[kRouterThreads / 32][kRouterRows][FP9_MAX_BSZ];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e0 = blockIdx.x * kRouterRows;
+    const int H4 = a.H / 4;
+
+    float acc[kRouterRows][FP9_MAX_BSZ];
+#pragma unroll
+    for (int r = 0; r < kRouterRows; ++r)
+#pragma unroll
+        for (int t = 0; t < FP9_MAX_BSZ; ++t) acc[r][t] = 0.0f;
+
+    const float4* x4 = reinterpret_cast<const float4*>(a.x);
+    const float4* w4 = reinterpret_cast<const float4*>(a.wr);
+#pragma unroll 4
+    for (int c = tid; c < H4; c += kRouterThreads) {
+        float4 wv[kRouterRows];
+#pragma unroll
+        for (int r = 0; r < kRouterRows; ++r)
+            wv[r] = (e0 + r < a.E) ? __ldcs(w4 + static_cast<int64_t>(e0 + r) * H4 + c)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < FP9_MAX_BSZ; ++t) {
+            if (t < a.bsz) {
+                const float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
+#pragma unroll
+                for (int r = 0; r < kRouterRows; ++r) {
+                    float v = acc[r][t];
+                    v = fmaf(wv[r].x, xv.x, v);
+                    v = fmaf(wv[r].y, xv.y, v);
+                    v = fmaf(wv[r].z, xv.z, v);
+                    v = fmaf(wv[r].w, xv.w, v);
+                    acc[r][t] = v;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kRouterRows; ++r)
+#pragma unroll
+        for (int t = 0; t < FP9_MAX_BSZ; ++t) {
+            const float v = warp_sum(acc[r][t]);
+            if (lane == 0) s_red[warp][r][t] = v;
+        }
+    __syncthreads();
+    if (tid < kRouterRows * FP9_MAX_BSZ) {
+        const int r = tid / FP9_MAX_BSZ, t = tid % FP9_MAX_BSZ;
+        if (t < a.bsz && e0 + r < a.E) {
+            float v = 0.0f;
+            for (int w = 0; w < kRouterThreads / 32; ++w) v += s_red[w][r][t];
+            a.logits[t * a.E + e0 + r] = v;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicInc(&a.ctl->ticket, gridDim.x - 1) == gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    for (int i = tid; i < a.bsz * a.E; i += kRouterThreads) {
+        const float l = __ldcg(a.logits + i);
+        const float s = 1.0f / (1.0f + expf(-l));
+        s_scores[i] = (s == s) ? s : -INFINITY;
+    }
+    __syncthreads();
+    if (warp < a.bsz) select_token(a, s_scores + warp * a.E, warp, lane);
+    __threadfence_block();
+    __syncthreads();
+    if (a.jobs != nullptr) build_jobs(a, tid);
+}
+
+// Validation shared by moe_router and fp9_moe_forward (no CUDA calls).
+fp9_status check_layer(const fp9_moe_layer* L, int32_t bsz) {
+    FP9_CHECK_ARG(L != nullptr, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(bsz >= 1 && bsz <= FP9_MAX_BSZ, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(hidden_ok(L->hidden), FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->inter >= 1, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->n_experts >= 1 && L->n_experts <= FP9_MAX_EXPERTS, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->n_groups >= 1 && L->n_groups <= FP9_MAX_GROUPS && L->n_experts % L->n_groups == 0,
+                  FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->topk_groups >= 1 && L->topk_groups <= L->n_groups, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->topk >= 1 && L->topk <= FP9_MAX_TOPK &&
+                      L->topk <= L->topk_groups * (L->n_experts / L->n_groups),
+                  FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->n_shared >= 0 && L->n_shared <= FP9_MAX_SHARED, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->route_scale == L->route_scale, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(L->w_router != nullptr, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(L->w_router, 16), FP9_ERR_ALIGN);
+    fp9_status st = check_bank(L->routed, L->n_experts, L->inter, L->hidden);
+    if (st != FP9_OK) return st;
+    if (L->n_shared > 0) {
+        st = check_bank(L->shared, L->n_shared, L->inter, L->hidden);
+        if (st != FP9_OK) return st;
+    }
+    return FP9_OK;
+}
+
+// Queues the router kernel; writes the job list when `build` is set.
+fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, int32_t* ids_out,
+                         float* w_out, uint8_t* ws, const WsLayout& lay, bool build, cudaStream_t stream) {
+    RouterArgs a;
+    a.x = x;
+    a.wr = L->w_router;
+    a.bsz = bsz;
+    a.E = L->n_experts;
+    a.H = static_cast<int32_t>(L->hidden);
+    a.n_groups = L->n_groups;
+    a.topk_groups = L->topk_groups;
+    a.topk = L->topk;
+    a.n_shared = L->n_shared;
+    a.scale = L->route_scale;
+    a.ctl = reinterpret_cast<Control*>(ws);
+    a.logits = reinterpret_cast<float*>(ws + lay.off_logits);
+    a.ids_ws = reinterpret_cast<int32_t*>(ws + lay.off_ids);
+    a.w_ws = reinterpret_cast<float*>(ws + lay.off_w);
+    a.ids_out = ids_out;
+    a.w_out = w_out;
+    a.jobs = build ? reinterpret_cast<Job*>(ws + lay.off_jobs) : nullptr;
+    const unsigned grid = (L->n_experts + kRouterRows - 1) / kRouterRows;
+    const size_t smem = sizeof(float) * bsz * L->n_experts;
+    if (smem > 48 * 1024) {
+        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem)));
+    }
+    router_kernel<<<grid, kRouterThreads, smem, stream>>>(a);
+    FP9_CUDA_TRY(cudaGetLastError());
+    return FP9_OK;
+}
+
+}  // namespace fp9
+
+using namespace fp9;
+
+extern "C" size_t fp9_moe_workspace_bytes(const fp9_moe_layer* layer, int32_t bsz) {
+    if (check_layer(layer, bsz) != FP9_OK) return 0;
+    const int32_t sms = device_sm_count();
+    if (sms <= 0) return 0;
+    return moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms)
+        .total;
+}
+
+extern "C" fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int32_t bsz, int32_t* ids,
+                                 float* weights, void* ws, size_t ws_bytes, void* stream) {
+    fp9_status st = check_layer(layer, bsz);
+    if (st != FP9_OK) return st;
+    FP9_CHECK_ARG(x != nullptr && ids != nullptr && weights != nullptr && ws != nullptr, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(x, 16), FP9_ERR_ALIGN);
+    FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
+    const int32_t sms = device_sm_count();
+    FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
+    const WsLayout lay =
+        moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms);
+    FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
+    return launch_router(layer, x, bsz, ids, weights, static_cast<uint8_t*>(ws), lay, false,
+                         static_cast<cudaStream_t>(stream));
+}

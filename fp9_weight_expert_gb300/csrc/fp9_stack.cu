@@ -1,0 +1,76 @@
+// Stack glue between MoE layers: h += y, then x = RMSNorm(h) with unit gain.
+//
+// The pages keep the norm and the residual add on the GPU side of each
+// decode layer, next to attention ("第 9 章 MTP1 dual-lane overlap", section
+// 9.5: stage0 holds layernorm and the residual add); the step between two
+// MoE layers of a stack is h <- h + MoE(RMSNorm(h)).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fp9_device.cuh"
+#include "fp9_host.h"
+#include "fp9moe.h"
+
+namespace fp9 {
+
+constexpr int kNormThreads = 256;
+
+// One CTA per token; each thread keeps its float4 columns in a fixed order,
+// and the block sum of squares is added in a fixed order.
+__global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(float* h, const float* y, float* x_out,
+                                                                       int64_t H, float eps) {
+    __shared__ float red[kNormThreads / 32];
+    __shared__ float s_scale;
+    const int t = blockIdx.x;
+    float4* h4 = reinterpret_cast<float4*>(h + t * H);
+    const float4* y4 = y ? reinterpret_cast<const float4*>(y + t * H) : nullptr;
+    float4* x4 = reinterpret_cast<float4*>(x_out + t * H);
+    const int64_t H4 = H / 4;
+    float ss = 0.0f;
+    for (int64_t c = threadIdx.x; c < H4; c += kNormThreads) {
+        float4 v = h4[c];
+        if (y4) {
+            const float4 d = y4[c];
+            v.x += d.x;
+            v.y += d.y;
+            v.z += d.z;
+            v.w += d.w;
+            h4[c] = v;
+        }
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.0f;
+        for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+        s_scale = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+    }
+    __syncthreads();
+    const float scale = s_scale;
+    for (int64_t c = threadIdx.x; c < H4; c += kNormThreads) {
+        const float4 v = h4[c];
+        x4[c] = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
+    }
+}
+
+}  // namespace fp9
+
+using namespace fp9;
+
+extern "C" fp9_status fp9_residual_rmsnorm(float* h, const float* y, float* x_out, int32_t bsz, int64_t hidden,
+                                           float eps, void* stream) {
+    FP9_CHECK_ARG(h != nullptr && x_out != nullptr, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(bsz >= 1 && bsz <= FP9_MAX_BSZ, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(hidden >= 4 && hidden % 4 == 0, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(eps >= 0.0f, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(h, 16) && aligned(x_out, 16) && (y == nullptr || aligned(y, 16)), FP9_ERR_ALIGN);
+    residual_rmsnorm_kernel<<<bsz, kNormThreads, 0, static_cast<cudaStream_t>(stream)>>>(h, y, x_out, hidden, eps);
+    FP9_CUDA_TRY(cudaGetLastError());
+    return FP9_OK;
+}

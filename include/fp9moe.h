@@ -1,0 +1,225 @@
+/*
+ * fp9moe.h -- C ABI of the fp9 FFN/MoE decode-step library (libfp9moe.so).
+ *
+ * The library computes the decode-time FFN/MoE step of a DeepSeek-V3-class
+ * model whose expert weights are stored in the fp9 format, on one GB300
+ * (sm_103a) GPU, with hand-written CUDA kernels.
+ *
+ * Sources of the method:
+ *   [MEMOIR-FP9]  "一鸭三吃：我把评测鸭变成了满血 DeepSeek-V3.2 推理系统"
+ *                 (judgeduck.ai/duck-llm/zh/memoir.html), section
+ *                 "在只有 AVX2 的 N100 上，我先做出了单核 MLP fp9": the fp9
+ *                 format (1 sign bit, 5 exponent bits with the fp16 bias 15,
+ *                 3 mantissa bits), stored as an 8-bit body byte per weight
+ *                 plus a sign plane of 8 signs per byte, decoded by shifting
+ *                 the body into fp16 bits and widening to fp32.
+ *   [MEMOIR-COMM] same page, section "真正难的不是把参数塞下，而是通信": the
+ *                 FFN is split tensor-parallel and f32 partial sums are added.
+ *   [MEMOIR-16]   same page, section "16 tok/s 之后": the MoE forward and its
+ *                 reduce of partial sums.
+ *   [MTP-9.2]     "第 9 章 MTP1 dual-lane overlap"
+ *                 (judgeduck.ai/duck-llm/zh/09-mtp1-dual-lane-overlap.html),
+ *                 section 9.2: top_k = 8; a bsz = 2 pair reads two nearly
+ *                 disjoint expert sets.
+ *   [DS4-TP]      "ds4.c 学习笔记 — 张量并行"
+ *                 (ds4-learning.pages.dev/glossary/tensor-parallelism.html),
+ *                 section "形态一：Mac-to-Mac 张量并行": f32 partial sums, at
+ *                 most 8 rows per verify batch.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to memory of the current
+ *     CUDA device; the caller owns all memory. The library allocates no
+ *     memory and never synchronises: work is queued on `stream` (a
+ *     cudaStream_t; NULL means the legacy default stream).
+ *   - Argument checks run on the host before anything is queued and are
+ *     returned synchronously. A failed launch returns FP9_ERR_CUDA.
+ *   - Conditions found on the device (a value out of fp9 range, a bounded
+ *     wait that ran out) are recorded in *d_status, a device int32 the
+ *     caller zeroes; the first error wins. d_status may be NULL, in which
+ *     case they are not reported.
+ *   - Matrices are row-major. An fp9 matrix [rows, cols] is two planes:
+ *       body [rows, cols] uint8, byte = eeeeemmm;
+ *       sign [rows, cols/8] uint8, the sign of column c in bit (c mod 8) of
+ *       byte c/8 (least significant bit first); cols % 8 == 0.
+ *   - Calls that share a workspace must not overlap in time (use one
+ *     workspace per stream).
+ */
+#ifndef FP9MOE_H
+#define FP9MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp9_status {
+    FP9_OK = 0,
+    FP9_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad count      */
+    FP9_ERR_SHAPE = 2,       /* a dimension breaks a layout rule            */
+    FP9_ERR_ALIGN = 3,       /* a pointer is not aligned as required        */
+    FP9_ERR_WORKSPACE = 4,   /* the workspace is too small                  */
+    FP9_ERR_RANGE = 5,       /* device: a value is not representable in fp9 */
+    FP9_ERR_CUDA = 6,        /* a CUDA runtime call failed                  */
+    FP9_ERR_TIMEOUT = 7      /* device: a bounded wait ran out              */
+} fp9_status;
+
+/* Limits of this implementation. */
+#define FP9_MAX_BSZ 8          /* tokens per call ([DS4-TP]: 8 verify rows) */
+#define FP9_MAX_HIDDEN 7168    /* hidden size H; H % 128 == 0              */
+#define FP9_MAX_EXPERTS 1024   /* routed experts per layer                  */
+#define FP9_MAX_GROUPS 32      /* router groups                             */
+#define FP9_MAX_TOPK 16        /* experts chosen per token                  */
+#define FP9_MAX_SHARED 8       /* shared experts per layer                  */
+
+/*
+ * A bank of n SwiGLU FFNs of equal shape, each three fp9 matrices of
+ * [inter, hidden]: gate, up and down_t = W_down^T (so that one
+ * intermediate row's down weights are contiguous). Each plane pointer is a
+ * device pointer to n contiguous matrices:
+ *   gate_body, up_body, down_body: [n, inter, hidden]      uint8
+ *   gate_sign, up_sign, down_sign: [n, inter, hidden / 8]  uint8
+ * All six must be 16-byte aligned. For FFN k, y = W_down (SiLU(W_gate x) *
+ * (W_up x)) [MEMOIR-FP9].
+ */
+typedef struct fp9_ffn_bank {
+    int64_t n;
+    int64_t inter;
+    int64_t hidden;
+    const uint8_t* gate_body;
+    const uint8_t* gate_sign;
+    const uint8_t* up_body;
+    const uint8_t* up_sign;
+    const uint8_t* down_body;
+    const uint8_t* down_sign;
+} fp9_ffn_bank;
+
+/*
+ * One MoE layer (host struct; its pointers are device pointers).
+ * Router: s = sigmoid(w_router x) over n_experts (w_router fp32
+ * [n_experts, hidden], 16-byte aligned); the experts form n_groups equal
+ * groups; a group scores the sum of its two largest s (its one s if groups
+ * have one expert); the topk_groups best groups are kept, then the topk
+ * best experts inside them (ties go to the lower index), with weights
+ * s_i / sum(s_chosen) * route_scale. top_k = 8 is the pages' value
+ * [MTP-9.2]; the grouping is the DeepSeek-V3 gate.
+ * Output: y = sum_k w_k FFN_{id_k}(x) + sum of the shared FFNs (weight 1).
+ * routed.n must equal n_experts and shared.n must equal n_shared; both
+ * banks share the layer's hidden and inter.
+ */
+typedef struct fp9_moe_layer {
+    int64_t hidden;
+    int64_t inter;
+    int32_t n_experts;
+    int32_t n_groups;
+    int32_t topk_groups;
+    int32_t topk;
+    int32_t n_shared;
+    float route_scale;
+    const float* w_router;
+    fp9_ffn_bank routed;
+    fp9_ffn_bank shared;
+} fp9_moe_layer;
+
+/*
+ * fp9_pack: encode an fp32 matrix to fp9 planes [MEMOIR-FP9].
+ *   src  device fp32 [rows, cols], 16-byte aligned.
+ *   body device uint8 [rows, cols]; sign device uint8 [rows, cols / 8].
+ *   Rounds to nearest, ties to the even mantissa, directly from fp32;
+ *   keeps subnormals and the sign of zero. |x| >= 63488, Inf and NaN are
+ *   stored as e = 31 codes (Inf: body 0xF8, NaN: body 0xFC) and recorded
+ *   as FP9_ERR_RANGE in *d_status.
+ *   Needs cols % 8 == 0 (FP9_ERR_SHAPE); rows, cols >= 0 (0 is a no-op).
+ */
+fp9_status fp9_pack(const float* src, int64_t rows, int64_t cols,
+                    uint8_t* body, uint8_t* sign, int32_t* d_status, void* stream);
+
+/*
+ * fp9_decode: fp9 planes -> fp32 [rows, cols], bit-exact: each value is
+ * the IEEE fp16 with bits (body << 7 | sign << 15), widened [MEMOIR-FP9].
+ *   body, sign as in fp9_pack (device); dst device fp32 [rows, cols],
+ *   16-byte aligned. cols % 8 == 0.
+ */
+fp9_status fp9_decode(const uint8_t* body, const uint8_t* sign, int64_t rows,
+                      int64_t cols, float* dst, void* stream);
+
+/*
+ * Workspace sizes (bytes) for moe_router / fp9_moe_forward and for
+ * fp9_dense_ffn at batch bsz, on the current device. Return 0 when the
+ * arguments are invalid or the device cannot be queried. A workspace must
+ * be 256-byte aligned and zeroed once after allocation; every call leaves
+ * its internal counter at zero again.
+ */
+size_t fp9_moe_workspace_bytes(const fp9_moe_layer* layer, int32_t bsz);
+size_t fp9_dense_workspace_bytes(const fp9_ffn_bank* ffn, int32_t bsz);
+
+/*
+ * moe_router: routing only.
+ *   x device fp32 [bsz, hidden]; ids device int32 [bsz, topk] in
+ *   descending score order; weights device fp32 [bsz, topk]. 1 <= bsz <=
+ *   FP9_MAX_BSZ. Logits are fp32 dot products.
+ */
+fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int32_t bsz,
+                      int32_t* ids, float* weights, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * fp9_moe_forward: y = MoE(x) for one layer, at 1 <= bsz <= FP9_MAX_BSZ.
+ *   x, y device fp32 [bsz, hidden], 16-byte aligned (y may not alias x).
+ *   ids / weights: optional device outputs of the routing (NULL to skip).
+ *   Weights are streamed once per call for each group of up to two tokens
+ *   that share an expert; partial sums over intermediate slices stay fp32
+ *   and are added in a fixed order, so results are deterministic for a
+ *   given device ([MEMOIR-COMM], [MEMOIR-16], [DS4-TP]).
+ */
+fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x,
+                           int32_t bsz, float* y, int32_t* ids, float* weights,
+                           void* ws, size_t ws_bytes, int32_t* d_status,
+                           void* stream);
+
+/*
+ * fp9_dense_ffn: y = FFN(x) for a dense fp9 SwiGLU FFN (ffn->n == 1), as in
+ * the model's first layers. x, y device fp32 [bsz, hidden].
+ */
+fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
+                         float* y, void* ws, size_t ws_bytes, int32_t* d_status,
+                         void* stream);
+
+/*
+ * fp9_residual_rmsnorm: stack glue between layers, per token t:
+ *   h[t] += y[t] (skipped when y is NULL);
+ *   x_out[t] = h[t] / sqrt(mean(h[t]^2) + eps)   (unit gain).
+ *   h, y, x_out device fp32 [bsz, hidden], 16-byte aligned, hidden % 4 == 0.
+ */
+fp9_status fp9_residual_rmsnorm(float* h, const float* y, float* x_out,
+                                int32_t bsz, int64_t hidden, float eps,
+                                void* stream);
+
+/*
+ * fp9_selftest_timeout: failure-detection check. Launches the fused expert
+ * kernel on a small dense problem with its weight copies switched off, so
+ * every consumer wait runs out after timeout_us microseconds; the kernel
+ * records FP9_ERR_TIMEOUT in *d_status and returns with the context
+ * intact. ws: device, >= 64 KiB, 256-byte aligned (used as x and scratch).
+ */
+fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status,
+                                int32_t timeout_us, void* stream);
+
+/*
+ * fp9_profile_events: tracing hook. When both events (cudaEvent_t handles
+ * created by the caller) are non-NULL, every later launch of the fused
+ * expert kernel records `start` just before and `stop` just after itself,
+ * on its own stream, so the caller can time that kernel alone; NULL, NULL
+ * turns this off. Process-wide setting, not thread-safe.
+ */
+void fp9_profile_events(void* start, void* stop);
+
+/* Human-readable name of a status code (static string). */
+const char* fp9_status_str(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP9MOE_H */

@@ -98,19 +98,10 @@ def fp9_value(sign, body):
     return np.where(sign != 0, -mag, mag)
 
 
-def fp9_encode(x):
-    """Encode fp32 values to fp9: returns (sign u8, body u8, range_error bool).
+_BLOCK = 1 << 20   # elements per block of the elementwise codec (memory only)
 
-    Round to nearest, ties to even (R4), in exact float64 arithmetic: an fp32
-    value and every fp9 value and midpoint are exact in float64.
 
-    Steps: take the binade exponent e = floor(log2 |x|), clamped below at -14
-    (the subnormal range shares the spacing of the lowest normal binade); the
-    fp9 spacing there is 2**(e - 3); round |x| to a whole number q of spacings
-    (numpy's rint rounds half to even); q < 8 with e = -14 is a subnormal;
-    q = 16 carries into the next binade.
-    """
-    x = np.asarray(x, dtype=np.float32)
+def _encode_block(x):
     sign = np.signbit(x).astype(np.uint8)
     a = np.abs(x.astype(np.float64))
     finite = np.isfinite(a)
@@ -133,6 +124,29 @@ def fp9_encode(x):
     body = np.where(overflow | np.isinf(a), FP9_INF_BODY, body)
     body = np.where(np.isnan(a), FP9_NAN_BODY, body)
     return sign, body.astype(np.uint8), range_error
+
+
+def fp9_encode(x):
+    """Encode fp32 values to fp9: returns (sign u8, body u8, range_error bool).
+
+    Round to nearest, ties to even (R4), in exact float64 arithmetic: an fp32
+    value and every fp9 value and midpoint are exact in float64.
+
+    Steps: take the binade exponent e = floor(log2 |x|), clamped below at -14
+    (the subnormal range shares the spacing of the lowest normal binade); the
+    fp9 spacing there is 2**(e - 3); round |x| to a whole number q of spacings
+    (numpy's rint rounds half to even); q < 8 with e = -14 is a subnormal;
+    q = 16 carries into the next binade. Elements are independent; they are
+    processed in blocks only to bound memory.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    flat = x.reshape(-1)
+    sign = np.empty(flat.shape, np.uint8)
+    body = np.empty(flat.shape, np.uint8)
+    err = np.empty(flat.shape, bool)
+    for i in range(0, flat.size, _BLOCK):
+        sign[i:i + _BLOCK], body[i:i + _BLOCK], err[i:i + _BLOCK] = _encode_block(flat[i:i + _BLOCK])
+    return sign.reshape(x.shape), body.reshape(x.shape), err.reshape(x.shape)
 
 
 def fp9_pack(w):
@@ -158,11 +172,26 @@ def fp9_unpack_signs(sign, cols):
     return (sign[:, byte] >> bit[None, :]) & 1
 
 
+_VALUE_OF_CODE = None
+
+
 def fp9_decode(body, sign):
-    """Decode packed planes to float64 [rows, cols] [MEMOIR-FP9]."""
+    """Decode packed planes to float64 [rows, cols] [MEMOIR-FP9].
+
+    Each weight's 9-bit code (sign << 8 | body) is looked up in the table of
+    fp9_value() over all 512 codes, i.e. the closed form per weight."""
+    global _VALUE_OF_CODE
+    if _VALUE_OF_CODE is None:
+        codes = np.arange(512)
+        _VALUE_OF_CODE = fp9_value(codes >> 8, codes & 0xFF)
     body = np.asarray(body, dtype=np.uint8)
-    cols = body.shape[1]
-    return fp9_value(fp9_unpack_signs(sign, cols), body)
+    rows, cols = body.shape
+    out = np.empty((rows, cols), np.float64)
+    step = max(1, _BLOCK // max(cols, 1))
+    for r in range(0, rows, step):
+        s = fp9_unpack_signs(np.asarray(sign)[r:r + step], cols).astype(np.int16)
+        out[r:r + step] = _VALUE_OF_CODE[(s << 8) | body[r:r + step]]
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,106 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports
+every function include/fp9moe.h declares, and its host-side argument checks
+return the documented status codes before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp9_weight_expert_gb300 import binding, build_lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "fp9moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["fp9_pack", "fp9_decode", "moe_router", "fp9_moe_forward", "fp9_dense_ffn",
+              "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
+              "fp9_selftest_timeout", "fp9_status_str"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), f"libfp9moe.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert binding.status_str(code).startswith("FP9_")
+    assert "unknown" in binding.status_str(99)
+
+
+P = 0x100000  # a fake, 256-byte aligned "device" address: never dereferenced
+
+
+def _bank(n, inter, hidden, base=P):
+    return binding.FFNBankC(n, inter, hidden, base, base, base, base, base, base)
+
+
+def _layer(**kw):
+    d = dict(hidden=256, inter=128, n_experts=8, n_groups=1, topk_groups=1, topk=2, n_shared=1,
+             route_scale=1.0)
+    d.update(kw)
+    return binding.MoELayerC(d["hidden"], d["inter"], d["n_experts"], d["n_groups"],
+                             d["topk_groups"], d["topk"], d["n_shared"], d["route_scale"],
+                             kw.get("w_router", P), kw.get("routed", _bank(d["n_experts"], d["inter"], d["hidden"])),
+                             kw.get("shared", _bank(d["n_shared"], d["inter"], d["hidden"])))
+
+
+def test_pack_decode_argument_checks(lib):
+    assert lib.fp9_pack(P, 4, 12, P, P, None, None) == binding.FP9_ERR_SHAPE
+    assert lib.fp9_pack(P, -1, 8, P, P, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_pack(None, 4, 8, P, P, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_pack(P + 4, 4, 8, P, P, None, None) == binding.FP9_ERR_ALIGN
+    assert lib.fp9_pack(None, 0, 8, None, None, None, None) == binding.FP9_OK   # empty: no-op
+    assert lib.fp9_decode(P, P, 4, 12, P, None) == binding.FP9_ERR_SHAPE
+    assert lib.fp9_decode(P, P, 4, 8, P + 8, None) == binding.FP9_ERR_ALIGN
+
+
+def _fwd(lib, layer, bsz=1, x=P, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 30):
+    return lib.fp9_moe_forward(ctypes.byref(layer), x, bsz, y, None, None, ws, ws_bytes, None, None)
+
+
+def test_moe_forward_argument_checks(lib):
+    assert lib.fp9_moe_forward(None, P, 1, P, None, None, P, 1, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert _fwd(lib, _layer(), bsz=0) == binding.FP9_ERR_INVALID_ARG
+    assert _fwd(lib, _layer(), bsz=9) == binding.FP9_ERR_INVALID_ARG
+    assert _fwd(lib, _layer(hidden=200, routed=_bank(8, 128, 200), shared=_bank(1, 128, 200))) \
+        == binding.FP9_ERR_SHAPE
+    assert _fwd(lib, _layer(hidden=7296, routed=_bank(8, 128, 7296), shared=_bank(1, 128, 7296))) \
+        == binding.FP9_ERR_SHAPE
+    assert _fwd(lib, _layer(n_groups=3)) == binding.FP9_ERR_SHAPE        # 8 % 3 != 0
+    assert _fwd(lib, _layer(topk=17)) == binding.FP9_ERR_SHAPE
+    assert _fwd(lib, _layer(n_groups=4, topk_groups=1, topk=3)) == binding.FP9_ERR_SHAPE
+    assert _fwd(lib, _layer(routed=_bank(7, 128, 256))) == binding.FP9_ERR_SHAPE
+    assert _fwd(lib, _layer(routed=_bank(8, 128, 256, base=P + 8))) == binding.FP9_ERR_ALIGN
+    assert _fwd(lib, _layer(w_router=P + 4)) == binding.FP9_ERR_ALIGN
+    assert _fwd(lib, _layer(), x=P + 4) == binding.FP9_ERR_ALIGN
+    assert _fwd(lib, _layer(), y=P) == binding.FP9_ERR_INVALID_ARG       # y aliases x
+    assert _fwd(lib, _layer(), ws=P + 16) == binding.FP9_ERR_ALIGN
+    assert lib.fp9_moe_workspace_bytes(ctypes.byref(_layer(topk=17)), 1) == 0
+
+
+def test_dense_and_norm_argument_checks(lib):
+    b = _bank(2, 64, 256)
+    assert lib.fp9_dense_ffn(ctypes.byref(b), P, 1, P + 4096, P, 1 << 20, None, None) == binding.FP9_ERR_SHAPE
+    b = _bank(1, 64, 256)
+    assert lib.fp9_dense_ffn(ctypes.byref(b), P, 1, P, P, 1 << 20, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_residual_rmsnorm(P, None, P, 1, 6, ctypes.c_float(1e-6), None) == binding.FP9_ERR_SHAPE
+    assert lib.fp9_residual_rmsnorm(P, None, P, 0, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_residual_rmsnorm(P + 4, None, P, 1, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_ALIGN
+    assert lib.fp9_selftest_timeout(P, 1 << 20, None, 100, None) == binding.FP9_ERR_INVALID_ARG

@@ -1,0 +1,85 @@
+"""GPU parity for fp9_dense_ffn (the model's dense first layers) and for the
+layer stack glue (residual add + RMSNorm between MoE layers)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fp9_weight_expert_gb300 import FFNBank, Workspace, binding, synth
+from tests import support
+
+
+pytestmark = pytest.mark.gpu
+
+
+def _dense(hidden, inter, base):
+    f = FFNBank(1, inter, hidden)
+    planes = []
+    for m in range(3):
+        w = synth.ffn_weight(None, inter, hidden, synth.seed_for(base, 0, synth.DENSE, 0, m), "cuda")
+        f.pack(0, m, w)
+        body, sign, err = O.fp9_pack(w.cpu().numpy())
+        planes += [body, sign]
+    return f, tuple(planes)
+
+
+@pytest.mark.parametrize("hidden,inter", [(512, 333), (256, 4), (7168, 18432)])
+@pytest.mark.parametrize("bsz", [1, 2, 5])
+def test_dense_ffn_matches_oracle(hidden, inter, bsz):
+    if hidden == 7168 and bsz == 5:
+        pytest.skip("full-size dense layer is checked at bsz 1 and 2")
+    f, planes = _dense(hidden, inter, base=hidden + inter)
+    x = synth.tokens(bsz, hidden, synth.seed_for(9, 0, synth.TOKENS, bsz), "cuda")
+    y = torch.empty_like(x)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.fp9_dense_ffn(f, x, y, Workspace.for_dense(f, bsz).tensor, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = O.dense_ffn(x.cpu().numpy(), planes)
+    assert support.max_rel_err(y.cpu().numpy(), ref) <= support.TOL
+
+
+@pytest.mark.parametrize("bsz", [1, 3, 8])
+def test_residual_rmsnorm_matches_oracle(bsz):
+    h = synth.tokens(bsz, 7168, 5, "cuda") * 3.0
+    y = synth.tokens(bsz, 7168, 6, "cuda")
+    h0 = h.clone()
+    x = torch.empty_like(h)
+    binding.fp9_residual_rmsnorm(h, y, x, 1e-6)
+    torch.cuda.synchronize()
+    hr = h0.cpu().numpy().astype(np.float64) + y.cpu().numpy()
+    assert np.allclose(h.cpu().numpy(), hr, rtol=1e-6, atol=1e-6)
+    ref = O.rmsnorm(hr, 1e-6)
+    assert support.max_rel_err(x.cpu().numpy(), ref) <= 1e-5
+    x2 = torch.empty_like(h)
+    binding.fp9_residual_rmsnorm(h, None, x2, 1e-6)   # norm only
+    torch.cuda.synchronize()
+    assert support.max_rel_err(x2.cpu().numpy(), ref) <= 1e-5
+
+
+def test_stack_of_three_layers_matches_oracle():
+    shape, bsz = synth.TINY, 2
+    Ls = [support.build_layer(shape, base=50, layer=l) for l in range(3)]
+    Os = [support.OracleLayer(shape, base=50, layer=l) for l in range(3)]
+    h = support.safe_tokens(shape, Os[0].w_router, bsz, 51, device="cuda") * 2.0
+    h_in = h.cpu().numpy().astype(np.float64)
+    x = torch.empty_like(h)
+    y = torch.empty_like(h)
+    ws = Workspace.for_moe(Ls[0], bsz)
+    binding.fp9_residual_rmsnorm(h, None, x)
+    checked = 0
+    for l in range(3):
+        xr = x.cpu().numpy()
+        binding.fp9_moe_forward(Ls[l], x, y, ws.tensor)
+        torch.cuda.synchronize()
+        # teacher-forced: the oracle takes this layer's GPU input
+        if np.all(Os[l].margin(xr) >= support.MARGIN_MIN):
+            ref = O.moe(xr, **Os[l].kwargs())
+            assert support.max_rel_err(y.cpu().numpy(), ref) <= support.TOL
+            checked += 1
+        binding.fp9_residual_rmsnorm(h, y, x)
+    torch.cuda.synchronize()
+    assert checked >= 1
+    ref_h = O.stack(h_in, [o.kwargs() for o in Os])
+    assert support.max_rel_err(h.cpu().numpy(), ref_h) <= 1e-3   # end-to-end drift
