@@ -35,11 +35,13 @@ FP9_BYTES_PER_WEIGHT = 9.0 / 8.0
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=100)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--bsz", type=int, default=1)
     p.add_argument("--layers", type=int, default=4, help="resident layers rotated per step")
+    p.add_argument("--experts", type=int, default=256,
+                   help="routed experts per layer (smaller layers for profiling captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the bsz-2 / dense side runs")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
@@ -59,7 +61,7 @@ def _peaks():
 # ------------------------------------------------------------ clock sampler
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -85,23 +87,33 @@ class ClockSampler:
             out, _ = self.proc.communicate()
         self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and active throttle reasons over samples taken
+        between host times t0 and t1 (the nearest sample if none fell inside)."""
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), float(f[3]), f[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:
+            inside = [min(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[4]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": inside[0][2] if inside else None,
+                "power_w_max": max(r[3] for r in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
 # ----------------------------------------------------------- native bench
@@ -126,6 +138,9 @@ def _native(args):
     binding.load()
 
     shape = synth.DSV3
+    if args.experts != shape.n_experts:
+        import dataclasses
+        shape = dataclasses.replace(shape, n_experts=args.experts)
     H, I, bsz = shape.hidden, shape.inter, args.bsz
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -161,18 +176,23 @@ def _native(args):
     torch.cuda.synchronize()
 
     ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev_k:  # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    t_region0 = time.time()
     start.record(stream)
     for i in range(K):
         binding.fp9_profile_events(ev_k[i][0], ev_k[i][1])
         step(W + i, ids[i])
     stop.record(stream)
     torch.cuda.synchronize()
+    t_region1 = time.time()
     binding.fp9_profile_events(None, None)
     if world > 1:
         dist.barrier()
@@ -230,7 +250,7 @@ def _native(args):
     if rank != 0:
         return None
     value = world * bsz * K / (elapsed_ms / 1e3)
-    clocks = sampler.summary()
+    clocks = sampler.summary(t_region0, t_region1)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -245,8 +265,9 @@ def _native(args):
         "dtype": "f32",
         "data": "synthetic (seeded N(0,0.02) weights packed to fp9 on the GPU, N(0,1) tokens)",
         "config": {
-            "workload": "one DeepSeek-V3 MoE layer, bsz 1: hidden 7168, 256 routed experts "
-                        "(8 groups x 32, top-4 groups, top-8) + 1 shared, intermediate 2048, fp9 weights",
+            "workload": f"one DeepSeek-V3 MoE layer, bsz {bsz}: hidden 7168, {shape.n_experts} routed experts "
+                        f"(8 groups x {shape.n_experts // 8}, top-4 groups, top-8) + 1 shared, "
+                        "intermediate 2048, fp9 weights",
             "bsz": bsz,
             "resident_layers": len(Ls),
             "l2": "inputs larger than L2: 4 resident layers (12.7 GB each) rotate, each step streams "

@@ -205,6 +205,9 @@ def fp9_selftest_timeout(ws: torch.Tensor, status: torch.Tensor, timeout_us: int
 
 def fp9_profile_events(start, stop) -> None:
     """Brackets every later fused-kernel launch with two torch.cuda.Events
-    (recorded on the kernel's stream); (None, None) turns it off."""
+    (recorded on the kernel's stream); (None, None) turns it off. Each event
+    must have been recorded once, so that torch has created it."""
+    if start is not None and (start.cuda_event == 0 or stop.cuda_event == 0):
+        raise ValueError("record each event once before passing it (torch creates it lazily)")
     load().fp9_profile_events(start.cuda_event if start is not None else None,
                               stop.cuda_event if stop is not None else None)

@@ -26,48 +26,41 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t bits) {
     return __half22float2(h);
 }
 
-// Decode 16 consecutive weights: `body` holds their body bytes (byte i of
-// the 16 = column i), `s16` their 16 sign bits (bit i = column i).
-//
-// Each 32-bit body word k holds columns 4k..4k+3. Two fp16 values are built
-// per instruction pair as a half2: (4k, 4k+2) and (4k+1, 4k+3). The body
-// bytes are moved to the high byte of each 16-bit half and shifted right by
-// one (= body << 7 inside the half). The sign bits are moved to bits 15 and
-// 31 by one multiply of the sign byte by a two-bit constant: the two
-// shifted copies of the byte do not overlap, so no carry crosses them.
-__device__ __forceinline__ void decode16(const uint4 body, uint32_t s16, float w[16]) {
+// fp9 -> fp16 bits for pairs of weights. For 4 weights in one body word,
+// their 4 sign bits are first spread to the low bit of 4 bytes (one
+// multiply by a constant with bits at 0, 7, 14, 21: the shifted copies of a
+// 4-bit value never overlap, so no carry crosses them). One byte permute
+// then builds, in each 16-bit half, [sign byte (0 or 1)][body byte]: the
+// 9-bit fp9 code s eeeee mmm. Shifting it left by 7 (a multiply by 128,
+// which keeps the two halves apart because bits 9..15 of each half are 0)
+// gives the fp16 bits s eeeee mmm 0000000 of the same value.
+__device__ __forceinline__ uint32_t spread_sign_nibble(uint32_t nibble) {
+    return (nibble * 0x00204081u) & 0x01010101u;
+}
+
+// Decode 16 consecutive weights into 8 pairs in "pair order":
+// p[2k] = (w[4k], w[4k+2]) and p[2k+1] = (w[4k+1], w[4k+3]), the order in
+// which each half2 is built (callers keep x and y in the same order).
+// `body` holds the 16 body bytes (byte i = column i), `s16` the 16 sign
+// bits (bit i = column i).
+__device__ __forceinline__ void decode16_pairs(const uint4 body, uint32_t s16, float2 p[8]) {
     const uint32_t words[4] = {body.x, body.y, body.z, body.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint32_t s8 = (k < 2) ? (s16 & 0xFFu) : (s16 >> 8);
-        const int i = (k & 1) * 4;  // column of word k's first weight inside its sign byte
-        uint32_t a = __byte_perm(words[k], 0u, 0x2404u) >> 1;     // cols 4k, 4k+2
-        uint32_t b = (words[k] & 0xFF00FF00u) >> 1;               // cols 4k+1, 4k+3
-        const uint32_t ma = s8 * ((1u << (15 - i)) + (1u << (29 - i)));
-        const uint32_t mb = s8 * ((1u << (14 - i)) + (1u << (28 - i)));
-        a |= ma & 0x80008000u;
-        b |= mb & 0x80008000u;
-        const float2 fa = half2_bits_to_float2(a);
-        const float2 fb = half2_bits_to_float2(b);
-        w[4 * k + 0] = fa.x;
-        w[4 * k + 2] = fa.y;
-        w[4 * k + 1] = fb.x;
-        w[4 * k + 3] = fb.y;
+        const uint32_t e = spread_sign_nibble((s16 >> (4 * k)) & 0xFu);
+        p[2 * k] = half2_bits_to_float2(__byte_perm(words[k], e, 0x6240u) * 128u);      // cols 4k, 4k+2
+        p[2 * k + 1] = half2_bits_to_float2(__byte_perm(words[k], e, 0x7351u) * 128u);  // cols 4k+1, 4k+3
     }
 }
 
-// Decode 8 consecutive weights from two body words and one sign byte.
+// Decode 8 consecutive weights (two body words, one sign byte) in column order.
 __device__ __forceinline__ void decode8(uint32_t w0, uint32_t w1, uint32_t s8, float w[8]) {
     const uint32_t words[2] = {w0, w1};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const int i = k * 4;
-        uint32_t a = __byte_perm(words[k], 0u, 0x2404u) >> 1;
-        uint32_t b = (words[k] & 0xFF00FF00u) >> 1;
-        a |= (s8 * ((1u << (15 - i)) + (1u << (29 - i)))) & 0x80008000u;
-        b |= (s8 * ((1u << (14 - i)) + (1u << (28 - i)))) & 0x80008000u;
-        const float2 fa = half2_bits_to_float2(a);
-        const float2 fb = half2_bits_to_float2(b);
+        const uint32_t e = spread_sign_nibble((s8 >> (4 * k)) & 0xFu);
+        const float2 fa = half2_bits_to_float2(__byte_perm(words[k], e, 0x6240u) * 128u);
+        const float2 fb = half2_bits_to_float2(__byte_perm(words[k], e, 0x7351u) * 128u);
         w[4 * k + 0] = fa.x;
         w[4 * k + 2] = fa.y;
         w[4 * k + 1] = fb.x;

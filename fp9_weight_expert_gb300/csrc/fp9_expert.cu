@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "fp9_device.cuh"
 #include "fp9_host.h"
@@ -36,11 +37,11 @@
 
 namespace fp9 {
 
-constexpr int kR = 4;                                           // rows per chunk
+constexpr int kMaxRows = 8;                                     // rows per chunk (4 or 8)
 constexpr int kMaxStages = 16;
 constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / 16 / 32;     // 14
 constexpr int kMaxThreads = kMaxConsumerWarps * 32 + 32;        // 480
-constexpr int kMaxV = 2 * kR * kTokensPerJob;                   // reduced values per chunk
+constexpr int kMaxV = 2 * kMaxRows * kTokensPerJob;             // reduced values per chunk
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;           // 1 s
 
 struct BankPtrs {
@@ -92,9 +93,19 @@ __device__ __forceinline__ Job get_job(const Job* jobs, int32_t dense_jobs, int3
     return jobs[j];
 }
 
-__device__ __forceinline__ int64_t min3(int64_t a, int64_t b, int64_t c) {
-    const int64_t m = a < b ? a : b;
-    return m < c ? m : c;
+// Rows [start, end) of the job sequence owned by CTA b. Only the first
+// min(G, N) CTAs get rows, so every CTA that works owns at least one row.
+struct Range {
+    int64_t start, end, n, g;
+};
+
+__device__ __forceinline__ Range cta_range(int32_t J, int64_t I, int64_t grid, int64_t b) {
+    Range r;
+    r.n = static_cast<int64_t>(J) * I;
+    r.g = r.n < grid ? r.n : grid;
+    r.start = b < r.g ? cta_start(b, r.n, r.g) : 0;
+    r.end = b < r.g ? cta_start(b + 1, r.n, r.g) : 0;
+    return r;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -119,47 +130,95 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
     return r;
 }
 
-__device__ __forceinline__ void load_row16(const uint8_t* st, int H, int rr, int c16, uint4& body,
-                                           uint32_t& s16) {
-    body = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
-    s16 = *reinterpret_cast<const uint16_t*>(st + kR * H + rr * (H / 8) + c16 * 2);
-}
+
+// The walk over a CTA's rows, one chunk of at most R rows at a time (a
+// chunk never crosses a job boundary). Producer and consumers walk the
+// same sequence.
+struct Walk {
+    int64_t pos, end, I, r0;
+    int j;
+    int rows;  // rows of the current chunk
+
+    __device__ __forceinline__ void begin(const Range& rg, int64_t I_, int R) {
+        I = I_;
+        pos = rg.start;
+        end = rg.end;
+        j = static_cast<int>(pos / I);
+        r0 = pos - static_cast<int64_t>(j) * I;
+        set_rows(R);
+    }
+    __device__ __forceinline__ void set_rows(int R) {
+        int r = R;
+        if (I - r0 < r) r = static_cast<int>(I - r0);
+        if (end - pos < r) r = static_cast<int>(end - pos);
+        rows = r;
+    }
+    __device__ __forceinline__ bool done() const { return pos >= end; }
+    // Advances past the current chunk; returns true when the next chunk
+    // starts a new job.
+    __device__ __forceinline__ bool next(int R) {
+        pos += rows;
+        r0 += rows;
+        bool new_job = false;
+        if (r0 == I && pos < end) {
+            ++j;
+            r0 = 0;
+            new_job = true;
+        }
+        set_rows(R);
+        return new_job;
+    }
+};
 
 // ------------------------------------------------------------- producer ---
 
-__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, int64_t start, int64_t end,
+// Streams, per chunk c, its gate rows, its up rows, then the down rows of
+// chunk c - 1 (the consumers use chunk c - 1's down rows while chunk c's
+// gate/up sums are being reduced across the CTA); the last chunk's down
+// rows come after the loop.
+template <int R>
+__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const Range& rg,
                          uint32_t stage_bytes) {
     const uint64_t pol = l2_evict_first_policy();
     const int H = a.H;
-    const int64_t I = a.I;
     const uint32_t NS = static_cast<uint32_t>(a.nstages);
     uint32_t it = 0;
     bool ok = true;
-    for (int64_t pos = start; pos < end && ok;) {
-        const int j = static_cast<int>(pos / I);
-        const int64_t r0 = pos - static_cast<int64_t>(j) * I;
-        const int rows = static_cast<int>(min3(kR, I - r0, end - pos));
-        const Job job = get_job(a.jobs, a.dense_jobs, a.bsz, j);
+
+    auto issue = [&](int m, const Job& job, int64_t r0, int rows) -> bool {
+        const uint32_t slot = it % NS, ph = (it / NS) & 1u;
+        if (!mbar_wait_bounded(smem_addr(&ctl.empty[slot]), ph ^ 1u, a.timeout_ns, &ctl.abort)) return false;
         const BankPtrs& bp = a.bank[job.bank];
-        const int64_t row = static_cast<int64_t>(job.expert) * I + r0;
+        const int64_t row = static_cast<int64_t>(job.expert) * a.I + r0;
         const uint32_t bb = static_cast<uint32_t>(rows * H), sb = static_cast<uint32_t>(rows * (H / 8));
-        for (int m = 0; m < 3; ++m) {
-            const uint32_t slot = it % NS, ph = (it / NS) & 1u;
-            if (!mbar_wait_bounded(smem_addr(&ctl.empty[slot]), ph ^ 1u, a.timeout_ns, &ctl.abort)) {
-                ok = false;
-                break;
-            }
-            const uint32_t full = smem_addr(&ctl.full[slot]);
-            const uint32_t dst = smem_addr(ring + slot * stage_bytes);
-            if (!a.no_copy) {
-                mbar_arrive_expect_tx(full, bb + sb);
-                bulk_g2s(dst, bp.body[m] + row * H, bb, full, pol);
-                bulk_g2s(dst + kR * H, bp.sign[m] + row * (H / 8), sb, full, pol);
-            }
-            ++it;
+        const uint32_t full = smem_addr(&ctl.full[slot]);
+        const uint32_t dst = smem_addr(ring + slot * stage_bytes);
+        if (!a.no_copy) {
+            mbar_arrive_expect_tx(full, bb + sb);
+            bulk_g2s(dst, bp.body[m] + row * H, bb, full, pol);
+            bulk_g2s(dst + R * H, bp.sign[m] + row * (H / 8), sb, full, pol);
         }
-        pos += rows;
+        ++it;
+        return true;
+    };
+
+    Walk w;
+    w.begin(rg, a.I, R);
+    Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
+    Job pjob = job;
+    int64_t pr0 = 0;
+    int prows = 0;
+    bool pending = false;
+    while (!w.done() && ok) {
+        ok = issue(0, job, w.r0, w.rows) && issue(1, job, w.r0, w.rows);
+        if (ok && pending) ok = issue(2, pjob, pr0, prows);
+        pjob = job;
+        pr0 = w.r0;
+        prows = w.rows;
+        pending = true;
+        if (w.next(R)) job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
     }
+    if (ok && pending) ok = issue(2, pjob, pr0, prows);
     if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
         ctl.abort = 1;
@@ -173,189 +232,262 @@ __device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, int64
 
 // ------------------------------------------------------------- consumer ---
 
-struct ConsumerState {
-    uint32_t it = 0;      // stages consumed
-    uint32_t red_it = 0;  // CTA reductions done
+// x and y of a thread's 16 columns, per token, in the pair order of
+// decode16_pairs: p[2k] = (c[4k], c[4k+2]), p[2k+1] = (c[4k+1], c[4k+3]).
+template <int MT>
+struct Cols {
+    float2 p[MT][8];
 };
 
-// One chunk of `rows` rows for a job of T tokens. Returns false on timeout.
-template <int T>
-__device__ __forceinline__ bool run_chunk(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
-                                          uint32_t stage_bytes, ConsumerState& cs, int rows, int c16,
-                                          bool active, const Job& job, const float (&xr)[kTokensPerJob][16],
-                                          float (&yr)[kTokensPerJob][16], int NW, int warp, int lane) {
-    constexpr int V = 2 * kR * T;
-    const int H = a.H;
-    const uint32_t NS = static_cast<uint32_t>(a.nstages);
-    float v[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) v[i] = 0.0f;
+struct Stages {
+    uint32_t it = 0;      // stages consumed
+    uint32_t red_it = 0;  // CTA reductions started
+};
 
-    // gate (m = 0) and up (m = 1): partial dot products over my 16 columns
+__device__ __forceinline__ bool wait_stage(const ExpertArgs& a, SmemCtl& ctl, const Stages& cs, uint32_t& slot) {
+    const uint32_t NS = static_cast<uint32_t>(a.nstages);
+    slot = cs.it % NS;
+    return mbar_wait_bounded(smem_addr(&ctl.full[slot]), (cs.it / NS) & 1u, a.timeout_ns, &ctl.abort);
+}
+
+__device__ __forceinline__ void release_stage(SmemCtl& ctl, Stages& cs, uint32_t slot, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[slot]));
+    ++cs.it;
+}
+
+// Partial dot products of the stage's `rows` rows with x over my 16
+// columns, then their warp-level reduce-scatter into red_row[base + ...].
+template <int R, int T, int MT>
+__device__ __forceinline__ void gateup_rows(const uint8_t* st, int H, int rows, int c16, bool active,
+                                            const Cols<MT>& x, float* red_row, int base, int lane) {
+    float v[R * T];
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const uint32_t slot = cs.it % NS, ph = (cs.it / NS) & 1u;
-        if (!mbar_wait_bounded(smem_addr(&ctl.full[slot]), ph, a.timeout_ns, &ctl.abort)) return false;
-        const uint8_t* st = ring + slot * stage_bytes;
-        if (active) {
+    for (int i = 0; i < R * T; ++i) v[i] = 0.0f;
+    if (active) {
 #pragma unroll
-            for (int rr = 0; rr < kR; ++rr) {
-                if (rr < rows) {
-                    uint4 b;
-                    uint32_t s16;
-                    load_row16(st, H, rr, c16, b, s16);
-                    float w[16];
-                    decode16(b, s16, w);
+        for (int rr = 0; rr < R; ++rr) {
+            if (rr < rows) {
+                const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
+                const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
+                float2 w[8];
+                decode16_pairs(b, s16, w);
 #pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        float p0 = 0.0f, p1 = 0.0f;
+                for (int t = 0; t < T; ++t) {
+                    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            p0 = fmaf(w[i], xr[t][i], p0);
-                            p1 = fmaf(w[i + 1], xr[t][i + 1], p1);
-                        }
-                        v[m * kR * T + rr * T + t] = p0 + p1;
+                    for (int k = 0; k < 8; ++k) {
+                        a0 = fmaf(w[k].x, x.p[t][k].x, a0);
+                        a1 = fmaf(w[k].y, x.p[t][k].y, a1);
                     }
+                    v[rr * T + t] = a0 + a1;
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[slot]));
-        ++cs.it;
     }
+    const float r = warp_reduce_scatter<R * T>(v, lane);
+    if (lane < R * T) red_row[base + lane] = r;
+}
 
-    // CTA-wide sums of the 2 * kR * T values, in a fixed order
-    const float r = warp_reduce_scatter<V>(v, lane);
-    const uint32_t b = cs.red_it & 1u, rph = (cs.red_it >> 1) & 1u;
-    if (lane < V) ctl.red_vals[b][warp][lane] = r;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&ctl.red[b]));
-    if (!mbar_wait_bounded(smem_addr(&ctl.red[b]), rph, a.timeout_ns, &ctl.abort)) return false;
-    ++cs.red_it;
-    float tot = 0.0f;
-    if (lane < V)
-        for (int w = 0; w < NW; ++w) tot += ctl.red_vals[b][w][lane];
-    const float u = __shfl_down_sync(0xFFFFFFFFu, tot, kR * T);
-    float hv = 0.0f;
-    const float wt = (T == 2 && (lane & 1)) ? job.w[1] : job.w[0];
-    if (lane < kR * T) hv = silu(tot) * u * wt;
-    float h[kR][T];
+// y[c] += h_row * W_down^T[row, c] over my 16 columns; lane (rr * T + t)
+// of `hv` holds h of row rr, token t.
+template <int R, int T, int MT>
+__device__ __forceinline__ void down_rows(const uint8_t* st, int H, int rows, int c16, bool active, float hv,
+                                          Cols<MT>& y) {
+    float h[R][T];
 #pragma unroll
-    for (int rr = 0; rr < kR; ++rr)
+    for (int rr = 0; rr < R; ++rr)
 #pragma unroll
         for (int t = 0; t < T; ++t) h[rr][t] = __shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
-
-    // down rows: y[c] += h_row * W_down^T[row, c] over my 16 columns
-    {
-        const uint32_t slot = cs.it % NS, ph = (cs.it / NS) & 1u;
-        if (!mbar_wait_bounded(smem_addr(&ctl.full[slot]), ph, a.timeout_ns, &ctl.abort)) return false;
-        const uint8_t* st = ring + slot * stage_bytes;
-        if (active) {
+    if (!active) return;
 #pragma unroll
-            for (int rr = 0; rr < kR; ++rr) {
-                if (rr < rows) {
-                    uint4 bb;
-                    uint32_t s16;
-                    load_row16(st, H, rr, c16, bb, s16);
-                    float w[16];
-                    decode16(bb, s16, w);
+    for (int rr = 0; rr < R; ++rr) {
+        if (rr < rows) {
+            const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
+            const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
+            float2 w[8];
+            decode16_pairs(b, s16, w);
 #pragma unroll
-                    for (int t = 0; t < T; ++t)
+            for (int t = 0; t < T; ++t)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) yr[t][i] = fmaf(h[rr][t], w[i], yr[t][i]);
+                for (int k = 0; k < 8; ++k) {
+                    y.p[t][k].x = fmaf(h[rr][t], w[k].x, y.p[t][k].x);
+                    y.p[t][k].y = fmaf(h[rr][t], w[k].y, y.p[t][k].y);
                 }
-            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[slot]));
-        ++cs.it;
     }
+}
+
+// Gate and up stages of one chunk: waits, computes, releases, and writes
+// this warp's reduced values for the chunk's CTA sum. Returns false on timeout.
+template <int R, int T, int MT>
+__device__ __forceinline__ bool gateup_chunk(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
+                                             uint32_t stage_bytes, Stages& cs, int rows, int c16, bool active,
+                                             const Cols<MT>& x, int warp, int lane) {
+    float* red_row = ctl.red_vals[cs.red_it & 1u][warp];
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+        uint32_t slot;
+        if (!wait_stage(a, ctl, cs, slot)) return false;
+        gateup_rows<R, T, MT>(ring + slot * stage_bytes, a.H, rows, c16, active, x, red_row, m * R * T, lane);
+        release_stage(ctl, cs, slot, lane);
+    }
+    if (lane == 0) mbar_arrive(smem_addr(&ctl.red[cs.red_it & 1u]));
     return true;
 }
 
-__device__ __forceinline__ void flush_partial(const ExpertArgs& a, const Job& job, int64_t seg, int c16,
-                                              bool active, const float (&yr)[kTokensPerJob][16]) {
+template <int R, int T, int MT>
+__device__ __forceinline__ bool down_chunk(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
+                                           uint32_t stage_bytes, Stages& cs, int rows, int c16, bool active,
+                                           float hv, Cols<MT>& y, int lane) {
+    uint32_t slot;
+    if (!wait_stage(a, ctl, cs, slot)) return false;
+    down_rows<R, T, MT>(ring + slot * stage_bytes, a.H, rows, c16, active, hv, y);
+    release_stage(ctl, cs, slot, lane);
+    return true;
+}
+
+// Completes the CTA sum of chunk `red_it` and returns, in lane
+// (rr * T + t), h = SiLU(g) * u * w_route for row rr, token t.
+template <int R, int T>
+__device__ __forceinline__ bool finish_sum(const ExpertArgs& a, SmemCtl& ctl, Stages& cs, const Job& job, int NW,
+                                           int lane, float& hv) {
+    constexpr int V = R * T;
+    const uint32_t b = cs.red_it & 1u;
+    if (!mbar_wait_bounded(smem_addr(&ctl.red[b]), (cs.red_it >> 1) & 1u, a.timeout_ns, &ctl.abort)) return false;
+    ++cs.red_it;
+    float tot = 0.0f;
+    if (lane < 2 * V)
+        for (int w = 0; w < NW; ++w) tot += ctl.red_vals[b][w][lane];
+    const float u = __shfl_down_sync(0xFFFFFFFFu, tot, V);
+    const float wt = (T == 2 && (lane & 1)) ? job.w[1] : job.w[0];
+    hv = (lane < V) ? silu(tot) * u * wt : 0.0f;
+    return true;
+}
+
+template <int MT>
+__device__ __forceinline__ void flush_partial(const ExpertArgs& a, int ntok, int64_t seg, int c16, bool active,
+                                              const Cols<MT>& y) {
     if (!active) return;
 #pragma unroll
-    for (int t = 0; t < kTokensPerJob; ++t) {
-        if (t < job.ntok) {
+    for (int t = 0; t < MT; ++t) {
+        if (t < ntok) {
             float4* dst = reinterpret_cast<float4*>(
                 a.partial + ((static_cast<int64_t>(blockIdx.x) * a.maxseg + seg) * kTokensPerJob + t) * a.H +
                 c16 * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                dst[q] = make_float4(yr[t][4 * q], yr[t][4 * q + 1], yr[t][4 * q + 2], yr[t][4 * q + 3]);
+            for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(y.p[t][2 * k].x, y.p[t][2 * k + 1].x, y.p[t][2 * k].y, y.p[t][2 * k + 1].y);
         }
     }
 }
 
-__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring, int64_t start, int64_t end,
+template <int MT>
+__device__ __forceinline__ void load_x(const ExpertArgs& a, const Job& job, int c16, bool active, Cols<MT>& x) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const bool use = active && t < job.ntok;
+        const int tok = t == 0 ? job.tok[0] : job.tok[1];
+        const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H + c16 * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 xv = use ? __ldg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x.p[t][2 * k] = make_float2(xv.x, xv.z);
+            x.p[t][2 * k + 1] = make_float2(xv.y, xv.w);
+        }
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void zero_cols(Cols<MT>& y) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y.p[t][k] = make_float2(0.f, 0.f);
+}
+
+// Per chunk c: gate/up of c, arrive at c's CTA sum, down rows of c - 1
+// (whose h is known), then wait for c's sum. x follows the gate/up job, y
+// the down job; y is written out (and cleared) after the last down chunk
+// of each job.
+template <int R, int MT>
+__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring, const Range& rg,
                          uint32_t stage_bytes, int NW, int warp, int lane) {
-    const int H = a.H;
-    const int64_t I = a.I;
     const int c16 = warp * 32 + lane;
-    const bool active = c16 < H / 16;
-    float xr[kTokensPerJob][16], yr[kTokensPerJob][16];
-    Job job;
-    job.ntok = 0;
-    int cur = -1;
-    int64_t seg = 0;
-    const int64_t job0 = start / I;
-    ConsumerState cs;
+    const bool active = c16 < a.H / 16;
+    Cols<MT> x, y;
+    Walk w;
+    w.begin(rg, a.I, R);
+    const int j0 = w.j;
+    Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
+    load_x(a, job, c16, active, x);
+    zero_cols(y);
+    Stages cs;
     bool ok = true;
-    for (int64_t pos = start; pos < end;) {
-        const int j = static_cast<int>(pos / I);
-        const int64_t r0 = pos - static_cast<int64_t>(j) * I;
-        const int rows = static_cast<int>(min3(kR, I - r0, end - pos));
-        if (j != cur) {
-            if (cur >= 0) flush_partial(a, job, seg, c16, active, yr);
-            cur = j;
-            job = get_job(a.jobs, a.dense_jobs, a.bsz, j);
-            seg = j - job0;
-#pragma unroll
-            for (int t = 0; t < kTokensPerJob; ++t) {
-                const bool use = active && t < job.ntok;
-                const int tok = t == 0 ? job.tok[0] : job.tok[1];
-                const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * H + c16 * 16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 xv = use ? __ldg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    xr[t][4 * q] = xv.x;
-                    xr[t][4 * q + 1] = xv.y;
-                    xr[t][4 * q + 2] = xv.z;
-                    xr[t][4 * q + 3] = xv.w;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) yr[t][i] = 0.0f;
+    // the chunk whose down rows are pending
+    bool pending = false;
+    int p_rows = 0, p_ntok = 1, p_seg = 0;
+    bool p_last_of_job = false;
+    float p_hv = 0.0f;
+
+    while (!w.done()) {
+        const int T = MT == 1 ? 1 : job.ntok;
+        ok = (T == 2) ? gateup_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane)
+                      : gateup_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane);
+        if (!ok) break;
+        if (pending) {
+            ok = (p_ntok == 2)
+                     ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
+                     : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
+            if (!ok) break;
+            if (p_last_of_job) {
+                flush_partial(a, p_ntok, p_seg, c16, active, y);
+                zero_cols(y);
             }
         }
-        ok = (job.ntok == 2)
-                 ? run_chunk<2>(a, ctl, ring, stage_bytes, cs, rows, c16, active, job, xr, yr, NW, warp, lane)
-                 : run_chunk<1>(a, ctl, ring, stage_bytes, cs, rows, c16, active, job, xr, yr, NW, warp, lane);
+        float hv;
+        ok = (T == 2) ? finish_sum<R, MT>(a, ctl, cs, job, NW, lane, hv)
+                      : finish_sum<R, 1>(a, ctl, cs, job, NW, lane, hv);
         if (!ok) break;
-        pos += rows;
+        pending = true;
+        p_rows = w.rows;
+        p_ntok = T;
+        p_seg = w.j - j0;
+        p_hv = hv;
+        const bool new_job = w.next(R);
+        p_last_of_job = new_job;
+        if (new_job) {
+            job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
+            load_x(a, job, c16, active, x);
+        }
     }
-    if (ok) {
-        if (cur >= 0) flush_partial(a, job, seg, c16, active, yr);
-    } else {
+    if (ok && pending) {
+        ok = (p_ntok == 2)
+                 ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
+                 : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
+        if (ok) flush_partial(a, p_ntok, p_seg, c16, active, y);
+    }
+    if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
         ctl.abort = 1;
     }
 }
 
+// R: rows per chunk; MT: most tokens a job can hold (1 when bsz == 1).
+template <int R, int MT>
 __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem);
     uint8_t* ring = smem + kRingOffset;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NW = static_cast<int>(blockDim.x / 32) - 1;
-    const uint32_t stage_bytes = static_cast<uint32_t>(kR * a.H / 8 * 9);
+    const uint32_t stage_bytes = static_cast<uint32_t>(R * a.H / 8 * 9);
 
-    grid_dependency_wait();  // no-op unless launched as a programmatic dependent
+    grid_dependency_wait();  // the router's job list and x are complete
+    grid_launch_dependents();
     const int32_t J = a.dense_jobs > 0 ? a.dense_jobs : a.ctl->njobs;
-    const int64_t N = static_cast<int64_t>(J) * a.I, G = gridDim.x;
-    const int64_t start = cta_start(blockIdx.x, N, G), end = cta_start(blockIdx.x + 1, N, G);
-    if (start >= end) return;
+    const Range rg = cta_range(J, a.I, gridDim.x, blockIdx.x);
+    if (rg.start >= rg.end) return;
 
     if (tid == 0) {
         for (int s = 0; s < a.nstages; ++s) {
@@ -371,10 +503,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     __syncthreads();
 
     if (warp == NW) {
-        if (lane == 0) producer(a, ctl, ring, start, end, stage_bytes);
+        if (lane == 0) producer<R>(a, ctl, ring, rg, stage_bytes);
         return;
     }
-    consumer(a, ctl, ring, start, end, stage_bytes, NW, warp, lane);
+    consumer<R, MT>(a, ctl, ring, rg, stage_bytes, NW, warp, lane);
 }
 
 // ------------------------------------------------------------- combine ----
@@ -392,52 +524,73 @@ struct CombineArgs {
     float* y;
 };
 
+constexpr int kCombineCols = 64;               // columns per CTA: 16 lanes x float4
 constexpr int kCombineWarps = 8;
+constexpr int kCombineLanes = kCombineWarps * 2;  // segment lanes: two per warp
 
 // y[t, c] = sum over the jobs holding token t, in job order, and over the
-// CTAs covering each job, in CTA order, of their partials. Warp w adds the
-// segments w, w + 8, ...; the eight warp sums are added in warp order.
+// CTAs covering each job, in CTA order, of their partials. Segment lane s
+// (= 2 * warp + half-warp) adds the segments s, s + 16, ...; the sixteen
+// lane sums are then added in lane order.
+//
+// A job's rows [jI, jI + I) are covered by CTAs b0..b1. CTA b0 may have
+// started in an earlier job, so its partial for this job is its segment
+// k0 = j - first_job(b0); every later CTA b in (b0, b1] starts inside job j
+// and holds it as its segment 0.
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
-    __shared__ float4 red[kCombineWarps][32];
+    __shared__ float4 red[kCombineLanes][16];
+    grid_dependency_wait();  // all partials are written
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int half = lane >> 4, l16 = lane & 15;
+    const int sl = warp * 2 + half;
     const int t = blockIdx.y;
-    const int c = blockIdx.x * 128 + lane * 4;
+    const int c = blockIdx.x * kCombineCols + l16 * 4;
     const int32_t J = a.dense_jobs > 0 ? a.dense_jobs : a.ctl->njobs;
-    const int64_t N = static_cast<int64_t>(J) * a.I, G = a.grid;
+    const int64_t N = static_cast<int64_t>(J) * a.I;
+    const int64_t G = N < a.grid ? N : a.grid;
+    const int64_t stride_b = static_cast<int64_t>(a.maxseg) * kTokensPerJob * a.H;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int64_t idx = 0;
     for (int j = 0; j < J; ++j) {
         const Job job = get_job(a.jobs, a.dense_jobs, a.bsz, j);
-        for (int q = 0; q < job.ntok; ++q) {
-            if ((q == 0 ? job.tok[0] : job.tok[1]) != t) continue;
-            const int64_t first_row = static_cast<int64_t>(j) * a.I;
-            const int64_t b0 = cta_of_row(first_row, N, G);
-            const int64_t b1 = cta_of_row(first_row + a.I - 1, N, G);
-            const int64_t skip = ((warp - idx) % kCombineWarps + kCombineWarps) % kCombineWarps;
-            for (int64_t b = b0 + skip; b <= b1; b += kCombineWarps) {
-                const int64_t k = j - cta_start(b, N, G) / a.I;
-                const float4 p = __ldcs(reinterpret_cast<const float4*>(
-                    a.partial + ((b * a.maxseg + k) * kTokensPerJob + q) * a.H + c));
-                acc.x += p.x;
-                acc.y += p.y;
-                acc.z += p.z;
-                acc.w += p.w;
-            }
-            idx += b1 - b0 + 1;
+        int q = -1;
+        if (job.tok[0] == t) q = 0;
+        else if (job.ntok == 2 && job.tok[1] == t) q = 1;
+        if (q < 0) continue;
+        const int64_t first_row = static_cast<int64_t>(j) * a.I;
+        const int64_t b0 = cta_of_row(first_row, N, G);
+        const int64_t b1 = cta_of_row(first_row + a.I - 1, N, G);
+        const int64_t k0 = j - cta_start(b0, N, G) / a.I;
+        const int64_t nseg = b1 - b0 + 1;
+        int64_t s = ((sl - idx) % kCombineLanes + kCombineLanes) % kCombineLanes;
+        const float* base = a.partial + (static_cast<int64_t>(q)) * a.H + c;
+#pragma unroll 4
+        for (; s < nseg; s += kCombineLanes) {
+            const int64_t b = b0 + s;
+            const int64_t k = s == 0 ? k0 : 0;
+            const float4 p = __ldcs(reinterpret_cast<const float4*>(base + b * stride_b +
+                                                                    k * kTokensPerJob * a.H));
+            acc.x += p.x;
+            acc.y += p.y;
+            acc.z += p.z;
+            acc.w += p.w;
         }
+        idx += nseg;
     }
-    red[warp][lane] = acc;
+    red[sl][l16] = acc;
     __syncthreads();
-    if (warp == 0) {
-        float4 s = red[0][lane];
-        for (int w = 1; w < kCombineWarps; ++w) {
-            const float4 o = red[w][lane];
-            s.x += o.x;
-            s.y += o.y;
-            s.z += o.z;
-            s.w += o.w;
+    if (threadIdx.x < 16) {
+        float4 sum = red[0][threadIdx.x];
+        for (int w = 1; w < kCombineLanes; ++w) {
+            const float4 o = red[w][threadIdx.x];
+            sum.x += o.x;
+            sum.y += o.y;
+            sum.z += o.z;
+            sum.w += o.w;
         }
-        reinterpret_cast<float4*>(a.y + static_cast<int64_t>(t) * a.H)[c / 4] = s;
+        reinterpret_cast<float4*>(a.y + static_cast<int64_t>(t) * a.H)[(blockIdx.x * kCombineCols) / 4 +
+                                                                       threadIdx.x] = sum;
     }
 }
 
@@ -457,21 +610,40 @@ static BankPtrs bank_ptrs(const fp9_ffn_bank& b) {
 struct LaunchShape {
     int threads;
     int nstages;
+    int rows;
     size_t smem;
 };
+
+// Rows per streamed chunk: 8 unless FP9MOE_CHUNK_ROWS=4 is set (a tuning
+// knob: 8 halves the per-chunk reduction cost, 4 allows twice the stages).
+static int chunk_rows() {
+    static int rows = 0;
+    if (rows == 0) {
+        const char* e = getenv("FP9MOE_CHUNK_ROWS");
+        rows = (e != nullptr && atoi(e) == 4) ? 4 : 8;
+    }
+    return rows;
+}
 
 static fp9_status expert_shape(int32_t H, LaunchShape& s) {
     const int nw = (H / 16 + 31) / 32;
     s.threads = nw * 32 + 32;
-    const uint32_t stage = static_cast<uint32_t>(kR * H / 8 * 9);
+    s.rows = chunk_rows();
+    const uint32_t stage = static_cast<uint32_t>(s.rows * H / 8 * 9);
     const int32_t optin = device_max_smem_optin();
     if (optin <= 0) return FP9_ERR_CUDA;
     int ns = static_cast<int>((static_cast<int64_t>(optin) - kRingOffset) / stage);
     if (ns > kMaxStages) ns = kMaxStages;
-    if (ns < 2) return FP9_ERR_SHAPE;
+    if (ns < 3) return FP9_ERR_SHAPE;
     s.nstages = ns;
     s.smem = kRingOffset + static_cast<size_t>(ns) * stage;
     return FP9_OK;
+}
+
+template <int R, int MT>
+static cudaError_t set_smem(size_t smem) {
+    return cudaFuncSetAttribute(expert_kernel<R, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
 }
 
 static fp9_status ensure_smem_attr(size_t smem) {
@@ -480,8 +652,10 @@ static fp9_status ensure_smem_attr(size_t smem) {
     FP9_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
     if (configured[dev] < smem) {
-        FP9_CUDA_TRY(cudaFuncSetAttribute(expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem)));
+        FP9_CUDA_TRY((set_smem<4, 1>(smem)));
+        FP9_CUDA_TRY((set_smem<8, 1>(smem)));
+        FP9_CUDA_TRY((set_smem<4, 2>(smem)));
+        FP9_CUDA_TRY((set_smem<8, 2>(smem)));
         configured[dev] = smem;
     }
     return FP9_OK;
@@ -518,8 +692,12 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
     a.timeout_ns = timeout_ns;
     const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_start, stream));
-    expert_kernel<<<lay.grid, shp.threads, shp.smem, stream>>>(a);
-    FP9_CUDA_TRY(cudaGetLastError());
+    // jobs hold two tokens only when bsz >= 2; the one-token kernel keeps
+    // half the x / y registers live
+    void (*kern)(const ExpertArgs) = nullptr;
+    if (bsz == 1) kern = shp.rows == 8 ? expert_kernel<8, 1> : expert_kernel<4, 1>;
+    else kern = shp.rows == 8 ? expert_kernel<8, 2> : expert_kernel<4, 2>;
+    FP9_CUDA_TRY(launch_pdl(kern, dim3(lay.grid), dim3(shp.threads), shp.smem, stream, a));
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_stop, stream));
     if (!combine) return FP9_OK;
     CombineArgs c;
@@ -533,8 +711,7 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
     c.grid = lay.grid;
     c.I = I;
     c.y = y;
-    combine_kernel<<<dim3(H / 128, bsz), kCombineWarps * 32, 0, stream>>>(c);
-    FP9_CUDA_TRY(cudaGetLastError());
+    FP9_CUDA_TRY(launch_pdl(combine_kernel, dim3(H / kCombineCols, bsz), dim3(kCombineWarps * 32), 0, stream, c));
     return FP9_OK;
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -40,6 +41,26 @@ inline fp9_status check_bank(const fp9_ffn_bank& b, int64_t n, int64_t inter, in
 // row of the sign plane starts 16-byte aligned for the bulk copies) and at
 // most FP9_MAX_HIDDEN (one 16-column chunk per consumer thread).
 inline bool hidden_ok(int64_t h) { return h >= 128 && h <= FP9_MAX_HIDDEN && h % 128 == 0; }
+
+// Launches `kernel` on `stream` as a programmatic dependent of the work
+// queued before it: the launch may begin while the previous kernel is
+// still running, and each kernel of this library executes
+// griddepcontrol.wait before it reads anything an earlier launch wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Number of SMs of the current device (-1 if it cannot be queried).
 int32_t device_sm_count();

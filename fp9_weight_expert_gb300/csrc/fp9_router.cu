@@ -5,9 +5,10 @@
 // dual-lane overlap", section 9.2); the grouping (8 groups of 32, top-4
 // groups ranked by the sum of their two best scores) is the DeepSeek-V3 gate.
 //
-// One launch: every CTA computes the logits of kRouterRows experts for all
-// tokens; the last CTA to finish (a self-resetting atomicInc ticket, no
-// waiting) reads all logits back and does the selection and the job build.
+// One launch: CTA e computes the logits of expert e for all tokens; the
+// last CTA to finish (a self-resetting atomicInc ticket,
+// no waiting) reads all logits back and does the selection and the job
+// build.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -22,7 +23,7 @@
 namespace fp9 {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRouterRows = 2;
+constexpr int kRouterVec = FP9_MAX_HIDDEN / 4 / kRouterThreads;  // float4 of one row per thread
 constexpr int kMaxEntries = FP9_MAX_BSZ * FP9_MAX_TOPK;  // 128 (token, expert) pairs
 static_assert(kMaxEntries <= kRouterThreads, "one thread per routed pair");
 
@@ -66,8 +67,8 @@ __device__ void select_token(const RouterArgs& a, const float* s, int t, int lan
     float gscore = -INFINITY;
     if (lane < a.n_groups) {
         float m1 = -INFINITY, m2 = -INFINITY;
-        for (int i = 0; i < gsize; ++i) {
-            const float v = s[lane * gsize + i];
+        for (int i = 0; i < gsize; ++i) {  // rotated start: lanes hit distinct banks
+            const float v = s[lane * gsize + (i + lane) % gsize];
             if (v > m1) {
                 m2 = m1;
                 m1 = v;
@@ -197,58 +198,58 @@ __device__ void build_jobs(const RouterArgs& a, int tid) {
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
     extern __shared__ float s_scores[];  // [bsz, E] in the last CTA
-    __shared__ float s_red[kRouterThreads / 32][kRouterRows][FP9_MAX_BSZ];
+    __shared__ float s_red[kRouterThreads / 32][FP9_MAX_BSZ];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int e0 = blockIdx.x * kRouterRows;
+    const int e = blockIdx.x;
     const int H4 = a.H / 4;
-
-    float acc[kRouterRows][FP9_MAX_BSZ];
-#pragma unroll
-    for (int r = 0; r < kRouterRows; ++r)
-#pragma unroll
-        for (int t = 0; t < FP9_MAX_BSZ; ++t) acc[r][t] = 0.0f;
-
     const float4* x4 = reinterpret_cast<const float4*>(a.x);
-    const float4* w4 = reinterpret_cast<const float4*>(a.wr);
-#pragma unroll 4
-    for (int c = tid; c < H4; c += kRouterThreads) {
-        float4 wv[kRouterRows];
+    const float4* w4 = reinterpret_cast<const float4*>(a.wr) + static_cast<int64_t>(e) * H4;
+
+    // Nothing is read before the wait: the caller may have written x, W_g
+    // or the workspace with the kernel just before this one.
+    grid_dependency_wait();
+    grid_launch_dependents();
+    float4 wv[kRouterVec];
 #pragma unroll
-        for (int r = 0; r < kRouterRows; ++r)
-            wv[r] = (e0 + r < a.E) ? __ldcs(w4 + static_cast<int64_t>(e0 + r) * H4 + c)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < kRouterVec; ++i) {
+        const int c = tid + i * kRouterThreads;
+        wv[i] = c < H4 ? __ldcs(w4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    float acc[FP9_MAX_BSZ];
 #pragma unroll
-        for (int t = 0; t < FP9_MAX_BSZ; ++t) {
-            if (t < a.bsz) {
-                const float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
+    for (int t = 0; t < FP9_MAX_BSZ; ++t) acc[t] = 0.0f;
 #pragma unroll
-                for (int r = 0; r < kRouterRows; ++r) {
-                    float v = acc[r][t];
-                    v = fmaf(wv[r].x, xv.x, v);
-                    v = fmaf(wv[r].y, xv.y, v);
-                    v = fmaf(wv[r].z, xv.z, v);
-                    v = fmaf(wv[r].w, xv.w, v);
-                    acc[r][t] = v;
+    for (int i = 0; i < kRouterVec; ++i) {
+        const int c = tid + i * kRouterThreads;
+        if (c < H4) {
+#pragma unroll
+            for (int t = 0; t < FP9_MAX_BSZ; ++t) {
+                if (t < a.bsz) {
+                    const float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
+                    float v = acc[t];
+                    v = fmaf(wv[i].x, xv.x, v);
+                    v = fmaf(wv[i].y, xv.y, v);
+                    v = fmaf(wv[i].z, xv.z, v);
+                    v = fmaf(wv[i].w, xv.w, v);
+                    acc[t] = v;
                 }
             }
         }
     }
 #pragma unroll
-    for (int r = 0; r < kRouterRows; ++r)
-#pragma unroll
-        for (int t = 0; t < FP9_MAX_BSZ; ++t) {
-            const float v = warp_sum(acc[r][t]);
-            if (lane == 0) s_red[warp][r][t] = v;
+    for (int t = 0; t < FP9_MAX_BSZ; ++t) {
+        if (t < a.bsz) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) s_red[warp][t] = v;
         }
+    }
     __syncthreads();
-    if (tid < kRouterRows * FP9_MAX_BSZ) {
-        const int r = tid / FP9_MAX_BSZ, t = tid % FP9_MAX_BSZ;
-        if (t < a.bsz && e0 + r < a.E) {
-            float v = 0.0f;
-            for (int w = 0; w < kRouterThreads / 32; ++w) v += s_red[w][r][t];
-            a.logits[t * a.E + e0 + r] = v;
-        }
+    if (tid < a.bsz) {
+        float v = 0.0f;
+        for (int w = 0; w < kRouterThreads / 32; ++w) v += s_red[w][tid];
+        a.logits[tid * a.E + e] = v;
     }
     __threadfence();
     __syncthreads();
@@ -316,14 +317,8 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.ids_out = ids_out;
     a.w_out = w_out;
     a.jobs = build ? reinterpret_cast<Job*>(ws + lay.off_jobs) : nullptr;
-    const unsigned grid = (L->n_experts + kRouterRows - 1) / kRouterRows;
-    const size_t smem = sizeof(float) * bsz * L->n_experts;
-    if (smem > 48 * 1024) {
-        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem)));
-    }
-    router_kernel<<<grid, kRouterThreads, smem, stream>>>(a);
-    FP9_CUDA_TRY(cudaGetLastError());
+    const size_t smem = sizeof(float) * bsz * L->n_experts;  // <= 32 KB
+    FP9_CUDA_TRY(launch_pdl(router_kernel, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
     return FP9_OK;
 }
 

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(float* h
                                                                        int64_t H, float eps) {
     __shared__ float red[kNormThreads / 32];
     __shared__ float s_scale;
+    grid_dependency_wait();  // y and h are complete
+    grid_launch_dependents();
     const int t = blockIdx.x;
     float4* h4 = reinterpret_cast<float4*>(h + t * H);
     const float4* y4 = y ? reinterpret_cast<const float4*>(y + t * H) : nullptr;
@@ -70,7 +72,7 @@ extern "C" fp9_status fp9_residual_rmsnorm(float* h, const float* y, float* x_ou
     FP9_CHECK_ARG(hidden >= 4 && hidden % 4 == 0, FP9_ERR_SHAPE);
     FP9_CHECK_ARG(eps >= 0.0f, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(h, 16) && aligned(x_out, 16) && (y == nullptr || aligned(y, 16)), FP9_ERR_ALIGN);
-    residual_rmsnorm_kernel<<<bsz, kNormThreads, 0, static_cast<cudaStream_t>(stream)>>>(h, y, x_out, hidden, eps);
-    FP9_CUDA_TRY(cudaGetLastError());
+    FP9_CUDA_TRY(launch_pdl(residual_rmsnorm_kernel, dim3(bsz), dim3(kNormThreads), 0,
+                            static_cast<cudaStream_t>(stream), h, y, x_out, hidden, eps));
     return FP9_OK;
 }

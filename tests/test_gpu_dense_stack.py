@@ -24,7 +24,7 @@ def _dense(hidden, inter, base):
     return f, tuple(planes)
 
 
-@pytest.mark.parametrize("hidden,inter", [(512, 333), (256, 4), (7168, 18432)])
+@pytest.mark.parametrize("hidden,inter", [(512, 333), (256, 4), (128, 151), (7168, 18432)])
 @pytest.mark.parametrize("bsz", [1, 2, 5])
 def test_dense_ffn_matches_oracle(hidden, inter, bsz):
     if hidden == 7168 and bsz == 5:

@@ -20,6 +20,12 @@ MID = synth.MoEShape(hidden=1024, inter=203, n_experts=16, n_groups=4, topk_grou
 # 128-wide hidden (the smallest allowed), 1-row intermediate: every chunk is a tail
 NARROW = synth.MoEShape(hidden=128, inter=1, n_experts=8, n_groups=2, topk_groups=1, topk=3,
                         n_shared=0, route_scale=1.0, router_std=0.05)
+# fewer (job, row) pairs than SMs: each job spans several one-row CTAs
+FEWROWS = synth.MoEShape(hidden=256, inter=5, n_experts=8, n_groups=1, topk_groups=1, topk=3,
+                         n_shared=1, route_scale=1.0, router_std=0.05)
+# about as many rows as SMs: CTAs own one or two rows across job boundaries
+NEARSM = synth.MoEShape(hidden=384, inter=37, n_experts=16, n_groups=2, topk_groups=1, topk=3,
+                        n_shared=1, route_scale=1.0, router_std=0.05 * (16 / 384) ** 0.5)
 
 
 def _run(shape, bsz, base, layer=None, ol=None):
@@ -37,7 +43,8 @@ def _run(shape, bsz, base, layer=None, ol=None):
     return L, ol, x, y, ids, w, ws, status
 
 
-@pytest.mark.parametrize("shape", [synth.TINY, MID, NARROW], ids=["tiny", "mid", "narrow"])
+@pytest.mark.parametrize("shape", [synth.TINY, MID, NARROW, FEWROWS, NEARSM],
+                         ids=["tiny", "mid", "narrow", "fewrows", "nearsm"])
 @pytest.mark.parametrize("bsz", [1, 2, 3, 5, 8])
 def test_moe_forward_matches_oracle(shape, bsz):
     L, ol, x, y, ids, w, ws, status = _run(shape, bsz, base=200 + bsz)
