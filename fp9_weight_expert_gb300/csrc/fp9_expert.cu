@@ -52,7 +52,7 @@ struct BankPtrs {
 struct ExpertArgs {
     BankPtrs bank[2];        // 0: routed experts / dense FFN, 1: shared experts
     const float* x;          // [bsz, H]
-    float* partial;          // [grid * maxseg * 2, H]
+    float* partial;          // token-major: [bsz * maxseg, H]
     const Job* jobs;         // MoE mode
     const Control* ctl;      // MoE mode: job count
     int32_t dense_jobs;      // > 0: dense mode, jobs are implicit
@@ -82,12 +82,14 @@ __device__ __forceinline__ Job get_job(const Job* jobs, int32_t dense_jobs, int3
         Job jb;
         jb.bank = 0;
         jb.expert = 0;
-        jb.pad0 = 0;
+        jb.pad[0] = jb.pad[1] = 0;
         jb.tok[0] = kTokensPerJob * j;
         jb.ntok = (kTokensPerJob * j + 1 < bsz) ? 2 : 1;
         jb.tok[1] = jb.ntok == 2 ? jb.tok[0] + 1 : jb.tok[0];
         jb.w[0] = 1.0f;
         jb.w[1] = jb.ntok == 2 ? 1.0f : 0.0f;
+        jb.b0 = -1;  // computed where needed
+        jb.seg_base[0] = jb.seg_base[1] = 0;  // a dense token is in exactly one job
         return jb;
     }
     return jobs[j];
@@ -350,7 +352,7 @@ __device__ __forceinline__ bool down_chunk(const ExpertArgs& a, SmemCtl& ctl, co
 // Completes the CTA sum of chunk `red_it` and returns, in lane
 // (rr * T + t), h = SiLU(g) * u * w_route for row rr, token t.
 template <int R, int T>
-__device__ __forceinline__ bool finish_sum(const ExpertArgs& a, SmemCtl& ctl, Stages& cs, const Job& job, int NW,
+__device__ __forceinline__ bool finish_sum(const ExpertArgs& a, SmemCtl& ctl, Stages& cs, float w0, float w1, int NW,
                                            int lane, float& hv) {
     constexpr int V = R * T;
     const uint32_t b = cs.red_it & 1u;
@@ -360,21 +362,42 @@ __device__ __forceinline__ bool finish_sum(const ExpertArgs& a, SmemCtl& ctl, St
     if (lane < 2 * V)
         for (int w = 0; w < NW; ++w) tot += ctl.red_vals[b][w][lane];
     const float u = __shfl_down_sync(0xFFFFFFFFu, tot, V);
-    const float wt = (T == 2 && (lane & 1)) ? job.w[1] : job.w[0];
+    const float wt = (T == 2 && (lane & 1)) ? w1 : w0;
     hv = (lane < V) ? silu(tot) * u * wt : 0.0f;
     return true;
 }
 
+// What the consumers keep of a job: its token count, routing weights, and
+// for each token the row of the partial list this CTA writes its share to
+// (slot = tok * maxseg + seg_base + (b - b0)).
+struct JobState {
+    int ntok;
+    float w0, w1;
+    int slot0, slot1;
+};
+
+__device__ __forceinline__ JobState job_state(const ExpertArgs& a, const Job& job, int job_index, const Range& rg) {
+    const int64_t b0 = job.b0 >= 0 ? job.b0 : cta_of_row(static_cast<int64_t>(job_index) * a.I, rg.n, rg.g);
+    const int rel = static_cast<int>(static_cast<int64_t>(blockIdx.x) - b0);
+    JobState js;
+    js.ntok = job.ntok;
+    js.w0 = job.w[0];
+    js.w1 = job.w[1];
+    js.slot0 = job.tok[0] * a.maxseg + job.seg_base[0] + rel;
+    js.slot1 = job.tok[1] * a.maxseg + job.seg_base[1] + rel;
+    return js;
+}
+
+// Writes y (this CTA's share of one job) to the job's partial slots.
 template <int MT>
-__device__ __forceinline__ void flush_partial(const ExpertArgs& a, int ntok, int64_t seg, int c16, bool active,
-                                              const Cols<MT>& y) {
+__device__ __forceinline__ void flush_partial(const ExpertArgs& a, int ntok, int slot0, int slot1, int c16,
+                                              bool active, const Cols<MT>& y) {
     if (!active) return;
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
         if (t < ntok) {
-            float4* dst = reinterpret_cast<float4*>(
-                a.partial + ((static_cast<int64_t>(blockIdx.x) * a.maxseg + seg) * kTokensPerJob + t) * a.H +
-                c16 * 16);
+            const int slot = t == 0 ? slot0 : slot1;
+            float4* dst = reinterpret_cast<float4*>(a.partial + static_cast<int64_t>(slot) * a.H + c16 * 16);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 dst[k] = make_float4(y.p[t][2 * k].x, y.p[t][2 * k + 1].x, y.p[t][2 * k].y, y.p[t][2 * k + 1].y);
@@ -418,20 +441,19 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
     Cols<MT> x, y;
     Walk w;
     w.begin(rg, a.I, R);
-    const int j0 = w.j;
     Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
     load_x(a, job, c16, active, x);
+    JobState js = job_state(a, job, w.j, rg);
     zero_cols(y);
     Stages cs;
     bool ok = true;
     // the chunk whose down rows are pending
-    bool pending = false;
-    int p_rows = 0, p_ntok = 1, p_seg = 0;
-    bool p_last_of_job = false;
+    bool pending = false, p_last_of_job = false;
+    int p_rows = 0, p_ntok = 1, p_slot0 = 0, p_slot1 = 0;
     float p_hv = 0.0f;
 
     while (!w.done()) {
-        const int T = MT == 1 ? 1 : job.ntok;
+        const int T = MT == 1 ? 1 : js.ntok;
         ok = (T == 2) ? gateup_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane)
                       : gateup_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane);
         if (!ok) break;
@@ -441,31 +463,31 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
                      : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
             if (!ok) break;
             if (p_last_of_job) {
-                flush_partial(a, p_ntok, p_seg, c16, active, y);
+                flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
                 zero_cols(y);
             }
         }
         float hv;
-        ok = (T == 2) ? finish_sum<R, MT>(a, ctl, cs, job, NW, lane, hv)
-                      : finish_sum<R, 1>(a, ctl, cs, job, NW, lane, hv);
+        ok = (T == 2) ? finish_sum<R, MT>(a, ctl, cs, js.w0, js.w1, NW, lane, hv)
+                      : finish_sum<R, 1>(a, ctl, cs, js.w0, js.w1, NW, lane, hv);
         if (!ok) break;
         pending = true;
         p_rows = w.rows;
         p_ntok = T;
-        p_seg = w.j - j0;
+        p_slot0 = js.slot0;
+        p_slot1 = js.slot1;
         p_hv = hv;
-        const bool new_job = w.next(R);
-        p_last_of_job = new_job;
-        if (new_job) {
+        p_last_of_job = w.next(R);
+        if (p_last_of_job) {
             job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
             load_x(a, job, c16, active, x);
+            js = job_state(a, job, w.j, rg);
         }
     }
     if (ok && pending) {
-        ok = (p_ntok == 2)
-                 ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
-                 : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
-        if (ok) flush_partial(a, p_ntok, p_seg, c16, active, y);
+        ok = (p_ntok == 2) ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
+                           : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
+        if (ok) flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
     }
     if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
@@ -528,15 +550,10 @@ constexpr int kCombineCols = 64;               // columns per CTA: 16 lanes x fl
 constexpr int kCombineWarps = 8;
 constexpr int kCombineLanes = kCombineWarps * 2;  // segment lanes: two per warp
 
-// y[t, c] = sum over the jobs holding token t, in job order, and over the
-// CTAs covering each job, in CTA order, of their partials. Segment lane s
-// (= 2 * warp + half-warp) adds the segments s, s + 16, ...; the sixteen
-// lane sums are then added in lane order.
-//
-// A job's rows [jI, jI + I) are covered by CTAs b0..b1. CTA b0 may have
-// started in an earlier job, so its partial for this job is its segment
-// k0 = j - first_job(b0); every later CTA b in (b0, b1] starts inside job j
-// and holds it as its segment 0.
+// y[t, c] = sum of token t's partials, in list order (= job order, then
+// CTA order within a job). Segment lane s (= 2 * warp + half-warp) adds
+// partials s, s + 16, ...; the sixteen lane sums are then added in lane
+// order.
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
     __shared__ float4 red[kCombineLanes][16];
     grid_dependency_wait();  // all partials are written
@@ -546,37 +563,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const int sl = warp * 2 + half;
     const int t = blockIdx.y;
     const int c = blockIdx.x * kCombineCols + l16 * 4;
-    const int32_t J = a.dense_jobs > 0 ? a.dense_jobs : a.ctl->njobs;
-    const int64_t N = static_cast<int64_t>(J) * a.I;
-    const int64_t G = N < a.grid ? N : a.grid;
-    const int64_t stride_b = static_cast<int64_t>(a.maxseg) * kTokensPerJob * a.H;
+    int n;
+    if (a.dense_jobs > 0) {  // token t is in job t / 2 only
+        const int64_t N = static_cast<int64_t>(a.dense_jobs) * a.I;
+        const int64_t G = N < a.grid ? N : a.grid;
+        const int64_t first = static_cast<int64_t>(t / kTokensPerJob) * a.I;
+        n = static_cast<int>(cta_of_row(first + a.I - 1, N, G) - cta_of_row(first, N, G) + 1);
+    } else {
+        n = a.ctl->nseg[t];
+    }
+    const float* base = a.partial + static_cast<int64_t>(t) * a.maxseg * a.H + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int64_t idx = 0;
-    for (int j = 0; j < J; ++j) {
-        const Job job = get_job(a.jobs, a.dense_jobs, a.bsz, j);
-        int q = -1;
-        if (job.tok[0] == t) q = 0;
-        else if (job.ntok == 2 && job.tok[1] == t) q = 1;
-        if (q < 0) continue;
-        const int64_t first_row = static_cast<int64_t>(j) * a.I;
-        const int64_t b0 = cta_of_row(first_row, N, G);
-        const int64_t b1 = cta_of_row(first_row + a.I - 1, N, G);
-        const int64_t k0 = j - cta_start(b0, N, G) / a.I;
-        const int64_t nseg = b1 - b0 + 1;
-        int64_t s = ((sl - idx) % kCombineLanes + kCombineLanes) % kCombineLanes;
-        const float* base = a.partial + (static_cast<int64_t>(q)) * a.H + c;
 #pragma unroll 4
-        for (; s < nseg; s += kCombineLanes) {
-            const int64_t b = b0 + s;
-            const int64_t k = s == 0 ? k0 : 0;
-            const float4 p = __ldcs(reinterpret_cast<const float4*>(base + b * stride_b +
-                                                                    k * kTokensPerJob * a.H));
-            acc.x += p.x;
-            acc.y += p.y;
-            acc.z += p.z;
-            acc.w += p.w;
-        }
-        idx += nseg;
+    for (int s = sl; s < n; s += kCombineLanes) {
+        const float4 p = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(s) * a.H));
+        acc.x += p.x;
+        acc.y += p.y;
+        acc.z += p.z;
+        acc.w += p.w;
     }
     red[sl][l16] = acc;
     __syncthreads();
@@ -787,7 +791,7 @@ extern "C" fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d
     // one CTA, one dense job: x at the start of ws, partials after the layout
     WsLayout lay = dense_layout(1, I, H, 1);
     lay.off_partial = align_up(sizeof(float) * H + kAlign);
-    lay.total = lay.off_partial + sizeof(float) * lay.maxseg * kTokensPerJob * H;
+    lay.total = lay.off_partial + sizeof(float) * lay.maxseg * H;
     FP9_CHECK_ARG(ws_bytes >= lay.total && ws_bytes >= 65536, FP9_ERR_WORKSPACE);
     uint8_t* w = static_cast<uint8_t*>(ws);
     BankPtrs p;  // never dereferenced: no copies are issued

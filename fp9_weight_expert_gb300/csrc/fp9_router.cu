@@ -32,6 +32,8 @@ struct RouterArgs {
     const float* wr;     // [E, H]
     int32_t bsz, E, H, n_groups, topk_groups, topk, n_shared;
     float scale;
+    int64_t I;           // intermediate size (rows per job)
+    int32_t grid;        // CTAs of the fused expert kernel
     Control* ctl;
     float* logits;       // [bsz, E]
     int32_t* ids_ws;     // [bsz, topk]
@@ -41,34 +43,31 @@ struct RouterArgs {
     Job* jobs;           // [jmax]
 };
 
-// Argmax over a warp of (value, index) pairs: larger value wins, ties go to
-// the lower index.
-__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, m);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, m);
-        if (ov > v || (ov == v && oi < idx)) {
-            v = ov;
-            idx = oi;
-        }
-    }
-}
-
+// (v, i) beats (bv, bi): a larger value, or an equal value and a lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-// Selection for token t by one warp. `s` holds the token's E sigmoid
-// scores (NaN already replaced by -inf so that the choice stays defined).
-__device__ void select_token(const RouterArgs& a, const float* s, int t, int lane) {
-    const int gsize = a.E / a.n_groups;
+// Selection for all tokens by the whole CTA, by ranks: a candidate's rank
+// is the number of candidates that beat it (a larger score, or an equal
+// score and a lower index), so the k best are the candidates of rank < k,
+// each at the position of its rank (the order of a sort by score
+// descending, ties to the lower index). `s` holds the [bsz, E] sigmoid
+// scores (NaN replaced by -inf so that the choice stays defined).
+__device__ void select_all(const RouterArgs& a, const float* s, int tid, int32_t* s_ids, float* s_wts) {
+    __shared__ float s_gs[FP9_MAX_BSZ][FP9_MAX_GROUPS];
+    __shared__ uint32_t s_kept[FP9_MAX_BSZ];
+    __shared__ float s_sel[kMaxEntries];
+    const int E = a.E, G = a.n_groups, gsize = E / G;
     // group scores: sum of the two largest members (the one member if gsize == 1)
-    float gscore = -INFINITY;
-    if (lane < a.n_groups) {
+    for (int i = tid; i < a.bsz * G; i += blockDim.x) {
+        const int t = i / G, g = i % G;
+        const float* grp = s + t * E + g * gsize;
         float m1 = -INFINITY, m2 = -INFINITY;
-        for (int i = 0; i < gsize; ++i) {  // rotated start: lanes hit distinct banks
-            const float v = s[lane * gsize + (i + lane) % gsize];
+        int idx = g % gsize;  // rotated start: the groups' threads hit distinct banks
+        for (int m = 0; m < gsize; ++m) {
+            const float v = grp[idx];
+            idx = (idx + 1 == gsize) ? 0 : idx + 1;
             if (v > m1) {
                 m2 = m1;
                 m1 = v;
@@ -76,69 +75,74 @@ __device__ void select_token(const RouterArgs& a, const float* s, int t, int lan
                 m2 = v;
             }
         }
-        gscore = (gsize == 1) ? m1 : m1 + m2;
+        s_gs[t][g] = (gsize == 1) ? m1 : m1 + m2;
     }
-    uint32_t kept = 0;  // bit g set when group g is kept
-    for (int r = 0; r < a.topk_groups; ++r) {
-        float v = -INFINITY;
-        int idx = INT_MAX;
-        if (lane < a.n_groups && !((kept >> lane) & 1u)) {
-            v = gscore;
-            idx = lane;
-        }
-        warp_argmax(v, idx);
-        kept |= 1u << idx;
+    if (tid < a.bsz) s_kept[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < a.bsz * G; i += blockDim.x) {
+        const int t = i / G, g = i % G;
+        const float v = s_gs[t][g];
+        int rank = 0;
+        for (int o = 0; o < G; ++o) rank += better(s_gs[t][o], o, v, g) ? 1 : 0;
+        if (rank < a.topk_groups) atomicOr(&s_kept[t], 1u << g);
     }
-    // experts e = lane + 32 * j; chosen bits per lane
-    uint32_t taken = 0;
-    const int per_lane = (a.E + 31) / 32;
-    float sum = 0.0f;
-    int my_id = 0;
-    float my_s = 0.0f;
-    for (int k = 0; k < a.topk; ++k) {
-        float v = -INFINITY;
-        int idx = INT_MAX;
-        for (int j = 0; j < per_lane; ++j) {
-            const int e = lane + 32 * j;
-            if (e < a.E && ((kept >> (e / gsize)) & 1u) && !((taken >> j) & 1u)) {
-                if (better(s[e], e, v, idx)) {
-                    v = s[e];
-                    idx = e;
-                }
-            }
+    __syncthreads();
+    for (int i = tid; i < a.bsz * E; i += blockDim.x) {
+        const int t = i / E, e = i % E;
+        const uint32_t kept = s_kept[t];
+        if (!((kept >> (e / gsize)) & 1u)) continue;
+        const float* st = s + t * E;
+        const float v = st[e];
+        int rank = 0;
+        for (int g = 0; g < G; ++g) {
+            if (!((kept >> g) & 1u)) continue;
+            const float* grp = st + g * gsize;
+            const int base = g * gsize;
+            for (int m = 0; m < gsize; ++m) rank += better(grp[m], base + m, v, e) ? 1 : 0;
         }
-        warp_argmax(v, idx);
-        if ((idx & 31) == lane) taken |= 1u << (idx / 32);
-        sum += v;  // identical on every lane, added in rank order
-        if (lane == k) {
-            my_id = idx;
-            my_s = v;
+        if (rank < a.topk) {
+            s_ids[t * a.topk + rank] = e;
+            s_sel[t * a.topk + rank] = v;
         }
     }
-    if (lane < a.topk) {
-        const float w = my_s / sum * a.scale;
-        a.ids_ws[t * a.topk + lane] = my_id;
-        a.w_ws[t * a.topk + lane] = w;
-        if (a.ids_out) a.ids_out[t * a.topk + lane] = my_id;
-        if (a.w_out) a.w_out[t * a.topk + lane] = w;
+    __syncthreads();
+    if (tid < a.bsz) {  // weights: s_i / sum(s_chosen) * route_scale, summed in rank order
+        const int t = tid;
+        float sum = 0.0f;
+        for (int k = 0; k < a.topk; ++k) sum += s_sel[t * a.topk + k];
+        for (int k = 0; k < a.topk; ++k) {
+            const int id = s_ids[t * a.topk + k];
+            const float w = s_sel[t * a.topk + k] / sum * a.scale;
+            s_wts[t * a.topk + k] = w;
+            a.ids_ws[t * a.topk + k] = id;
+            a.w_ws[t * a.topk + k] = w;
+            if (a.ids_out) a.ids_out[t * a.topk + k] = id;
+            if (a.w_out) a.w_out[t * a.topk + k] = w;
+        }
     }
+    __syncthreads();
 }
 
 // Job list: shared experts first (tokens in pairs, weight 1), then routed
 // experts in ascending id, each with its tokens in ascending order, in
-// groups of up to two.
-__device__ void build_jobs(const RouterArgs& a, int tid) {
+// groups of up to two. Then, for the fused kernel and the combine: the
+// first CTA covering each job, and where each job's partials start in the
+// token-major partial list of each of its tokens.
+__device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, const float* s_wts) {
     __shared__ int32_t s_in[kMaxEntries];
     __shared__ int32_t s_key[kMaxEntries];
     __shared__ float s_w[kMaxEntries];
     __shared__ int32_t s_start[kMaxEntries];
+    __shared__ Job s_jobs[kMaxJobs];
+    __shared__ int32_t s_nseg[kMaxJobs];
+    __shared__ int32_t s_J;
     const int P = a.bsz * a.topk;
     int32_t key = INT_MAX;
     float w = 0.0f;
     if (tid < P) {
         const int t = tid / a.topk;
-        key = a.ids_ws[tid] * FP9_MAX_BSZ + t;  // unique: a token picks an expert once
-        w = a.w_ws[tid];
+        key = s_ids[tid] * FP9_MAX_BSZ + t;  // unique: a token picks an expert once
+        w = s_wts[tid];
         s_in[tid] = key;
     }
     __syncthreads();
@@ -167,33 +171,64 @@ __device__ void build_jobs(const RouterArgs& a, int tid) {
         Job j;
         j.bank = 0;
         j.expert = e;
-        j.pad0 = 0;
         j.tok[0] = s_key[tid] % FP9_MAX_BSZ;
         j.w[0] = s_w[tid];
         const bool two = (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
         j.ntok = two ? 2 : 1;
         j.tok[1] = two ? s_key[tid + 1] % FP9_MAX_BSZ : j.tok[0];
         j.w[1] = two ? s_w[tid + 1] : 0.0f;
-        a.jobs[nshared_jobs + before] = j;
+        s_jobs[nshared_jobs + before] = j;
     }
     if (tid < nshared_jobs) {
         const int sh = tid / pairs, pr = tid % pairs;
         Job j;
         j.bank = 1;
         j.expert = sh;
-        j.pad0 = 0;
         j.tok[0] = 2 * pr;
         j.ntok = (2 * pr + 1 < a.bsz) ? 2 : 1;
         j.tok[1] = (j.ntok == 2) ? 2 * pr + 1 : 2 * pr;
         j.w[0] = 1.0f;
         j.w[1] = (j.ntok == 2) ? 1.0f : 0.0f;
-        a.jobs[tid] = j;
+        s_jobs[tid] = j;
     }
     if (tid == 0) {
         int starts = 0;
         for (int q = 0; q < P; ++q) starts += s_start[q];
-        a.ctl->njobs = nshared_jobs + starts;
+        s_J = nshared_jobs + starts;
     }
+    __syncthreads();
+    const int J = s_J;
+    const int64_t N = static_cast<int64_t>(J) * a.I;
+    const int64_t G = N < a.grid ? N : a.grid;
+    for (int j = tid; j < J; j += blockDim.x) {  // CTAs b0..b1 cover job j
+        const int64_t b0 = cta_of_row(static_cast<int64_t>(j) * a.I, N, G);
+        const int64_t b1 = cta_of_row(static_cast<int64_t>(j) * a.I + a.I - 1, N, G);
+        s_jobs[j].b0 = static_cast<int32_t>(b0);
+        s_nseg[j] = static_cast<int32_t>(b1 - b0 + 1);
+    }
+    __syncthreads();
+    if (tid < a.bsz) {  // token tid: its partials, job by job
+        int off = 0;
+        for (int j = 0; j < J; ++j) {
+            const Job& jb = s_jobs[j];
+            if (jb.tok[0] == tid) {
+                s_jobs[j].seg_base[0] = off;
+                off += s_nseg[j];
+            } else if (jb.ntok == 2 && jb.tok[1] == tid) {
+                s_jobs[j].seg_base[1] = off;
+                off += s_nseg[j];
+            }
+        }
+        a.ctl->nseg[tid] = off;
+    }
+    __syncthreads();
+    for (int j = tid; j < J; j += blockDim.x) {
+        Job jb = s_jobs[j];
+        if (jb.ntok == 1) jb.seg_base[1] = jb.seg_base[0];
+        jb.pad[0] = jb.pad[1] = 0;
+        a.jobs[j] = jb;
+    }
+    if (tid == 0) a.ctl->njobs = J;
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
@@ -250,13 +285,15 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
         float v = 0.0f;
         for (int w = 0; w < kRouterThreads / 32; ++w) v += s_red[w][tid];
         a.logits[tid * a.E + e] = v;
+        __threadfence();  // the logit is visible before this CTA is counted
     }
-    __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = (atomicInc(&a.ctl->ticket, gridDim.x - 1) == gridDim.x - 1) ? 1 : 0;
+    if (tid == 0) {
+        s_last = (atomicInc(&a.ctl->ticket, gridDim.x - 1) == gridDim.x - 1) ? 1 : 0;
+        if (s_last) __threadfence();
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
 
     for (int i = tid; i < a.bsz * a.E; i += kRouterThreads) {
         const float l = __ldcg(a.logits + i);
@@ -264,10 +301,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
         s_scores[i] = (s == s) ? s : -INFINITY;
     }
     __syncthreads();
-    if (warp < a.bsz) select_token(a, s_scores + warp * a.E, warp, lane);
-    __threadfence_block();
-    __syncthreads();
-    if (a.jobs != nullptr) build_jobs(a, tid);
+    __shared__ int32_t s_ids[kMaxEntries];
+    __shared__ float s_wts[kMaxEntries];
+    select_all(a, s_scores, tid, s_ids, s_wts);
+    if (a.jobs != nullptr) build_jobs(a, tid, s_ids, s_wts);
 }
 
 // Validation shared by moe_router and fp9_moe_forward (no CUDA calls).
@@ -317,7 +354,17 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.ids_out = ids_out;
     a.w_out = w_out;
     a.jobs = build ? reinterpret_cast<Job*>(ws + lay.off_jobs) : nullptr;
+    a.I = L->inter;
+    a.grid = lay.grid;
     const size_t smem = sizeof(float) * bsz * L->n_experts;  // <= 32 KB
+    static bool configured[64] = {false};
+    int dev = 0;
+    FP9_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
+        configured[dev] = true;
+    }
     FP9_CUDA_TRY(launch_pdl(router_kernel, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
     return FP9_OK;
 }
