@@ -116,6 +116,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+# ------------------------------------------------------- replica plumbing
+
+def max_over_ranks(value: float) -> float:
+    """Largest value over the ranks of the default process group (the value
+    itself when not distributed). Host-side only (gloo), no data-path
+    collective: replicas are independent."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, bsz: int, steps: int, max_elapsed_s: float) -> float:
+    """Whole-job tokens/s: every rank processed bsz * steps tokens; the job
+    took as long as its slowest rank."""
+    return world * bsz * steps / max_elapsed_s
+
+
 # ----------------------------------------------------------- native bench
 
 def _native(args):
@@ -201,12 +222,8 @@ def _native(args):
     if int(status.item()) != 0:
         raise RuntimeError("device status: " + binding.status_str(int(status.item())))
 
-    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop))
     kern_ms = [a.elapsed_time(b) for a, b in ev_k]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
 
     # union of experts streamed per step: distinct routed ids + shared
     idc = ids.cpu()
@@ -237,11 +254,7 @@ def _native(args):
         binding.fp9_moe_forward(Ls[i % len(Ls)], xd, y, ws.tensor, status)
         yh.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t_e
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t_e)
 
     extra = {}
     if not args.no_extra and world == 1:
@@ -249,7 +262,7 @@ def _native(args):
 
     if rank != 0:
         return None
-    value = world * bsz * K / (elapsed_ms / 1e3)
+    value = replica_throughput(world, bsz, K, elapsed_ms / 1e3)
     clocks = sampler.summary(t_region0, t_region1)
     out = {
         "metric": METRIC,
@@ -289,7 +302,7 @@ def _native(args):
         "weight_stream_gbs_per_step": round(step_gbs, 1),
         "us_per_layer": round(elapsed_ms / K * 1e3, 2),
         "e2e": {
-            "value": round(world * bsz * Ke / e2e_s, 2),
+            "value": round(replica_throughput(world, bsz, Ke, e2e_s), 2),
             "unit": "tok/s",
             "h2d_bytes_per_step": bsz * H * 4,
             "d2h_bytes_per_step": bsz * H * 4,
