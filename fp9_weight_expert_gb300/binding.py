@@ -91,6 +91,10 @@ _SIGS = {
                                             ctypes.c_int32, ctypes.c_void_p]),
     "fp9_status_str": (ctypes.c_char_p, [ctypes.c_int32]),
     "fp9_profile_events": (None, [ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_moe_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int32,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
 }
 
 
@@ -211,3 +215,18 @@ def fp9_profile_events(start, stop) -> None:
         raise ValueError("record each event once before passing it (torch creates it lazily)")
     load().fp9_profile_events(start.cuda_event if start is not None else None,
                               stop.cuda_event if stop is not None else None)
+
+
+def fp9_moe_forward_noalloc(layer, x: torch.Tensor, y: torch.Tensor, status: torch.Tensor | None = None,
+                            ids: torch.Tensor | None = None, weights: torch.Tensor | None = None,
+                            stream=None) -> None:
+    """fp9_moe_forward without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed scratch array is used
+    instead (see include/fp9moe.h for its size and sharing rules)."""
+    _check(load().fp9_moe_forward_noalloc(ctypes.byref(layer.c_struct()), _ptr(x), x.shape[0], _ptr(y),
+                                          _ptr(ids), _ptr(weights), _ptr(status), _stream(stream)),
+           "fp9_moe_forward_noalloc")
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load().fp9_moe_noalloc_scratch_bytes())

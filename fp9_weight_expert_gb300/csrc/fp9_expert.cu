@@ -29,6 +29,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 
 #include "fp9_device.cuh"
 #include "fp9_host.h"
@@ -807,3 +808,75 @@ extern "C" void fp9_profile_events(void* start, void* stop) {
     g_prof_start = static_cast<cudaEvent_t>(start);
     g_prof_stop = static_cast<cudaEvent_t>(stop);
 }
+
+// ----------------------------------------------- allocation-free variant ---
+//
+// fp9_moe_forward_noalloc: the same router, fused expert and combine
+// kernels as fp9_moe_forward, with their workspace in a fixed array of
+// device memory that belongs to this library instead of a caller buffer.
+// It is for callers that cannot call cudaMalloc at all: runtimes whose
+// device memory is owned and capped by another framework, plugins handed
+// only input and output buffers, and latency-critical paths that must not
+// risk the implicit synchronisation of an allocation.
+//
+// The array is a file-scope __device__ object: every GPU that loads this
+// library holds kNoAllocScratchBytes for it until the process exits. Host
+// code may not use the array's name as a device address, so the address is
+// looked up once per device with cudaGetSymbolAddress (with that device
+// current) on the first call made on that device; make that first call
+// before any stream capture. All calls share the array and it keeps the
+// last call's contents: the control block (the router's ticket and
+// counts) is cleared by every call, and calls that overlap on the GPU
+// (two streams, or two host threads) race on it.
+
+namespace fp9 {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static void* noalloc_scratch_ptr(int dev) {
+    static std::mutex mu;
+    static void* ptrs[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace fp9
+
+extern "C" fp9_status fp9_moe_forward_noalloc(const fp9_moe_layer* layer, const float* x, int32_t bsz, float* y,
+                                              int32_t* ids, float* weights, int32_t* d_status, void* stream) {
+    fp9_status st = check_layer(layer, bsz);
+    if (st != FP9_OK) return st;
+    FP9_CHECK_ARG(x != nullptr && y != nullptr && x != y, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(x, 16) && aligned(y, 16), FP9_ERR_ALIGN);
+    const int32_t sms = device_sm_count();
+    FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
+    const WsLayout lay =
+        moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms);
+    // the fixed array must hold this call's workspace
+    FP9_CHECK_ARG(lay.total <= kNoAllocScratchBytes, FP9_ERR_WORKSPACE);
+    int dev = 0;
+    FP9_CUDA_TRY(cudaGetDevice(&dev));
+    uint8_t* w = static_cast<uint8_t*>(noalloc_scratch_ptr(dev));
+    FP9_CHECK_ARG(w != nullptr, FP9_ERR_CUDA);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FP9_CUDA_TRY(cudaMemsetAsync(w, 0, sizeof(Control), s));
+    st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s);
+    if (st != FP9_OK) return st;
+    const BankPtrs routed = bank_ptrs(layer->routed);
+    const BankPtrs shared = layer->n_shared > 0 ? bank_ptrs(layer->shared) : routed;
+    return launch_ffn(routed, shared, x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, 0,
+                      d_status, s, kDefaultTimeoutNs, false, true);
+}
+
+extern "C" size_t fp9_moe_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }

@@ -207,6 +207,33 @@ fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status,
                                 int32_t timeout_us, void* stream);
 
 /*
+ * fp9_moe_forward_noalloc: fp9_moe_forward for callers that cannot
+ * allocate device memory (a runtime whose device memory is owned and
+ * capped by another framework, a plugin handed only its input and output
+ * buffers, a latency-critical path that must not risk the synchronisation
+ * of an allocation). The pages have no counterpart: this is an interface
+ * of this library only.
+ *   Same arguments and results as fp9_moe_forward without ws / ws_bytes.
+ *   The workspace is a fixed array of fp9_moe_noalloc_scratch_bytes()
+ *   (16 MiB) of device memory inside the library, held by every GPU that
+ *   loads it until the process exits; no memory is allocated by the call.
+ *   A call whose workspace would not fit returns FP9_ERR_WORKSPACE (the
+ *   DeepSeek-V3 layer fits up to bsz 3 on a 152-SM GPU).
+ *   The first call on a device looks up the array's device address on
+ *   that device (cudaGetSymbolAddress): make it before any stream capture.
+ *   Every call clears the control block it needs zeroed. All calls share
+ *   the one array, so calls that overlap on the GPU (other streams, other
+ *   host threads) race: serialise them.
+ */
+fp9_status fp9_moe_forward_noalloc(const fp9_moe_layer* layer, const float* x,
+                                   int32_t bsz, float* y, int32_t* ids,
+                                   float* weights, int32_t* d_status,
+                                   void* stream);
+
+/* Size in bytes of the fixed scratch array of fp9_moe_forward_noalloc. */
+size_t fp9_moe_noalloc_scratch_bytes(void);
+
+/*
  * fp9_profile_events: tracing hook. When both events (cudaEvent_t handles
  * created by the caller) are non-NULL, every later launch of the fused
  * expert kernel records `start` just before and `stop` just after itself,
