@@ -48,6 +48,28 @@ def _args():
     return p.parse_args()
 
 
+KERNEL_SOURCES = ("fp9_weight_expert_gb300/csrc/fp9_expert.cu", "fp9_weight_expert_gb300/csrc/fp9_device.cuh",
+                  "fp9_weight_expert_gb300/csrc/fp9_plan.h")
+
+
+def _profiled_traffic():
+    """DRAM bytes per fused-kernel launch from the committed ncu summary, or
+    None when the kernel's sources changed since that capture."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", "expert_kernel_dsv3_bsz1.md")).read()
+        want = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text).group(1)
+        traffic = int(re.search(r"traffic_bytes_per_launch:\s*(\d+)", text).group(1))
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        return traffic if h.hexdigest()[:16] == want else None
+    except Exception:
+        return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -295,7 +317,7 @@ def _native(args):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(kernel_gbs / peak, 4),
-            "traffic": None,
+            "traffic": _profiled_traffic() if bsz == 1 else None,
             "algorithmic_bytes_per_launch": round(sum(weight_bytes) / K),
             "kernel_us": round(mean_kern_s * 1e6, 2),
         },
