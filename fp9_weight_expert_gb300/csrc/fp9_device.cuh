@@ -109,6 +109,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// try_wait that may suspend the thread in hardware for up to `hint_ns`
+// (it returns as soon as the phase completes), so waiting warps do not spin
+// on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase of `parity` to complete, giving up after `limit_ns`
 // nanoseconds or as soon as another thread of the CTA has raised *abort.
 // Returns false when it gave up; then the caller records a timeout.
@@ -116,12 +131,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 15u) == 0u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 2000u)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

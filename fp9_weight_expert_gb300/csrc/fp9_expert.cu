@@ -15,13 +15,19 @@
 // in registers and writes it once per job it touches, and a second kernel
 // adds those partials in a fixed order.
 //
-// CTA layout (one per SM): warps 0..NW-1 are consumers, each thread owning
-// 16 consecutive columns of the hidden dimension; warp NW is the producer,
-// whose lane 0 streams chunks of kR rows of one matrix (bodies, then signs)
-// with bulk copies into a ring of shared-memory stages guarded by mbarriers.
-// Per chunk: gate rows, up rows (each a dot product over the hidden
-// dimension, reduced across the CTA), then the down rows (an axpy into the
-// thread's 16 columns of y, no reduction).
+// CTA layout (one per SM): NW consumer warps and one producer warp. The
+// producer's lane 0 streams each chunk of R rows as three stages, one per
+// ring slot: slot 0 the gate rows, slot 1 the up rows, slot 2 the down rows
+// (bodies, then signs; bulk copies completing on mbarriers).
+//   gate/up: the 2R rows of a chunk are dealt round-robin to the warps; a
+//     warp computes whole rows (x is staged in shared memory), so the only
+//     reduction is a 5-step warp sum per row; lane 0 publishes g or u.
+//   down: each thread owns 16 consecutive hidden columns and keeps y for
+//     them in registers: an axpy with no reduction.
+// Per chunk c a warp does its gate/up rows, arrives at c's publish barrier,
+// processes the down rows of chunk c - 1 (whose h is known), then waits for
+// c's barrier and forms h = SiLU(g) * u * w_route. The producer streams
+// gate c, up c, then down c - 1.
 //
 // Every wait is bounded (a timeout sets FP9_ERR_TIMEOUT in the status word
 // and the CTA drains its copies in flight and returns).
@@ -38,12 +44,12 @@
 
 namespace fp9 {
 
-constexpr int kMaxRows = 8;                                     // rows per chunk (4 or 8)
-constexpr int kMaxStages = 16;
+constexpr int kMaxRows = 16;                                    // rows per chunk
+constexpr int kSlots = 3;                                       // gate, up, down
 constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / 16 / 32;     // 14
 constexpr int kMaxThreads = kMaxConsumerWarps * 32 + 32;        // 480
-constexpr int kMaxV = 2 * kMaxRows * kTokensPerJob;             // reduced values per chunk
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;           // 1 s
+constexpr int kGate = 0, kUp = 1, kDown = 2;
 
 struct BankPtrs {
     const uint8_t* body[3];  // gate, up, down_t
@@ -61,22 +67,27 @@ struct ExpertArgs {
     int32_t H;
     int32_t maxseg;
     int64_t I;
-    int32_t nstages;
+    int32_t rows;            // R: rows per chunk
     int32_t no_copy;         // self-test: the producer issues no copies
     int32_t* status;
     uint64_t timeout_ns;
 };
 
 struct SmemCtl {
-    uint64_t full[kMaxStages];
-    uint64_t empty[kMaxStages];
-    uint64_t red[2];
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
+    uint64_t pub[2];         // gate/up sums of a chunk published (double-buffered by chunk parity)
+    uint64_t xbar;           // a job's x staged in shared memory
     int abort;
-    int never;  // stays 0: a flag nobody raises
-    float red_vals[2][kMaxConsumerWarps][kMaxV];
+    int never;               // stays 0: a flag nobody raises
+    float gu[2][2][kMaxRows][kTokensPerJob];  // [chunk parity][gate, up][row][token]
 };
 
-constexpr uint32_t kRingOffset = (sizeof(SmemCtl) + 127) / 128 * 128;
+constexpr uint32_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
+
+// Shared memory: [SmemCtl][x: MT planes x 4 float4 lanes x H/16 chunks][3 stages]
+__host__ __device__ inline uint32_t x_bytes(int H, int MT) { return static_cast<uint32_t>(MT * H * 4); }
+__host__ __device__ inline uint32_t stage_bytes(int H, int R) { return static_cast<uint32_t>(R * H / 8 * 9); }
 
 __device__ __forceinline__ Job get_job(const Job* jobs, int32_t dense_jobs, int32_t bsz, int j) {
     if (dense_jobs > 0) {
@@ -112,27 +123,6 @@ __device__ __forceinline__ Range cta_range(int32_t J, int64_t I, int64_t grid, i
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
-// Butterfly reduce-scatter of V values over a warp: returns, in lane l, the
-// warp-wide sum of value (l mod V). V - 1 + log2(32 / V) shuffles.
-template <int V>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
-#pragma unroll
-    for (int m = V / 2; m >= 1; m >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < m; ++i) {
-            const float send = upper ? v[i] : v[i + m];
-            const float keep = upper ? v[i + m] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (int m = V; m < 32; m <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, m);
-    return r;
-}
-
 
 // The walk over a CTA's rows, one chunk of at most R rows at a time (a
 // chunk never crosses a job boundary). Producer and consumers walk the
@@ -173,35 +163,37 @@ struct Walk {
     }
 };
 
+// Warp w handles gate/up rows k = w, w + NW, ... of [0, 2R) (k < R: gate
+// row k, else up row k - R). Whether it reads the gate / up stage at all:
+__device__ __forceinline__ bool reads_stage(int w, int NW, int R, int m) {
+    for (int k = w; k < 2 * R; k += NW)
+        if ((k >= R) == (m == kUp)) return true;
+    return false;
+}
+
 // ------------------------------------------------------------- producer ---
 
-// Streams, per chunk c, its gate rows, its up rows, then the down rows of
-// chunk c - 1 (the consumers use chunk c - 1's down rows while chunk c's
-// gate/up sums are being reduced across the CTA); the last chunk's down
-// rows come after the loop.
-template <int R>
-__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const Range& rg,
-                         uint32_t stage_bytes) {
+__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const Range& rg) {
     const uint64_t pol = l2_evict_first_policy();
-    const int H = a.H;
-    const uint32_t NS = static_cast<uint32_t>(a.nstages);
-    uint32_t it = 0;
+    const int H = a.H, R = a.rows;
+    const uint32_t sbytes = stage_bytes(H, R);
+    uint32_t use[kSlots] = {0u, 0u, 0u};
     bool ok = true;
 
     auto issue = [&](int m, const Job& job, int64_t r0, int rows) -> bool {
-        const uint32_t slot = it % NS, ph = (it / NS) & 1u;
-        if (!mbar_wait_bounded(smem_addr(&ctl.empty[slot]), ph ^ 1u, a.timeout_ns, &ctl.abort)) return false;
+        if (!mbar_wait_bounded(smem_addr(&ctl.empty[m]), (use[m] & 1u) ^ 1u, a.timeout_ns, &ctl.abort))
+            return false;
         const BankPtrs& bp = a.bank[job.bank];
         const int64_t row = static_cast<int64_t>(job.expert) * a.I + r0;
         const uint32_t bb = static_cast<uint32_t>(rows * H), sb = static_cast<uint32_t>(rows * (H / 8));
-        const uint32_t full = smem_addr(&ctl.full[slot]);
-        const uint32_t dst = smem_addr(ring + slot * stage_bytes);
+        const uint32_t full = smem_addr(&ctl.full[m]);
+        const uint32_t dst = smem_addr(ring + m * sbytes);
         if (!a.no_copy) {
             mbar_arrive_expect_tx(full, bb + sb);
             bulk_g2s(dst, bp.body[m] + row * H, bb, full, pol);
             bulk_g2s(dst + R * H, bp.sign[m] + row * (H / 8), sb, full, pol);
         }
-        ++it;
+        ++use[m];
         return true;
     };
 
@@ -213,159 +205,148 @@ __device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const
     int prows = 0;
     bool pending = false;
     while (!w.done() && ok) {
-        ok = issue(0, job, w.r0, w.rows) && issue(1, job, w.r0, w.rows);
-        if (ok && pending) ok = issue(2, pjob, pr0, prows);
+        ok = issue(kGate, job, w.r0, w.rows) && issue(kUp, job, w.r0, w.rows);
+        if (ok && pending) ok = issue(kDown, pjob, pr0, prows);
         pjob = job;
         pr0 = w.r0;
         prows = w.rows;
         pending = true;
         if (w.next(R)) job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
     }
-    if (ok && pending) ok = issue(2, pjob, pr0, prows);
+    if (ok && pending) ok = issue(kDown, pjob, pr0, prows);
     if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
         ctl.abort = 1;
         if (!a.no_copy) {  // let the copies already issued land before the CTA exits
-            const uint32_t first = it > NS ? it - NS : 0u;
-            for (uint32_t s = first; s < it; ++s)
-                (void)mbar_wait_bounded(smem_addr(&ctl.full[s % NS]), (s / NS) & 1u, a.timeout_ns, &ctl.never);
+            for (int m = 0; m < kSlots; ++m)
+                if (use[m] > 0)
+                    (void)mbar_wait_bounded(smem_addr(&ctl.full[m]), (use[m] - 1u) & 1u, a.timeout_ns, &ctl.never);
         }
     }
 }
 
 // ------------------------------------------------------------- consumer ---
 
-// x and y of a thread's 16 columns, per token, in the pair order of
+// y of a thread's 16 columns, per token, in the pair order of
 // decode16_pairs: p[2k] = (c[4k], c[4k+2]), p[2k+1] = (c[4k+1], c[4k+3]).
 template <int MT>
 struct Cols {
     float2 p[MT][8];
 };
 
-struct Stages {
-    uint32_t it = 0;      // stages consumed
-    uint32_t red_it = 0;  // CTA reductions started
-};
-
-__device__ __forceinline__ bool wait_stage(const ExpertArgs& a, SmemCtl& ctl, const Stages& cs, uint32_t& slot) {
-    const uint32_t NS = static_cast<uint32_t>(a.nstages);
-    slot = cs.it % NS;
-    return mbar_wait_bounded(smem_addr(&ctl.full[slot]), (cs.it / NS) & 1u, a.timeout_ns, &ctl.abort);
+template <int MT>
+__device__ __forceinline__ void zero_cols(Cols<MT>& y) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y.p[t][k] = make_float2(0.f, 0.f);
 }
 
-__device__ __forceinline__ void release_stage(SmemCtl& ctl, Stages& cs, uint32_t slot, int lane) {
+__device__ __forceinline__ bool wait_full(const ExpertArgs& a, SmemCtl& ctl, int m, uint32_t use) {
+    return mbar_wait_bounded(smem_addr(&ctl.full[m]), use & 1u, a.timeout_ns, &ctl.abort);
+}
+
+__device__ __forceinline__ void release(SmemCtl& ctl, int m, int lane) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[slot]));
-    ++cs.it;
+    if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[m]));
 }
 
-// Partial dot products of the stage's `rows` rows with x over my 16
-// columns, then their warp-level reduce-scatter into red_row[base + ...].
-template <int R, int T, int MT>
-__device__ __forceinline__ void gateup_rows(const uint8_t* st, int H, int rows, int c16, bool active,
-                                            const Cols<MT>& x, float* red_row, int base, int lane) {
-    float v[R * T];
+// Dot product of one gate/up row of a stage with x, over the whole hidden
+// dimension: lane l takes the 16-column chunks l, l + 32, ...; x comes from
+// shared memory as float4 (plane t * 4 + q holds columns 16 c + 4q .. +3 of
+// chunk c, so consecutive lanes read consecutive 16-byte words).
+template <int T, int NC>
+__device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, const float4* xs, int nch, int lane,
+                                        float (&acc)[T]) {
+    float a0[T], a1[T];
 #pragma unroll
-    for (int i = 0; i < R * T; ++i) v[i] = 0.0f;
-    if (active) {
+    for (int t = 0; t < T; ++t) a0[t] = a1[t] = 0.0f;
+    const uint8_t* brow = st + r * H;
+    const uint8_t* srow = st + R * H + r * (H / 8);
+    auto step = [&](int c) {
+        const uint4 b = *reinterpret_cast<const uint4*>(brow + c * 16);
+        const uint32_t s16 = *reinterpret_cast<const uint16_t*>(srow + c * 2);
+        float2 w[8];
+        decode16_pairs(b, s16, w);
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-            if (rr < rows) {
-                const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
-                const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
-                float2 w[8];
-                decode16_pairs(b, s16, w);
+        for (int t = 0; t < T; ++t) {
 #pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        a0 = fmaf(w[k].x, x.p[t][k].x, a0);
-                        a1 = fmaf(w[k].y, x.p[t][k].y, a1);
-                    }
-                    v[rr * T + t] = a0 + a1;
-                }
+            for (int q = 0; q < 4; ++q) {
+                const float4 xv = xs[(t * 4 + q) * nch + c];
+                a0[t] = fmaf(w[2 * q].x, xv.x, a0[t]);
+                a1[t] = fmaf(w[2 * q].y, xv.z, a1[t]);
+                a0[t] = fmaf(w[2 * q + 1].x, xv.y, a0[t]);
+                a1[t] = fmaf(w[2 * q + 1].y, xv.w, a1[t]);
             }
         }
+    };
+    if constexpr (NC > 0) {  // every lane has NC chunks: no bounds test
+#pragma unroll 2
+        for (int i = 0; i < NC; ++i) step(lane + 32 * i);
+    } else {
+#pragma unroll 2
+        for (int c = lane; c < nch; c += 32) step(c);
     }
-    const float r = warp_reduce_scatter<R * T>(v, lane);
-    if (lane < R * T) red_row[base + lane] = r;
+#pragma unroll
+    for (int t = 0; t < T; ++t) acc[t] = warp_sum(a0[t] + a1[t]);
+}
+
+// This warp's rows of the gate (m = 0) or up (m = 1) stage of a chunk;
+// lane 0 publishes each row's sums into gu[par][m][row][token].
+template <int T, int NC>
+__device__ __forceinline__ void gateup_stage(SmemCtl& ctl, const uint8_t* st, int H, int R, int rows, int m,
+                                             uint32_t par, const float4* xs, int nch, int warp, int NW, int lane) {
+    for (int k = warp; k < 2 * R; k += NW) {
+        if ((k >= R) != (m == kUp)) continue;
+        const int r = k - m * R;
+        if (r >= rows) continue;
+        float acc[T];
+        row_dot<T, NC>(st, H, R, r, xs, nch, lane, acc);
+        if (lane == 0) {
+#pragma unroll
+            for (int t = 0; t < T; ++t) ctl.gu[par][m][r][t] = acc[t];
+        }
+    }
 }
 
 // y[c] += h_row * W_down^T[row, c] over my 16 columns; lane (rr * T + t)
-// of `hv` holds h of row rr, token t.
-template <int R, int T, int MT>
-__device__ __forceinline__ void down_rows(const uint8_t* st, int H, int rows, int c16, bool active, float hv,
-                                          Cols<MT>& y) {
-    float h[R][T];
+// of `hv` holds h of row rr, token t. RC > 0: a full chunk of RC rows and
+// every lane active (no guards).
+template <int T, int MT>
+__device__ __forceinline__ void down_row(const uint8_t* st, int H, int R, int rr, int c16, float hv, Cols<MT>& y) {
+    float h[T];
 #pragma unroll
-    for (int rr = 0; rr < R; ++rr)
+    for (int t = 0; t < T; ++t) h[t] = __shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
+    const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
+    const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
+    float2 w[8];
+    decode16_pairs(b, s16, w);
 #pragma unroll
-        for (int t = 0; t < T; ++t) h[rr][t] = __shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
-    if (!active) return;
+    for (int t = 0; t < T; ++t)
 #pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-        if (rr < rows) {
-            const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
-            const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
-            float2 w[8];
-            decode16_pairs(b, s16, w);
+        for (int k = 0; k < 8; ++k) {
+            y.p[t][k].x = fmaf(h[t], w[k].x, y.p[t][k].x);
+            y.p[t][k].y = fmaf(h[t], w[k].y, y.p[t][k].y);
+        }
+}
+
+template <int T, int MT, int RC>
+__device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int rows, int c16, bool active, float hv,
+                                           Cols<MT>& y) {
+    if (RC > 0 && rows == RC) {
 #pragma unroll
-            for (int t = 0; t < T; ++t)
+        for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, c16, hv, y);
+        return;
+    }
+#pragma unroll 1
+    for (int rr = 0; rr < rows; ++rr) {
+        if (active) {
+            down_row<T, MT>(st, H, R, rr, c16, hv, y);
+        } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    y.p[t][k].x = fmaf(h[rr][t], w[k].x, y.p[t][k].x);
-                    y.p[t][k].y = fmaf(h[rr][t], w[k].y, y.p[t][k].y);
-                }
+            for (int t = 0; t < T; ++t) (void)__shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
         }
     }
-}
-
-// Gate and up stages of one chunk: waits, computes, releases, and writes
-// this warp's reduced values for the chunk's CTA sum. Returns false on timeout.
-template <int R, int T, int MT>
-__device__ __forceinline__ bool gateup_chunk(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
-                                             uint32_t stage_bytes, Stages& cs, int rows, int c16, bool active,
-                                             const Cols<MT>& x, int warp, int lane) {
-    float* red_row = ctl.red_vals[cs.red_it & 1u][warp];
-#pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
-        uint32_t slot;
-        if (!wait_stage(a, ctl, cs, slot)) return false;
-        gateup_rows<R, T, MT>(ring + slot * stage_bytes, a.H, rows, c16, active, x, red_row, m * R * T, lane);
-        release_stage(ctl, cs, slot, lane);
-    }
-    if (lane == 0) mbar_arrive(smem_addr(&ctl.red[cs.red_it & 1u]));
-    return true;
-}
-
-template <int R, int T, int MT>
-__device__ __forceinline__ bool down_chunk(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
-                                           uint32_t stage_bytes, Stages& cs, int rows, int c16, bool active,
-                                           float hv, Cols<MT>& y, int lane) {
-    uint32_t slot;
-    if (!wait_stage(a, ctl, cs, slot)) return false;
-    down_rows<R, T, MT>(ring + slot * stage_bytes, a.H, rows, c16, active, hv, y);
-    release_stage(ctl, cs, slot, lane);
-    return true;
-}
-
-// Completes the CTA sum of chunk `red_it` and returns, in lane
-// (rr * T + t), h = SiLU(g) * u * w_route for row rr, token t.
-template <int R, int T>
-__device__ __forceinline__ bool finish_sum(const ExpertArgs& a, SmemCtl& ctl, Stages& cs, float w0, float w1, int NW,
-                                           int lane, float& hv) {
-    constexpr int V = R * T;
-    const uint32_t b = cs.red_it & 1u;
-    if (!mbar_wait_bounded(smem_addr(&ctl.red[b]), (cs.red_it >> 1) & 1u, a.timeout_ns, &ctl.abort)) return false;
-    ++cs.red_it;
-    float tot = 0.0f;
-    if (lane < 2 * V)
-        for (int w = 0; w < NW; ++w) tot += ctl.red_vals[b][w][lane];
-    const float u = __shfl_down_sync(0xFFFFFFFFu, tot, V);
-    const float wt = (T == 2 && (lane & 1)) ? w1 : w0;
-    hv = (lane < V) ? silu(tot) * u * wt : 0.0f;
-    return true;
 }
 
 // What the consumers keep of a job: its token count, routing weights, and
@@ -406,89 +387,129 @@ __device__ __forceinline__ void flush_partial(const ExpertArgs& a, int ntok, int
     }
 }
 
+// Stages the job's x into shared memory (plane t * 4 + q, chunk c =
+// columns 16 c + 4 q .. +3 of token t), then waits until every consumer
+// warp has written its share.
 template <int MT>
-__device__ __forceinline__ void load_x(const ExpertArgs& a, const Job& job, int c16, bool active, Cols<MT>& x) {
-#pragma unroll
+__device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const Job& job, int nch,
+                                        int tid, int NT, uint32_t& xuse, int lane) {
+    const int H4 = a.H / 4;
     for (int t = 0; t < MT; ++t) {
-        const bool use = active && t < job.ntok;
+        if (t >= job.ntok) break;
         const int tok = t == 0 ? job.tok[0] : job.tok[1];
-        const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H + c16 * 16);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 xv = use ? __ldg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-            x.p[t][2 * k] = make_float2(xv.x, xv.z);
-            x.p[t][2 * k + 1] = make_float2(xv.y, xv.w);
-        }
+        const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H);
+        for (int j = tid; j < H4; j += NT) xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = __ldg(src + j);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl.xbar));
+    const bool ok = mbar_wait_bounded(smem_addr(&ctl.xbar), xuse & 1u, a.timeout_ns, &ctl.abort);
+    ++xuse;
+    return ok;
 }
 
-template <int MT>
-__device__ __forceinline__ void zero_cols(Cols<MT>& y) {
-#pragma unroll
-    for (int t = 0; t < MT; ++t)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) y.p[t][k] = make_float2(0.f, 0.f);
-}
+// The fixed shape of a specialised kernel: hidden size HC (0: any), its
+// 16-column chunks per lane, and its rows per chunk (one gate/up row per
+// consumer warp).
+template <int HC>
+struct Shape {
+    static constexpr int kNch = HC / 16;
+    static constexpr int kNW = (kNch + 31) / 32;
+    static constexpr int kNC = (HC > 0 && kNch % 32 == 0) ? kNch / 32 : 0;
+    static constexpr int kRows = HC > 0 ? (kNW / 2 > 4 ? kNW / 2 : 4) : 0;
+};
 
-// Per chunk c: gate/up of c, arrive at c's CTA sum, down rows of c - 1
-// (whose h is known), then wait for c's sum. x follows the gate/up job, y
-// the down job; y is written out (and cleared) after the last down chunk
-// of each job.
-template <int R, int MT>
-__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring, const Range& rg,
-                         uint32_t stage_bytes, int NW, int warp, int lane) {
+template <int MT, int HC>
+__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const uint8_t* ring, const Range& rg,
+                         int NW, int warp, int lane) {
+    using S = Shape<HC>;
+    const int H = HC > 0 ? HC : a.H;
+    const int R = S::kRows > 0 ? S::kRows : a.rows;
+    if (S::kNW > 0) NW = S::kNW;
+    const int nch = H / 16;
     const int c16 = warp * 32 + lane;
-    const bool active = c16 < a.H / 16;
-    Cols<MT> x, y;
+    const bool active = c16 < nch;
+    const uint32_t sbytes = stage_bytes(H, R);
+    const bool rd_gate = reads_stage(warp, NW, R, kGate), rd_up = reads_stage(warp, NW, R, kUp);
+    Cols<MT> y;
+    zero_cols(y);
     Walk w;
     w.begin(rg, a.I, R);
     Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
-    load_x(a, job, c16, active, x);
     JobState js = job_state(a, job, w.j, rg);
-    zero_cols(y);
-    Stages cs;
-    bool ok = true;
+    uint32_t xuse = 0;
+    bool ok = stage_x<MT>(a, ctl, xs, job, nch, warp * 32 + lane, NW * 32, xuse, lane);
+    uint32_t c = 0;  // chunk index: uses of the gate and up slots, and the publish parity
     // the chunk whose down rows are pending
     bool pending = false, p_last_of_job = false;
     int p_rows = 0, p_ntok = 1, p_slot0 = 0, p_slot1 = 0;
     float p_hv = 0.0f;
 
-    while (!w.done()) {
+    while (ok && !w.done()) {
         const int T = MT == 1 ? 1 : js.ntok;
-        ok = (T == 2) ? gateup_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane)
-                      : gateup_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, w.rows, c16, active, x, warp, lane);
+        const uint32_t par = c & 1u;
+        for (int m = kGate; m <= kUp && ok; ++m) {
+            if (!(m == kGate ? rd_gate : rd_up)) continue;
+            if (!wait_full(a, ctl, m, c)) {
+                ok = false;
+                break;
+            }
+            if (T == 2)
+                gateup_stage<MT, S::kNC>(ctl, ring + m * sbytes, H, R, w.rows, m, par, xs, nch, warp, NW, lane);
+            else
+                gateup_stage<1, S::kNC>(ctl, ring + m * sbytes, H, R, w.rows, m, par, xs, nch, warp, NW, lane);
+            release(ctl, m, lane);
+        }
         if (!ok) break;
+        if (lane == 0) mbar_arrive(smem_addr(&ctl.pub[par]));
         if (pending) {
-            ok = (p_ntok == 2)
-                     ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
-                     : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
-            if (!ok) break;
+            if (!wait_full(a, ctl, kDown, c - 1u)) {
+                ok = false;
+                break;
+            }
+            if (p_ntok == 2)
+                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            else
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            release(ctl, kDown, lane);
             if (p_last_of_job) {
                 flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
                 zero_cols(y);
             }
         }
-        float hv;
-        ok = (T == 2) ? finish_sum<R, MT>(a, ctl, cs, js.w0, js.w1, NW, lane, hv)
-                      : finish_sum<R, 1>(a, ctl, cs, js.w0, js.w1, NW, lane, hv);
-        if (!ok) break;
+        if (!mbar_wait_bounded(smem_addr(&ctl.pub[par]), (c >> 1) & 1u, a.timeout_ns, &ctl.abort)) {
+            ok = false;
+            break;
+        }
+        float hv = 0.0f;  // lane (r * T + t): h of row r, token t
+        if (lane < R * T) {
+            const int r = lane / T, t = lane % T;
+            const float wt = t == 0 ? js.w0 : js.w1;
+            hv = silu(ctl.gu[par][kGate][r][t]) * ctl.gu[par][kUp][r][t] * wt;
+        }
         pending = true;
         p_rows = w.rows;
         p_ntok = T;
         p_slot0 = js.slot0;
         p_slot1 = js.slot1;
         p_hv = hv;
+        ++c;
         p_last_of_job = w.next(R);
-        if (p_last_of_job) {
+        if (p_last_of_job) {  // every warp has finished the previous job's gate/up rows
             job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
-            load_x(a, job, c16, active, x);
             js = job_state(a, job, w.j, rg);
+            ok = stage_x<MT>(a, ctl, xs, job, nch, warp * 32 + lane, NW * 32, xuse, lane);
         }
     }
     if (ok && pending) {
-        ok = (p_ntok == 2) ? down_chunk<R, MT, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane)
-                           : down_chunk<R, 1, MT>(a, ctl, ring, stage_bytes, cs, p_rows, c16, active, p_hv, y, lane);
-        if (ok) flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
+        ok = wait_full(a, ctl, kDown, c - 1u);
+        if (ok) {
+            if (p_ntok == 2)
+                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            else
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            release(ctl, kDown, lane);
+            flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
+        }
     }
     if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
@@ -496,15 +517,16 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, const uint8_t* ring,
     }
 }
 
-// R: rows per chunk; MT: most tokens a job can hold (1 when bsz == 1).
-template <int R, int MT>
+// MT: most tokens a job can hold (1 when bsz == 1). HC: the hidden size
+// the kernel is specialised for (0: any).
+template <int MT, int HC>
 __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem);
-    uint8_t* ring = smem + kRingOffset;
+    float4* xs = reinterpret_cast<float4*>(smem + kCtlBytes);
+    uint8_t* ring = smem + kCtlBytes + (x_bytes(a.H, MT) + 127u) / 128u * 128u;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NW = static_cast<int>(blockDim.x / 32) - 1;
-    const uint32_t stage_bytes = static_cast<uint32_t>(R * a.H / 8 * 9);
 
     grid_dependency_wait();  // the router's job list and x are complete
     grid_launch_dependents();
@@ -513,12 +535,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     if (rg.start >= rg.end) return;
 
     if (tid == 0) {
-        for (int s = 0; s < a.nstages; ++s) {
-            mbar_init(smem_addr(&ctl.full[s]), 1);
-            mbar_init(smem_addr(&ctl.empty[s]), NW);
+        int gate_readers = 0, up_readers = 0;
+        for (int w = 0; w < NW; ++w) {
+            gate_readers += reads_stage(w, NW, a.rows, kGate) ? 1 : 0;
+            up_readers += reads_stage(w, NW, a.rows, kUp) ? 1 : 0;
         }
-        mbar_init(smem_addr(&ctl.red[0]), NW);
-        mbar_init(smem_addr(&ctl.red[1]), NW);
+        for (int m = 0; m < kSlots; ++m) mbar_init(smem_addr(&ctl.full[m]), 1);
+        mbar_init(smem_addr(&ctl.empty[kGate]), gate_readers);
+        mbar_init(smem_addr(&ctl.empty[kUp]), up_readers);
+        mbar_init(smem_addr(&ctl.empty[kDown]), NW);
+        mbar_init(smem_addr(&ctl.pub[0]), NW);
+        mbar_init(smem_addr(&ctl.pub[1]), NW);
+        mbar_init(smem_addr(&ctl.xbar), NW);
         ctl.abort = 0;
         ctl.never = 0;
         fence_mbar_init();
@@ -526,10 +554,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     __syncthreads();
 
     if (warp == NW) {
-        if (lane == 0) producer<R>(a, ctl, ring, rg, stage_bytes);
+        if (lane == 0) producer(a, ctl, ring, rg);
         return;
     }
-    consumer<R, MT>(a, ctl, ring, rg, stage_bytes, NW, warp, lane);
+    consumer<MT, HC>(a, ctl, xs, ring, rg, NW, warp, lane);
 }
 
 // ------------------------------------------------------------- combine ----
@@ -614,54 +642,48 @@ static BankPtrs bank_ptrs(const fp9_ffn_bank& b) {
 
 struct LaunchShape {
     int threads;
-    int nstages;
     int rows;
     size_t smem;
 };
 
-// Rows per streamed chunk: 8 unless FP9MOE_CHUNK_ROWS=4 is set (a tuning
-// knob: 8 halves the per-chunk reduction cost, 4 allows twice the stages).
-static int chunk_rows() {
-    static int rows = 0;
-    if (rows == 0) {
-        const char* e = getenv("FP9MOE_CHUNK_ROWS");
-        rows = (e != nullptr && atoi(e) == 4) ? 4 : 8;
-    }
-    return rows;
-}
+constexpr int kDsv3Hidden = 7168;
 
-static fp9_status expert_shape(int32_t H, LaunchShape& s) {
+// Rows per chunk: half the consumer warps (so that the 2R gate/up rows of a
+// chunk give every warp one row; 7 for hidden 7168), at least 4, and as
+// many as fit in shared memory next to x.
+static fp9_status expert_shape(int32_t H, int MT, LaunchShape& s) {
     const int nw = (H / 16 + 31) / 32;
     s.threads = nw * 32 + 32;
-    s.rows = chunk_rows();
-    const uint32_t stage = static_cast<uint32_t>(s.rows * H / 8 * 9);
     const int32_t optin = device_max_smem_optin();
     if (optin <= 0) return FP9_ERR_CUDA;
-    int ns = static_cast<int>((static_cast<int64_t>(optin) - kRingOffset) / stage);
-    if (ns > kMaxStages) ns = kMaxStages;
-    if (ns < 3) return FP9_ERR_SHAPE;
-    s.nstages = ns;
-    s.smem = kRingOffset + static_cast<size_t>(ns) * stage;
+    int R = nw / 2 > 4 ? nw / 2 : 4;
+    if (R > kMaxRows) R = kMaxRows;
+    const size_t fixed = kCtlBytes + (x_bytes(H, MT) + 127u) / 128u * 128u;
+    while (R > 1 && fixed + kSlots * static_cast<size_t>(stage_bytes(H, R)) > static_cast<size_t>(optin)) --R;
+    if (fixed + kSlots * static_cast<size_t>(stage_bytes(H, R)) > static_cast<size_t>(optin)) return FP9_ERR_SHAPE;
+    s.rows = R;
+    s.smem = fixed + kSlots * static_cast<size_t>(stage_bytes(H, R));
     return FP9_OK;
 }
 
-template <int R, int MT>
-static cudaError_t set_smem(size_t smem) {
-    return cudaFuncSetAttribute(expert_kernel<R, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+template <int MT, int HC>
+static cudaError_t set_smem(int optin) {
+    return cudaFuncSetAttribute(expert_kernel<MT, HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
-static fp9_status ensure_smem_attr(size_t smem) {
-    static size_t configured[64] = {0};
+static fp9_status ensure_smem_attr() {
+    static bool configured[64] = {false};
     int dev = 0;
     FP9_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
-    if (configured[dev] < smem) {
-        FP9_CUDA_TRY((set_smem<4, 1>(smem)));
-        FP9_CUDA_TRY((set_smem<8, 1>(smem)));
-        FP9_CUDA_TRY((set_smem<4, 2>(smem)));
-        FP9_CUDA_TRY((set_smem<8, 2>(smem)));
-        configured[dev] = smem;
+    if (!configured[dev]) {
+        const int32_t optin = device_max_smem_optin();
+        if (optin <= 0) return FP9_ERR_CUDA;
+        FP9_CUDA_TRY((set_smem<1, 0>(optin)));
+        FP9_CUDA_TRY((set_smem<2, 0>(optin)));
+        FP9_CUDA_TRY((set_smem<1, kDsv3Hidden>(optin)));
+        FP9_CUDA_TRY((set_smem<2, kDsv3Hidden>(optin)));
+        configured[dev] = true;
     }
     return FP9_OK;
 }
@@ -674,10 +696,11 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
                              int32_t H, int64_t I, uint8_t* ws, const WsLayout& lay, int32_t dense_jobs,
                              int32_t* status, cudaStream_t stream, uint64_t timeout_ns, bool no_copy,
                              bool combine) {
+    const int MT = bsz == 1 ? 1 : 2;  // jobs hold two tokens only when bsz >= 2
     LaunchShape shp;
-    fp9_status st = expert_shape(H, shp);
+    fp9_status st = expert_shape(H, MT, shp);
     if (st != FP9_OK) return st;
-    st = ensure_smem_attr(shp.smem);
+    st = ensure_smem_attr();
     if (st != FP9_OK) return st;
     ExpertArgs a;
     a.bank[0] = b0;
@@ -691,17 +714,16 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
     a.H = H;
     a.maxseg = lay.maxseg;
     a.I = I;
-    a.nstages = shp.nstages;
+    a.rows = shp.rows;
     a.no_copy = no_copy ? 1 : 0;
     a.status = status;
     a.timeout_ns = timeout_ns;
     const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_start, stream));
-    // jobs hold two tokens only when bsz >= 2; the one-token kernel keeps
-    // half the x / y registers live
-    void (*kern)(const ExpertArgs) = nullptr;
-    if (bsz == 1) kern = shp.rows == 8 ? expert_kernel<8, 1> : expert_kernel<4, 1>;
-    else kern = shp.rows == 8 ? expert_kernel<8, 2> : expert_kernel<4, 2>;
+    // the DeepSeek-V3 hidden size has its own kernel with every loop bound fixed
+    const bool special = H == kDsv3Hidden && shp.rows == Shape<kDsv3Hidden>::kRows;
+    void (*kern)(const ExpertArgs) = special ? (MT == 1 ? expert_kernel<1, kDsv3Hidden> : expert_kernel<2, kDsv3Hidden>)
+                                             : (MT == 1 ? expert_kernel<1, 0> : expert_kernel<2, 0>);
     FP9_CUDA_TRY(launch_pdl(kern, dim3(lay.grid), dim3(shp.threads), shp.smem, stream, a));
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_stop, stream));
     if (!combine) return FP9_OK;
