@@ -15,13 +15,14 @@
 // in registers and writes it once per job it touches, and a second kernel
 // adds those partials in a fixed order.
 //
-// CTA layout (one per SM): NW consumer warps and one producer warp. The
-// producer's lane 0 streams each chunk of R rows as three stages, one per
-// ring slot: slot 0 the gate rows, slot 1 the up rows, slot 2 the down rows
-// (bodies, then signs; bulk copies completing on mbarriers).
-//   gate/up: the 2R rows of a chunk are dealt round-robin to the warps; a
-//     warp computes whole rows (x is staged in shared memory), so the only
-//     reduction is a 5-step warp sum per row; lane 0 publishes g or u.
+// CTA layout (one per SM): NW = H / 512 consumer warps (14 for H = 7168)
+// and one producer warp. The producer's lane 0 streams each chunk of
+// R = NW / 2 rows as three stages, one per ring slot: slot 0 the gate rows,
+// slot 1 the up rows, slot 2 the down rows (bodies, then signs; bulk copies
+// completing on mbarriers).
+//   gate/up: the 2R rows of a chunk are dealt to the warps, one row each; a
+//     warp computes its row against x (staged in shared memory), so the
+//     only reduction is a 5-step warp sum; lane 0 publishes the sum.
 //   down: each thread owns 16 consecutive hidden columns and keeps y for
 //     them in registers: an axpy with no reduction.
 // Per chunk c a warp does its gate/up rows, arrives at c's publish barrier,
@@ -46,7 +47,8 @@ namespace fp9 {
 
 constexpr int kMaxRows = 16;                                    // rows per chunk
 constexpr int kSlots = 3;                                       // gate, up, down
-constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / 16 / 32;     // 14
+constexpr int kDownCols = 16;                                   // down columns per thread
+constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / kDownCols / 32;  // 14
 constexpr int kMaxThreads = kMaxConsumerWarps * 32 + 32;        // 480
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;           // 1 s
 constexpr int kGate = 0, kUp = 1, kDown = 2;
@@ -59,13 +61,17 @@ struct BankPtrs {
 struct ExpertArgs {
     BankPtrs bank[2];        // 0: routed experts / dense FFN, 1: shared experts
     const float* x;          // [bsz, H]
-    float* partial;          // token-major: [bsz * maxseg, H]
-    const Job* jobs;         // MoE mode
-    const Control* ctl;      // MoE mode: job count
-    int32_t dense_jobs;      // > 0: dense mode, jobs are implicit
+    float* partial;          // token-major: [bsz * gridDim.x, H]
+    uint32_t* mask;          // [gridDim.x]: bit t = partial of token t written
+    const Job* jobs;         // phase 1: the router's jobs
+    const Control* ctl;      // phase 1: CTAs that own rows
+    const int64_t* cta_row;  // phase 1: [geff + 1] first row (job * I + row) of each CTA
+    int32_t impl_jobs;       // phase 0: jobs that need no routing
+    int32_t impl_nexp;       // phase 0: experts of the bank (shared experts, or 1 for the dense FFN)
+    int32_t impl_bank;       // phase 0: 1 (shared experts) or 0 (dense FFN)
+    int32_t routed;          // 1: phase 1 runs on the router's plan (MoE call)
     int32_t bsz;
     int32_t H;
-    int32_t maxseg;
     int64_t I;
     int32_t rows;            // R: rows per chunk
     int32_t no_copy;         // self-test: the producer issues no copies
@@ -89,82 +95,87 @@ constexpr uint32_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
 __host__ __device__ inline uint32_t x_bytes(int H, int MT) { return static_cast<uint32_t>(MT * H * 4); }
 __host__ __device__ inline uint32_t stage_bytes(int H, int R) { return static_cast<uint32_t>(R * H / 8 * 9); }
 
-__device__ __forceinline__ Job get_job(const Job* jobs, int32_t dense_jobs, int32_t bsz, int j) {
-    if (dense_jobs > 0) {
-        Job jb;
-        jb.bank = 0;
-        jb.expert = 0;
-        jb.pad[0] = jb.pad[1] = 0;
-        jb.tok[0] = kTokensPerJob * j;
-        jb.ntok = (kTokensPerJob * j + 1 < bsz) ? 2 : 1;
-        jb.tok[1] = jb.ntok == 2 ? jb.tok[0] + 1 : jb.tok[0];
-        jb.w[0] = 1.0f;
-        jb.w[1] = jb.ntok == 2 ? 1.0f : 0.0f;
-        jb.b0 = -1;  // computed where needed
-        jb.seg_base[0] = jb.seg_base[1] = 0;  // a dense token is in exactly one job
-        return jb;
-    }
-    return jobs[j];
-}
-
-// Rows [start, end) of the job sequence owned by CTA b. Only the first
-// min(G, N) CTAs get rows, so every CTA that works owns at least one row.
-struct Range {
-    int64_t start, end, n, g;
-};
-
-__device__ __forceinline__ Range cta_range(int32_t J, int64_t I, int64_t grid, int64_t b) {
-    Range r;
-    r.n = static_cast<int64_t>(J) * I;
-    r.g = r.n < grid ? r.n : grid;
-    r.start = b < r.g ? cta_start(b, r.n, r.g) : 0;
-    r.end = b < r.g ? cta_start(b + 1, r.n, r.g) : 0;
-    return r;
-}
-
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
-// The walk over a CTA's rows, one chunk of at most R rows at a time (a
-// chunk never crosses a job boundary). Producer and consumers walk the
-// same sequence.
+// The walk over a CTA's chunks: its rows of phase 0 (the jobs that need no
+// routing, split evenly by rows over the first min(G, N) CTAs), then, for an
+// MoE call, its rows of phase 1 (the router's cost-weighted split). Row
+// j * I + r of a phase is row r of its job j; a chunk of at most R rows
+// never crosses a job boundary. Producer and consumers walk the same
+// sequence; every thread that walks into phase 1 first waits for the
+// router's grid, so it reads the plan only once the plan is complete.
 struct Walk {
-    int64_t pos, end, I, r0;
+    int phase;
+    int32_t pos, end, I, r0;  // rows of a phase number at most kMaxJobs * FP9_MAX_INTER < 2^31
     int j;
     int rows;  // rows of the current chunk
+    Job job;
 
-    __device__ __forceinline__ void begin(const Range& rg, int64_t I_, int R) {
-        I = I_;
-        pos = rg.start;
-        end = rg.end;
-        j = static_cast<int>(pos / I);
-        r0 = pos - static_cast<int64_t>(j) * I;
-        set_rows(R);
+    __device__ __forceinline__ void load_job(const ExpertArgs& a) {
+        job = phase == 0 ? implicit_job(j, a.impl_nexp, a.impl_bank, a.bsz) : a.jobs[j];
+    }
+    __device__ __forceinline__ void set_phase(const ExpertArgs& a, int ph) {
+        phase = ph;
+        int64_t s = 0, e = 0;
+        const int64_t b = blockIdx.x;
+        if (ph == 0) {
+            const int64_t n = static_cast<int64_t>(a.impl_jobs) * I;
+            const int64_t g = n < gridDim.x ? n : gridDim.x;
+            if (b < g) {
+                s = cta_start(b, n, g);
+                e = cta_start(b + 1, n, g);
+            }
+        } else {
+            grid_dependency_wait();  // the router's plan is complete and visible
+            if (b < a.ctl->geff) {
+                s = a.cta_row[b];
+                e = a.cta_row[b + 1];
+            }
+        }
+        pos = static_cast<int32_t>(s);
+        end = static_cast<int32_t>(e);
+        j = pos / I;
+        r0 = pos - j * I;
     }
     __device__ __forceinline__ void set_rows(int R) {
         int r = R;
-        if (I - r0 < r) r = static_cast<int>(I - r0);
-        if (end - pos < r) r = static_cast<int>(end - pos);
+        if (I - r0 < r) r = I - r0;
+        if (end - pos < r) r = end - pos;
         rows = r;
+    }
+    __device__ __forceinline__ void begin(const ExpertArgs& a, int R) {
+        I = static_cast<int32_t>(a.I);
+        set_phase(a, 0);
+        if (pos >= end && a.routed) set_phase(a, 1);
+        if (pos < end) load_job(a);
+        set_rows(R);
     }
     __device__ __forceinline__ bool done() const { return pos >= end; }
     // Advances past the current chunk; returns true when the next chunk
     // starts a new job.
-    __device__ __forceinline__ bool next(int R) {
+    __device__ __forceinline__ bool next(const ExpertArgs& a, int R) {
         pos += rows;
         r0 += rows;
         bool new_job = false;
-        if (r0 == I && pos < end) {
+        if (pos >= end) {
+            if (phase == 0 && a.routed) {
+                set_phase(a, 1);
+                new_job = pos < end;
+            }
+        } else if (r0 == I) {
             ++j;
             r0 = 0;
             new_job = true;
         }
+        if (new_job) load_job(a);
         set_rows(R);
         return new_job;
     }
 };
 
-// Warp w handles gate/up rows k = w, w + NW, ... of [0, 2R) (k < R: gate
-// row k, else up row k - R). Whether it reads the gate / up stage at all:
+// Warp w handles the gate/up rows k = w, w + NW, ... of [0, 2R): rows
+// [0, R) are the gate rows and [R, 2R) the up rows. Whether it reads the
+// gate / up stage at all:
 __device__ __forceinline__ bool reads_stage(int w, int NW, int R, int m) {
     for (int k = w; k < 2 * R; k += NW)
         if ((k >= R) == (m == kUp)) return true;
@@ -173,7 +184,7 @@ __device__ __forceinline__ bool reads_stage(int w, int NW, int R, int m) {
 
 // ------------------------------------------------------------- producer ---
 
-__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const Range& rg) {
+__device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring) {
     const uint64_t pol = l2_evict_first_policy();
     const int H = a.H, R = a.rows;
     const uint32_t sbytes = stage_bytes(H, R);
@@ -198,20 +209,19 @@ __device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring, const
     };
 
     Walk w;
-    w.begin(rg, a.I, R);
-    Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
-    Job pjob = job;
+    w.begin(a, R);
+    Job pjob = w.job;
     int64_t pr0 = 0;
     int prows = 0;
     bool pending = false;
     while (!w.done() && ok) {
-        ok = issue(kGate, job, w.r0, w.rows) && issue(kUp, job, w.r0, w.rows);
+        ok = issue(kGate, w.job, w.r0, w.rows) && issue(kUp, w.job, w.r0, w.rows);
         if (ok && pending) ok = issue(kDown, pjob, pr0, prows);
-        pjob = job;
+        pjob = w.job;
         pr0 = w.r0;
         prows = w.rows;
         pending = true;
-        if (w.next(R)) job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
+        (void)w.next(a, R);
     }
     if (ok && pending) ok = issue(kDown, pjob, pr0, prows);
     if (!ok) {
@@ -254,13 +264,16 @@ __device__ __forceinline__ void release(SmemCtl& ctl, int m, int lane) {
 // Dot product of one gate/up row of a stage with x, over the whole hidden
 // dimension: lane l takes the 16-column chunks l, l + 32, ...; x comes from
 // shared memory as float4 (plane t * 4 + q holds columns 16 c + 4q .. +3 of
-// chunk c, so consecutive lanes read consecutive 16-byte words).
+// chunk c in the order (0, 2, 1, 3), so consecutive lanes read consecutive
+// 16-byte words and each half of the float4 pairs with one decoded weight
+// pair of decode16_pairs). The multiply-adds run two at a time (packed
+// fp32 FMA, each lane of it rounded like fmaf).
 template <int T, int NC>
 __device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, const float4* xs, int nch, int lane,
                                         float (&acc)[T]) {
-    float a0[T], a1[T];
+    float2 a0[T], a1[T];
 #pragma unroll
-    for (int t = 0; t < T; ++t) a0[t] = a1[t] = 0.0f;
+    for (int t = 0; t < T; ++t) a0[t] = a1[t] = make_float2(0.0f, 0.0f);
     const uint8_t* brow = st + r * H;
     const uint8_t* srow = st + R * H + r * (H / 8);
     auto step = [&](int c) {
@@ -273,10 +286,8 @@ __device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, 
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 xv = xs[(t * 4 + q) * nch + c];
-                a0[t] = fmaf(w[2 * q].x, xv.x, a0[t]);
-                a1[t] = fmaf(w[2 * q].y, xv.z, a1[t]);
-                a0[t] = fmaf(w[2 * q + 1].x, xv.y, a0[t]);
-                a1[t] = fmaf(w[2 * q + 1].y, xv.w, a1[t]);
+                a0[t] = __ffma2_rn(w[2 * q], make_float2(xv.x, xv.y), a0[t]);
+                a1[t] = __ffma2_rn(w[2 * q + 1], make_float2(xv.z, xv.w), a1[t]);
             }
         }
     };
@@ -288,7 +299,7 @@ __device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, 
         for (int c = lane; c < nch; c += 32) step(c);
     }
 #pragma unroll
-    for (int t = 0; t < T; ++t) acc[t] = warp_sum(a0[t] + a1[t]);
+    for (int t = 0; t < T; ++t) acc[t] = warp_sum((a0[t].x + a0[t].y) + (a1[t].x + a1[t].y));
 }
 
 // This warp's rows of the gate (m = 0) or up (m = 1) stage of a chunk;
@@ -310,38 +321,38 @@ __device__ __forceinline__ void gateup_stage(SmemCtl& ctl, const uint8_t* st, in
 }
 
 // y[c] += h_row * W_down^T[row, c] over my 16 columns; lane (rr * T + t)
-// of `hv` holds h of row rr, token t. RC > 0: a full chunk of RC rows and
-// every lane active (no guards).
+// of `hv` holds h of row rr, token t.
 template <int T, int MT>
-__device__ __forceinline__ void down_row(const uint8_t* st, int H, int R, int rr, int c16, float hv, Cols<MT>& y) {
+__device__ __forceinline__ void down_row(const uint8_t* st, int H, int R, int rr, int cc, float hv, Cols<MT>& y) {
     float h[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) h[t] = __shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
-    const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + c16 * 16);
-    const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + c16 * 2);
+    const uint4 b = *reinterpret_cast<const uint4*>(st + rr * H + cc * 16);
+    const uint32_t s16 = *reinterpret_cast<const uint16_t*>(st + R * H + rr * (H / 8) + cc * 2);
     float2 w[8];
     decode16_pairs(b, s16, w);
 #pragma unroll
-    for (int t = 0; t < T; ++t)
+    for (int t = 0; t < T; ++t) {
+        const float2 hh = make_float2(h[t], h[t]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            y.p[t][k].x = fmaf(h[t], w[k].x, y.p[t][k].x);
-            y.p[t][k].y = fmaf(h[t], w[k].y, y.p[t][k].y);
-        }
+        for (int k = 0; k < 8; ++k) y.p[t][k] = __ffma2_rn(hh, w[k], y.p[t][k]);
+    }
 }
 
+// The down rows of a chunk. RC > 0: a full chunk of RC rows with every lane
+// active is unrolled (no guards).
 template <int T, int MT, int RC>
-__device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int rows, int c16, bool active, float hv,
+__device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int rows, int cc, bool active, float hv,
                                            Cols<MT>& y) {
     if (RC > 0 && rows == RC) {
 #pragma unroll
-        for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, c16, hv, y);
+        for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, cc, hv, y);
         return;
     }
 #pragma unroll 1
     for (int rr = 0; rr < rows; ++rr) {
         if (active) {
-            down_row<T, MT>(st, H, R, rr, c16, hv, y);
+            down_row<T, MT>(st, H, R, rr, cc, hv, y);
         } else {
 #pragma unroll
             for (int t = 0; t < T; ++t) (void)__shfl_sync(0xFFFFFFFFu, hv, rr * T + t);
@@ -349,47 +360,45 @@ __device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int 
     }
 }
 
-// What the consumers keep of a job: its token count, routing weights, and
-// for each token the row of the partial list this CTA writes its share to
-// (slot = tok * maxseg + seg_base + (b - b0)).
-struct JobState {
-    int ntok;
-    float w0, w1;
-    int slot0, slot1;
-};
-
-__device__ __forceinline__ JobState job_state(const ExpertArgs& a, const Job& job, int job_index, const Range& rg) {
-    const int64_t b0 = job.b0 >= 0 ? job.b0 : cta_of_row(static_cast<int64_t>(job_index) * a.I, rg.n, rg.g);
-    const int rel = static_cast<int>(static_cast<int64_t>(blockIdx.x) - b0);
-    JobState js;
-    js.ntok = job.ntok;
-    js.w0 = job.w[0];
-    js.w1 = job.w[1];
-    js.slot0 = job.tok[0] * a.maxseg + job.seg_base[0] + rel;
-    js.slot1 = job.tok[1] * a.maxseg + job.seg_base[1] + rel;
-    return js;
-}
-
-// Writes y (this CTA's share of one job) to the job's partial slots.
+// Adds y (this CTA's share for the tokens of `tk`) into the CTA's partial
+// row of each of those tokens (row tok * G + b): the CTA's first write of a
+// token stores, later ones add, so a CTA's partial of a token sums its rows
+// in walk order. `written` (the same in every thread) tracks the tokens
+// written so far.
 template <int MT>
-__device__ __forceinline__ void flush_partial(const ExpertArgs& a, int ntok, int slot0, int slot1, int c16,
-                                              bool active, const Cols<MT>& y) {
-    if (!active) return;
+__device__ __forceinline__ void flush_y(const ExpertArgs& a, int ntok, int tok0, int tok1, int cc, bool active,
+                                        uint32_t& written, const Cols<MT>& y) {
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
         if (t < ntok) {
-            const int slot = t == 0 ? slot0 : slot1;
-            float4* dst = reinterpret_cast<float4*>(a.partial + static_cast<int64_t>(slot) * a.H + c16 * 16);
+            const int tok = t == 0 ? tok0 : tok1;
+            const bool add = (written >> tok) & 1u;
+            written |= 1u << tok;
+            if (active) {
+                float4* dst = reinterpret_cast<float4*>(
+                    a.partial + (static_cast<int64_t>(tok) * gridDim.x + blockIdx.x) * a.H + cc * kDownCols);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                dst[k] = make_float4(y.p[t][2 * k].x, y.p[t][2 * k + 1].x, y.p[t][2 * k].y, y.p[t][2 * k + 1].y);
+                for (int k = 0; k < 4; ++k) {
+                    float4 v = make_float4(y.p[t][2 * k].x, y.p[t][2 * k + 1].x, y.p[t][2 * k].y, y.p[t][2 * k + 1].y);
+                    if (add) {
+                        const float4 o = dst[k];
+                        v.x += o.x;
+                        v.y += o.y;
+                        v.z += o.z;
+                        v.w += o.w;
+                    }
+                    dst[k] = v;
+                }
+            }
         }
     }
 }
 
 // Stages the job's x into shared memory (plane t * 4 + q, chunk c =
-// columns 16 c + 4 q .. +3 of token t), then waits until every consumer
-// warp has written its share.
+// columns 16 c + 4 q + (0, 2, 1, 3) of token t), then waits until every
+// consumer warp has written its share. x is read from L2 (ld.global.cg):
+// in an MoE call the fused kernel reads it before its own grid-dependency
+// wait, once the kernel that wrote it has completed.
 template <int MT>
 __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const Job& job, int nch,
                                         int tid, int NT, uint32_t& xuse, int lane) {
@@ -398,7 +407,10 @@ __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float
         if (t >= job.ntok) break;
         const int tok = t == 0 ? job.tok[0] : job.tok[1];
         const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H);
-        for (int j = tid; j < H4; j += NT) xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = __ldg(src + j);
+        for (int j = tid; j < H4; j += NT) {
+            const float4 v = __ldcg(src + j);
+            xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x, v.z, v.y, v.w);
+        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&ctl.xbar));
@@ -408,44 +420,45 @@ __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float
 }
 
 // The fixed shape of a specialised kernel: hidden size HC (0: any), its
-// 16-column chunks per lane, and its rows per chunk (one gate/up row per
-// consumer warp).
+// consumer warps (16 down columns per thread), the 16-column chunks per
+// lane of a gate/up row, and its rows per chunk (one gate/up row per
+// consumer warp, at least 4).
 template <int HC>
 struct Shape {
     static constexpr int kNch = HC / 16;
-    static constexpr int kNW = (kNch + 31) / 32;
+    static constexpr int kNW = (HC / kDownCols + 31) / 32;
     static constexpr int kNC = (HC > 0 && kNch % 32 == 0) ? kNch / 32 : 0;
     static constexpr int kRows = HC > 0 ? (kNW / 2 > 4 ? kNW / 2 : 4) : 0;
 };
 
 template <int MT, int HC>
-__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const uint8_t* ring, const Range& rg,
-                         int NW, int warp, int lane) {
+__device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const uint8_t* ring, int NW, int warp,
+                         int lane) {
     using S = Shape<HC>;
     const int H = HC > 0 ? HC : a.H;
     const int R = S::kRows > 0 ? S::kRows : a.rows;
     if (S::kNW > 0) NW = S::kNW;
     const int nch = H / 16;
-    const int c16 = warp * 32 + lane;
-    const bool active = c16 < nch;
+    const int cc = warp * 32 + lane;
+    const bool active = cc < H / kDownCols;
     const uint32_t sbytes = stage_bytes(H, R);
     const bool rd_gate = reads_stage(warp, NW, R, kGate), rd_up = reads_stage(warp, NW, R, kUp);
     Cols<MT> y;
     zero_cols(y);
+    uint32_t written = 0;  // tokens whose partial row this CTA has written
     Walk w;
-    w.begin(rg, a.I, R);
-    Job job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
-    JobState js = job_state(a, job, w.j, rg);
+    w.begin(a, R);
     uint32_t xuse = 0;
-    bool ok = stage_x<MT>(a, ctl, xs, job, nch, warp * 32 + lane, NW * 32, xuse, lane);
+    bool ok = true;
+    if (!w.done()) ok = stage_x<MT>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
     uint32_t c = 0;  // chunk index: uses of the gate and up slots, and the publish parity
-    // the chunk whose down rows are pending
-    bool pending = false, p_last_of_job = false;
-    int p_rows = 0, p_ntok = 1, p_slot0 = 0, p_slot1 = 0;
+    // the chunk whose down rows are pending (chunk c - 1) and its tokens
+    bool pending = false, p_flush = false;
+    int p_rows = 0, p_T = 1, p_ntok = 1, p_tok0 = 0, p_tok1 = 0;
     float p_hv = 0.0f;
 
     while (ok && !w.done()) {
-        const int T = MT == 1 ? 1 : js.ntok;
+        const int T = MT == 1 ? 1 : w.job.ntok;
         const uint32_t par = c & 1u;
         for (int m = kGate; m <= kUp && ok; ++m) {
             if (!(m == kGate ? rd_gate : rd_up)) continue;
@@ -466,13 +479,13 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
                 ok = false;
                 break;
             }
-            if (p_ntok == 2)
-                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            if (p_T == 2)
+                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             else
-                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             release(ctl, kDown, lane);
-            if (p_last_of_job) {
-                flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
+            if (p_flush) {
+                flush_y(a, p_ntok, p_tok0, p_tok1, cc, active, written, y);
                 zero_cols(y);
             }
         }
@@ -483,34 +496,37 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
         float hv = 0.0f;  // lane (r * T + t): h of row r, token t
         if (lane < R * T) {
             const int r = lane / T, t = lane % T;
-            const float wt = t == 0 ? js.w0 : js.w1;
+            const float wt = t == 0 ? w.job.w[0] : w.job.w[1];
             hv = silu(ctl.gu[par][kGate][r][t]) * ctl.gu[par][kUp][r][t] * wt;
         }
         pending = true;
         p_rows = w.rows;
-        p_ntok = T;
-        p_slot0 = js.slot0;
-        p_slot1 = js.slot1;
+        p_T = T;
         p_hv = hv;
-        ++c;
-        p_last_of_job = w.next(R);
-        if (p_last_of_job) {  // every warp has finished the previous job's gate/up rows
-            job = get_job(a.jobs, a.dense_jobs, a.bsz, w.j);
-            js = job_state(a, job, w.j, rg);
-            ok = stage_x<MT>(a, ctl, xs, job, nch, warp * 32 + lane, NW * 32, xuse, lane);
+        p_ntok = w.job.ntok;
+        p_tok0 = w.job.tok[0];
+        p_tok1 = w.job.tok[1];
+        p_flush = false;
+        if (w.next(a, R) && (w.job.ntok != p_ntok || w.job.tok[0] != p_tok0 || w.job.tok[1] != p_tok1)) {
+            // new tokens: y is flushed after this chunk's down rows; every
+            // warp is past this chunk's gate/up rows, so x may change now
+            p_flush = true;
+            ok = stage_x<MT>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
         }
+        ++c;
     }
     if (ok && pending) {
         ok = wait_full(a, ctl, kDown, c - 1u);
         if (ok) {
-            if (p_ntok == 2)
-                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+            if (p_T == 2)
+                down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             else
-                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, c16, active, p_hv, y);
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             release(ctl, kDown, lane);
-            flush_partial(a, p_ntok, p_slot0, p_slot1, c16, active, y);
+            flush_y(a, p_ntok, p_tok0, p_tok1, cc, active, written, y);
         }
     }
+    if (warp == 0 && lane == 0) a.mask[blockIdx.x] = written;
     if (!ok) {
         record_status(a.status, FP9_ERR_TIMEOUT);
         ctl.abort = 1;
@@ -528,11 +544,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NW = static_cast<int>(blockDim.x / 32) - 1;
 
-    grid_dependency_wait();  // the router's job list and x are complete
+    // A dense call reads x, written by the kernel queued before it, so it
+    // waits first. An MoE call starts while the router runs: it starts no
+    // earlier than the router's CTAs have all passed their own wait for the
+    // kernel that wrote x (and read the previous call's partials), and it
+    // waits for the router itself before phase 1.
+    if (!a.routed) grid_dependency_wait();
     grid_launch_dependents();
-    const int32_t J = a.dense_jobs > 0 ? a.dense_jobs : a.ctl->njobs;
-    const Range rg = cta_range(J, a.I, gridDim.x, blockIdx.x);
-    if (rg.start >= rg.end) return;
 
     if (tid == 0) {
         int gate_readers = 0, up_readers = 0;
@@ -554,35 +572,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     __syncthreads();
 
     if (warp == NW) {
-        if (lane == 0) producer(a, ctl, ring, rg);
+        if (lane == 0) producer(a, ctl, ring);
         return;
     }
-    consumer<MT, HC>(a, ctl, xs, ring, rg, NW, warp, lane);
+    consumer<MT, HC>(a, ctl, xs, ring, NW, warp, lane);
 }
 
 // ------------------------------------------------------------- combine ----
 
 struct CombineArgs {
-    const float* partial;
-    const Job* jobs;
-    const Control* ctl;
-    int32_t dense_jobs;
-    int32_t bsz;
+    const float* partial;  // [bsz * grid, H]
+    const uint32_t* mask;  // [grid]
     int32_t H;
-    int32_t maxseg;
-    int32_t grid;  // CTAs of the expert kernel
-    int64_t I;
+    int32_t grid;          // CTAs of the expert kernel
     float* y;
 };
 
 constexpr int kCombineCols = 64;               // columns per CTA: 16 lanes x float4
 constexpr int kCombineWarps = 8;
-constexpr int kCombineLanes = kCombineWarps * 2;  // segment lanes: two per warp
+constexpr int kCombineLanes = kCombineWarps * 2;  // partial lanes: two per warp
 
-// y[t, c] = sum of token t's partials, in list order (= job order, then
-// CTA order within a job). Segment lane s (= 2 * warp + half-warp) adds
-// partials s, s + 16, ...; the sixteen lane sums are then added in lane
-// order.
+// y[t, c] = the sum of the expert kernel's partials of token t, in CTA
+// order. Partial lane s (= 2 * warp + half-warp) adds the partials of CTAs
+// s, s + 16, ... that hold token t; the sixteen lane sums are then added in
+// lane order.
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
     __shared__ float4 red[kCombineLanes][16];
     grid_dependency_wait();  // all partials are written
@@ -592,20 +605,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const int sl = warp * 2 + half;
     const int t = blockIdx.y;
     const int c = blockIdx.x * kCombineCols + l16 * 4;
-    int n;
-    if (a.dense_jobs > 0) {  // token t is in job t / 2 only
-        const int64_t N = static_cast<int64_t>(a.dense_jobs) * a.I;
-        const int64_t G = N < a.grid ? N : a.grid;
-        const int64_t first = static_cast<int64_t>(t / kTokensPerJob) * a.I;
-        n = static_cast<int>(cta_of_row(first + a.I - 1, N, G) - cta_of_row(first, N, G) + 1);
-    } else {
-        n = a.ctl->nseg[t];
-    }
-    const float* base = a.partial + static_cast<int64_t>(t) * a.maxseg * a.H + c;
+    const float* base = a.partial + static_cast<int64_t>(t) * a.grid * a.H + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int s = sl; s < n; s += kCombineLanes) {
-        const float4 p = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(s) * a.H));
+    for (int b = sl; b < a.grid; b += kCombineLanes) {
+        if (!((__ldcg(a.mask + b) >> t) & 1u)) continue;
+        const float4 p = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(b) * a.H));
         acc.x += p.x;
         acc.y += p.y;
         acc.z += p.z;
@@ -648,11 +653,12 @@ struct LaunchShape {
 
 constexpr int kDsv3Hidden = 7168;
 
-// Rows per chunk: half the consumer warps (so that the 2R gate/up rows of a
-// chunk give every warp one row; 7 for hidden 7168), at least 4, and as
-// many as fit in shared memory next to x.
+// Consumer warps: one thread per 16 hidden columns. Rows per chunk: half
+// the consumer warps (so that the 2R gate/up rows of a chunk give every
+// warp one; 7 for hidden 7168), at least 4, and as many as fit in shared
+// memory next to x.
 static fp9_status expert_shape(int32_t H, int MT, LaunchShape& s) {
-    const int nw = (H / 16 + 31) / 32;
+    const int nw = (H / kDownCols + 31) / 32;
     s.threads = nw * 32 + 32;
     const int32_t optin = device_max_smem_optin();
     if (optin <= 0) return FP9_ERR_CUDA;
@@ -691,11 +697,20 @@ static fp9_status ensure_smem_attr() {
 // Optional events bracketing each fused-kernel launch (fp9_profile_events).
 static cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 
-// Queues the fused expert kernel and the combine kernel.
-static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float* x, float* y, int32_t bsz,
-                             int32_t H, int64_t I, uint8_t* ws, const WsLayout& lay, int32_t dense_jobs,
-                             int32_t* status, cudaStream_t stream, uint64_t timeout_ns, bool no_copy,
-                             bool combine) {
+// What one fused-kernel launch streams: the bank of phase 0 (shared experts
+// or the dense FFN) and, for an MoE call, the routed bank of phase 1.
+struct FfnCall {
+    BankPtrs routed;
+    BankPtrs implicit;
+    int32_t impl_nexp;   // experts of the phase-0 bank (0: none)
+    int32_t impl_bank;   // 1: shared experts, 0: dense FFN
+    bool moe;            // phase 1 runs on the router's plan
+};
+
+// Queues the fused expert kernel and (when `combine`) the combine kernel.
+static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int32_t bsz, int32_t H, int64_t I,
+                             uint8_t* ws, const WsLayout& lay, int32_t* status, cudaStream_t stream,
+                             uint64_t timeout_ns, bool no_copy, bool combine) {
     const int MT = bsz == 1 ? 1 : 2;  // jobs hold two tokens only when bsz >= 2
     LaunchShape shp;
     fp9_status st = expert_shape(H, MT, shp);
@@ -703,16 +718,20 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
     st = ensure_smem_attr();
     if (st != FP9_OK) return st;
     ExpertArgs a;
-    a.bank[0] = b0;
-    a.bank[1] = b1;
+    a.bank[0] = call.routed;
+    a.bank[1] = call.implicit;
     a.x = x;
     a.partial = reinterpret_cast<float*>(ws + lay.off_partial);
+    a.mask = reinterpret_cast<uint32_t*>(ws + lay.off_mask);
     a.jobs = reinterpret_cast<const Job*>(ws + lay.off_jobs);
     a.ctl = reinterpret_cast<const Control*>(ws);
-    a.dense_jobs = dense_jobs;
+    a.cta_row = reinterpret_cast<const int64_t*>(ws + lay.off_ctarow);
+    a.impl_nexp = call.impl_nexp > 0 ? call.impl_nexp : 1;
+    a.impl_jobs = call.impl_nexp * token_pairs(bsz);
+    a.impl_bank = call.impl_bank;
+    a.routed = call.moe ? 1 : 0;
     a.bsz = bsz;
     a.H = H;
-    a.maxseg = lay.maxseg;
     a.I = I;
     a.rows = shp.rows;
     a.no_copy = no_copy ? 1 : 0;
@@ -729,14 +748,9 @@ static fp9_status launch_ffn(const BankPtrs& b0, const BankPtrs& b1, const float
     if (!combine) return FP9_OK;
     CombineArgs c;
     c.partial = a.partial;
-    c.jobs = a.jobs;
-    c.ctl = a.ctl;
-    c.dense_jobs = dense_jobs;
-    c.bsz = bsz;
+    c.mask = a.mask;
     c.H = H;
-    c.maxseg = lay.maxseg;
     c.grid = lay.grid;
-    c.I = I;
     c.y = y;
     FP9_CUDA_TRY(launch_pdl(combine_kernel, dim3(H / kCombineCols, bsz), dim3(kCombineWarps * 32), 0, stream, c));
     return FP9_OK;
@@ -750,8 +764,18 @@ static fp9_status check_dense(const fp9_ffn_bank* f, int32_t bsz) {
     FP9_CHECK_ARG(f != nullptr, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(bsz >= 1 && bsz <= FP9_MAX_BSZ, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(hidden_ok(f->hidden), FP9_ERR_SHAPE);
-    FP9_CHECK_ARG(f->inter >= 1, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(f->inter >= 1 && f->inter <= FP9_MAX_INTER, FP9_ERR_SHAPE);
     return check_bank(*f, 1, f->inter, f->hidden);
+}
+
+static FfnCall moe_call(const fp9_moe_layer* layer) {
+    FfnCall c;
+    c.routed = bank_ptrs(layer->routed);
+    c.implicit = layer->n_shared > 0 ? bank_ptrs(layer->shared) : c.routed;
+    c.impl_nexp = layer->n_shared;
+    c.impl_bank = 1;
+    c.moe = true;
+    return c;
 }
 
 }  // namespace fp9
@@ -762,7 +786,7 @@ extern "C" size_t fp9_dense_workspace_bytes(const fp9_ffn_bank* ffn, int32_t bsz
     if (check_dense(ffn, bsz) != FP9_OK) return 0;
     const int32_t sms = device_sm_count();
     if (sms <= 0) return 0;
-    return dense_layout(bsz, ffn->inter, ffn->hidden, sms).total;
+    return dense_layout(bsz, ffn->hidden, expert_grid(sms, false)).total;
 }
 
 extern "C" fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x, int32_t bsz, float* y,
@@ -775,17 +799,14 @@ extern "C" fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x
     FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
     const int32_t sms = device_sm_count();
     FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
-    const WsLayout lay =
-        moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms);
+    const WsLayout lay = moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true));
     FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s);
     if (st != FP9_OK) return st;
-    const BankPtrs routed = bank_ptrs(layer->routed);
-    const BankPtrs shared = layer->n_shared > 0 ? bank_ptrs(layer->shared) : routed;
-    return launch_ffn(routed, shared, x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, 0,
-                      d_status, s, kDefaultTimeoutNs, false, true);
+    return launch_ffn(moe_call(layer), x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, d_status,
+                      s, kDefaultTimeoutNs, false, true);
 }
 
 extern "C" fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz, float* y, void* ws,
@@ -797,11 +818,15 @@ extern "C" fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int
     FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
     const int32_t sms = device_sm_count();
     FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
-    const WsLayout lay = dense_layout(bsz, ffn->inter, ffn->hidden, sms);
+    const WsLayout lay = dense_layout(bsz, ffn->hidden, expert_grid(sms, false));
     FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
-    const BankPtrs p = bank_ptrs(*ffn);
-    return launch_ffn(p, p, x, y, bsz, static_cast<int32_t>(ffn->hidden), ffn->inter, static_cast<uint8_t*>(ws),
-                      lay, lay.jmax, d_status, static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false, true);
+    FfnCall c;
+    c.routed = c.implicit = bank_ptrs(*ffn);
+    c.impl_nexp = 1;
+    c.impl_bank = 0;
+    c.moe = false;
+    return launch_ffn(c, x, y, bsz, static_cast<int32_t>(ffn->hidden), ffn->inter, static_cast<uint8_t*>(ws), lay,
+                      d_status, static_cast<cudaStream_t>(stream), kDefaultTimeoutNs, false, true);
 }
 
 extern "C" fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status, int32_t timeout_us,
@@ -811,18 +836,24 @@ extern "C" fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d
     FP9_CHECK_ARG(timeout_us >= 1 && timeout_us <= 1000000, FP9_ERR_INVALID_ARG);
     constexpr int32_t H = 256;
     constexpr int64_t I = 8;
-    // one CTA, one dense job: x at the start of ws, partials after the layout
-    WsLayout lay = dense_layout(1, I, H, 1);
-    lay.off_partial = align_up(sizeof(float) * H + kAlign);
-    lay.total = lay.off_partial + sizeof(float) * lay.maxseg * H;
+    // one CTA, one dense job: x at the start of ws, mask and partials after it
+    WsLayout lay = dense_layout(1, H, 1);
+    const size_t shift = align_up(sizeof(float) * H + kAlign);
+    lay.off_mask += shift;
+    lay.off_partial += shift;
+    lay.total += shift;
     FP9_CHECK_ARG(ws_bytes >= lay.total && ws_bytes >= 65536, FP9_ERR_WORKSPACE);
     uint8_t* w = static_cast<uint8_t*>(ws);
-    BankPtrs p;  // never dereferenced: no copies are issued
+    FfnCall c;  // never dereferenced: no copies are issued
     for (int m = 0; m < 3; ++m) {
-        p.body[m] = w;
-        p.sign[m] = w;
+        c.routed.body[m] = w;
+        c.routed.sign[m] = w;
     }
-    return launch_ffn(p, p, reinterpret_cast<const float*>(w + kAlign), nullptr, 1, H, I, w, lay, 1, d_status,
+    c.implicit = c.routed;
+    c.impl_nexp = 1;
+    c.impl_bank = 0;
+    c.moe = false;
+    return launch_ffn(c, reinterpret_cast<const float*>(w + kAlign), nullptr, 1, H, I, w, lay, d_status,
                       static_cast<cudaStream_t>(stream), static_cast<uint64_t>(timeout_us) * 1000ull, true, false);
 }
 
@@ -883,8 +914,7 @@ extern "C" fp9_status fp9_moe_forward_noalloc(const fp9_moe_layer* layer, const 
     FP9_CHECK_ARG(aligned(x, 16) && aligned(y, 16), FP9_ERR_ALIGN);
     const int32_t sms = device_sm_count();
     FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
-    const WsLayout lay =
-        moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms);
+    const WsLayout lay = moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true));
     // the fixed array must hold this call's workspace
     FP9_CHECK_ARG(lay.total <= kNoAllocScratchBytes, FP9_ERR_WORKSPACE);
     int dev = 0;
@@ -895,10 +925,8 @@ extern "C" fp9_status fp9_moe_forward_noalloc(const fp9_moe_layer* layer, const 
     FP9_CUDA_TRY(cudaMemsetAsync(w, 0, sizeof(Control), s));
     st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s);
     if (st != FP9_OK) return st;
-    const BankPtrs routed = bank_ptrs(layer->routed);
-    const BankPtrs shared = layer->n_shared > 0 ? bank_ptrs(layer->shared) : routed;
-    return launch_ffn(routed, shared, x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, 0,
-                      d_status, s, kDefaultTimeoutNs, false, true);
+    return launch_ffn(moe_call(layer), x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, d_status,
+                      s, kDefaultTimeoutNs, false, true);
 }
 
 extern "C" size_t fp9_moe_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }

@@ -4,12 +4,24 @@
 // A job is one FFN streamed for a group of up to two tokens (the pages' bsz =
 // 2 pair hits nearly disjoint expert sets, so most jobs hold one token of a
 // pair; a shared expert holds both) [MTP-9.2]. The jobs' intermediate rows
-// are concatenated and split evenly over the CTAs of the fused kernel: each
-// CTA owns one contiguous range of (job, row) pairs and writes one fp32
-// partial output per job it touches; the combine kernel adds them in a
-// fixed order. This is the single-GPU restatement of the pages' split of
-// the FFN intermediate dimension over nodes with f32 partial sums
-// [MEMOIR-COMM], [DS4-TP].
+// are concatenated and split over the CTAs of the fused kernel: each CTA
+// owns one contiguous range of (job, row) pairs, keeps y of the job's tokens
+// in registers and adds it into its own fp32 partial output of each token;
+// the combine kernel adds the CTAs' partials in CTA order. This is the
+// single-GPU restatement of the pages' split of the FFN intermediate
+// dimension over nodes with f32 partial sums [MEMOIR-COMM], [DS4-TP].
+//
+// The fused kernel runs two phases. Phase 0 streams the jobs that need no
+// routing (the shared experts of an MoE layer, or the dense FFN), split
+// evenly by rows; phase 1 streams the routed experts on the router's plan.
+// Phase 0 does not wait for the router, so the router's selection runs
+// while the shared expert streams.
+//
+// The router's split balances work, not rows: a row of a two-token job
+// streams the same bytes as a one-token row but does about twice the
+// multiply-adds, so rows are weighted by row_cost(ntok) units and every CTA
+// gets an equal share of the units. A row belongs to the CTA whose unit
+// range holds the row's first unit.
 #pragma once
 
 #include <cstddef>
@@ -20,51 +32,71 @@
 namespace fp9 {
 
 constexpr int kTokensPerJob = 2;
-// the combine kernel keeps per-job data for at most this many jobs
-constexpr int kMaxJobs = 256;
-static_assert(FP9_MAX_SHARED * ((FP9_MAX_BSZ + 1) / 2) + FP9_MAX_BSZ * FP9_MAX_TOPK <= kMaxJobs,
-              "job count bound");
+// work units of one intermediate row of a job holding 1 or 2 tokens
+constexpr int32_t kRowCost1 = 8, kRowCost2 = 11;
+__host__ __device__ inline int32_t row_cost(int32_t ntok) { return ntok == 2 ? kRowCost2 : kRowCost1; }
+
+// the router keeps one thread per routed job
+constexpr int kMaxJobs = FP9_MAX_BSZ * FP9_MAX_TOPK;  // 128
 
 struct __align__(16) Job {
     int32_t bank;      // 0 = routed experts (or the dense FFN), 1 = shared
     int32_t expert;    // index inside the bank
     int32_t ntok;      // 1 or 2
-    int32_t b0;        // first CTA of the fused kernel that covers this job
+    int32_t pad;
     int32_t tok[kTokensPerJob];
-    float w[kTokensPerJob];         // routing weight per token (1 for shared / dense)
-    int32_t seg_base[kTokensPerJob];  // where this job's partials start in each token's list
-    int32_t pad[2];
+    float w[kTokensPerJob];  // routing weight per token (1 for shared / dense)
 };
-static_assert(sizeof(Job) == 48, "Job is 48 bytes");
+static_assert(sizeof(Job) == 32, "Job is 32 bytes");
 
 struct Control {
     uint32_t ticket;   // last-arriver counter of the router (self-resetting)
-    int32_t njobs;     // jobs written by the router
-    int32_t nseg[FP9_MAX_BSZ];  // partials per token
+    int32_t njobs;     // routed jobs written by the router
+    int32_t geff;      // CTAs of the fused kernel that own routed rows
+    int32_t pad;
 };
+
+// Jobs of phase 0 (no routing): nexp experts of one bank for every pair of
+// tokens, pair-major (job j: token pair j / nexp, expert j % nexp), so that
+// consecutive jobs hold the same tokens.
+__host__ __device__ inline Job implicit_job(int32_t j, int32_t nexp, int32_t bank, int32_t bsz) {
+    Job jb;
+    const int32_t p = j / nexp;
+    jb.bank = bank;
+    jb.expert = j - p * nexp;
+    jb.pad = 0;
+    jb.tok[0] = kTokensPerJob * p;
+    jb.ntok = (kTokensPerJob * p + 1 < bsz) ? 2 : 1;
+    jb.tok[1] = jb.ntok == 2 ? jb.tok[0] + 1 : jb.tok[0];
+    jb.w[0] = 1.0f;
+    jb.w[1] = jb.ntok == 2 ? 1.0f : 0.0f;
+    return jb;
+}
+
+__host__ __device__ inline int32_t token_pairs(int32_t bsz) { return (bsz + kTokensPerJob - 1) / kTokensPerJob; }
 
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t off_logits = 0, off_ids = 0, off_w = 0, off_jobs = 0, off_partial = 0, total = 0;
-    int32_t jmax = 0;     // largest possible job count
-    int32_t maxseg = 0;   // partial slots per token
-    int32_t grid = 0;     // CTAs of the fused kernel
+    size_t off_logits = 0, off_ids = 0, off_w = 0, off_jobs = 0, off_ctarow = 0, off_mask = 0, off_partial = 0,
+           total = 0;
+    int32_t jmax = 0;  // largest routed job count
+    int32_t grid = 0;  // CTAs of the fused kernel
 };
 
-// Partial outputs are stored token-major: token t's partials are the
-// rows [t * maxseg, t * maxseg + nseg[t]) of a [bsz * maxseg, hidden]
-// fp32 array. A token's jobs cover disjoint row ranges, so its partials
-// number at most (CTAs) + (jobs holding the token).
-inline WsLayout moe_layout(int32_t bsz, int32_t n_experts, int32_t topk, int32_t n_shared,
-                           int64_t inter, int64_t hidden, int32_t grid) {
+// Partials are token-major: token t's partial of CTA b is row t * grid + b
+// of a [bsz * grid, hidden] fp32 array; bit t of mask[b] says whether CTA b
+// wrote it (a CTA that never held token t leaves its row unwritten).
+inline size_t partial_bytes(int32_t bsz, int32_t grid, int64_t hidden) {
+    return sizeof(float) * static_cast<size_t>(bsz) * grid * hidden;
+}
+
+inline WsLayout moe_layout(int32_t bsz, int32_t n_experts, int32_t topk, int64_t hidden, int32_t grid) {
     WsLayout L;
-    const int32_t pairs = (bsz + kTokensPerJob - 1) / kTokensPerJob;
-    L.jmax = n_shared * pairs + bsz * topk;
+    L.jmax = bsz * topk;
     L.grid = grid;
-    L.maxseg = grid + topk + n_shared;
     size_t off = align_up(sizeof(Control));
     L.off_logits = off;
     off = align_up(off + sizeof(float) * bsz * n_experts);
@@ -74,24 +106,34 @@ inline WsLayout moe_layout(int32_t bsz, int32_t n_experts, int32_t topk, int32_t
     off = align_up(off + sizeof(float) * bsz * topk);
     L.off_jobs = off;
     off = align_up(off + sizeof(Job) * L.jmax);
+    L.off_ctarow = off;  // [grid + 1] first (job * I + row) of each CTA in phase 1
+    off = align_up(off + sizeof(int64_t) * (grid + 1));
+    L.off_mask = off;
+    off = align_up(off + sizeof(uint32_t) * grid);
     L.off_partial = off;
-    off = align_up(off + sizeof(float) * static_cast<size_t>(bsz) * L.maxseg * hidden);
+    off = align_up(off + partial_bytes(bsz, grid, hidden));
     L.total = off;
     return L;
 }
 
-inline WsLayout dense_layout(int32_t bsz, int64_t inter, int64_t hidden, int32_t grid) {
+inline WsLayout dense_layout(int32_t bsz, int64_t hidden, int32_t grid) {
     WsLayout L;
-    L.jmax = (bsz + kTokensPerJob - 1) / kTokensPerJob;
     L.grid = grid;
-    L.maxseg = grid + 1;
-    L.off_partial = align_up(sizeof(Control));
-    L.total = align_up(L.off_partial + sizeof(float) * static_cast<size_t>(bsz) * L.maxseg * hidden);
+    L.off_mask = align_up(sizeof(Control));
+    L.off_partial = align_up(L.off_mask + sizeof(uint32_t) * grid);
+    L.total = align_up(L.off_partial + partial_bytes(bsz, grid, hidden));
     return L;
 }
 
-// First row of CTA b, and the CTA that owns row p, for n rows over g CTAs
-// (CTA b owns rows [b*n/g, (b+1)*n/g); g <= n, so none is empty).
+// CTAs of the fused kernel: one per SM. An MoE call leaves one SM free: the
+// router's last CTA (which builds the plan) still holds an SM when the
+// fused kernel's CTAs start, and those take the SMs in the order they free
+// up, so none of them waits for the router to finish.
+inline int32_t expert_grid(int32_t sms, bool moe) { return moe && sms > 1 ? sms - 1 : sms; }
+
+// First unit of CTA b, and the CTA that owns unit p, for n units over g
+// CTAs (CTA b owns units [b*n/g, (b+1)*n/g)). With one unit per row and
+// g <= n no CTA is empty.
 __host__ __device__ inline int64_t cta_start(int64_t b, int64_t n, int64_t g) { return b * n / g; }
 __host__ __device__ inline int64_t cta_of_row(int64_t p, int64_t n, int64_t g) {
     return ((p + 1) * g - 1) / n;

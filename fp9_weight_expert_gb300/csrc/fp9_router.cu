@@ -30,7 +30,7 @@ static_assert(kMaxEntries <= kRouterThreads, "one thread per routed pair");
 struct RouterArgs {
     const float* x;      // [bsz, H]
     const float* wr;     // [E, H]
-    int32_t bsz, E, H, n_groups, topk_groups, topk, n_shared;
+    int32_t bsz, E, H, n_groups, topk_groups, topk;
     float scale;
     int64_t I;           // intermediate size (rows per job)
     int32_t grid;        // CTAs of the fused expert kernel
@@ -41,7 +41,33 @@ struct RouterArgs {
     int32_t* ids_out;    // optional
     float* w_out;        // optional
     Job* jobs;           // [jmax]
+    int64_t* cta_row;    // [grid + 1] first row of each CTA of the fused kernel
 };
+
+static_assert(kMaxJobs <= kRouterThreads && kMaxEntries <= kRouterThreads, "one thread per job in the plan scan");
+
+// Exclusive prefix sum of v over the CTA's threads (all threads call it);
+// `total` gets the sum over all of them.
+__device__ int32_t block_exclusive_scan(int32_t v, int tid, int32_t& total) {
+    __shared__ int32_t s_warp[kRouterThreads / 32];
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int32_t off = 0, tot = 0;
+    for (int w = 0; w < kRouterThreads / 32; ++w) {
+        off += w < warp ? s_warp[w] : 0;
+        tot += s_warp[w];
+    }
+    total = tot;
+    __syncthreads();  // s_warp may be reused by the next call
+    return off + incl - v;
+}
 
 // (v, i) beats (bv, bi): a larger value, or an equal value and a lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -123,19 +149,18 @@ __device__ void select_all(const RouterArgs& a, const float* s, int tid, int32_t
     __syncthreads();
 }
 
-// Job list: shared experts first (tokens in pairs, weight 1), then routed
-// experts in ascending id, each with its tokens in ascending order, in
-// groups of up to two. Then, for the fused kernel and the combine: the
-// first CTA covering each job, and where each job's partials start in the
-// token-major partial list of each of its tokens.
+// Routed job list: experts in ascending id, each with its tokens in
+// ascending order, in groups of up to two (the shared experts need no
+// routing: the fused kernel streams them on its own, before these). Then
+// the cost-weighted split of the jobs' rows over the fused kernel's CTAs:
+// each CTA's first row.
 __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, const float* s_wts) {
     __shared__ int32_t s_in[kMaxEntries];
     __shared__ int32_t s_key[kMaxEntries];
     __shared__ float s_w[kMaxEntries];
-    __shared__ int32_t s_start[kMaxEntries];
     __shared__ Job s_jobs[kMaxJobs];
-    __shared__ int32_t s_nseg[kMaxJobs];
-    __shared__ int32_t s_J;
+    __shared__ int64_t s_u0[kMaxJobs];
+    __shared__ int32_t s_cost[kMaxJobs];
     const int P = a.bsz * a.topk;
     int32_t key = INT_MAX;
     float w = 0.0f;
@@ -153,82 +178,64 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         s_w[rank] = w;
     }
     __syncthreads();
-    int is_start = 0;
+    int32_t is_start = 0;
     int e = 0;
-    if (tid < P) {
+    if (tid < P) {  // a job starts at every other key of an expert's run
         e = s_key[tid] / FP9_MAX_BSZ;
         int pos = 0;
-        for (int q = 0; q < tid; ++q) pos += (s_key[q] / FP9_MAX_BSZ == e) ? 1 : 0;
+        for (int q = tid - 1; q >= 0 && s_key[q] / FP9_MAX_BSZ == e; --q) ++pos;
         is_start = (pos % kTokensPerJob == 0) ? 1 : 0;
-        s_start[tid] = is_start;
     }
-    __syncthreads();
-    const int pairs = (a.bsz + kTokensPerJob - 1) / kTokensPerJob;
-    const int nshared_jobs = a.n_shared * pairs;
-    if (tid < P && is_start) {
-        int before = 0;
-        for (int q = 0; q < tid; ++q) before += s_start[q];
+    int32_t J = 0;
+    const int32_t before = block_exclusive_scan(is_start, tid, J);
+    if (is_start) {
         Job j;
         j.bank = 0;
         j.expert = e;
+        j.pad = 0;
         j.tok[0] = s_key[tid] % FP9_MAX_BSZ;
         j.w[0] = s_w[tid];
         const bool two = (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
         j.ntok = two ? 2 : 1;
         j.tok[1] = two ? s_key[tid + 1] % FP9_MAX_BSZ : j.tok[0];
         j.w[1] = two ? s_w[tid + 1] : 0.0f;
-        s_jobs[nshared_jobs + before] = j;
+        s_jobs[before] = j;
     }
-    if (tid < nshared_jobs) {
-        const int sh = tid / pairs, pr = tid % pairs;
-        Job j;
-        j.bank = 1;
-        j.expert = sh;
-        j.tok[0] = 2 * pr;
-        j.ntok = (2 * pr + 1 < a.bsz) ? 2 : 1;
-        j.tok[1] = (j.ntok == 2) ? 2 * pr + 1 : 2 * pr;
-        j.w[0] = 1.0f;
-        j.w[1] = (j.ntok == 2) ? 1.0f : 0.0f;
-        s_jobs[tid] = j;
+    __syncthreads();
+    // Work units: job j's rows start at unit I * C_j, C_j the summed row
+    // costs of the jobs before it; each CTA gets U / G units. G is capped so
+    // that a CTA's share is at least one row of the dearest job, which
+    // leaves no CTA without a row.
+    const int32_t cj = tid < J ? row_cost(s_jobs[tid].ntok) : 0;
+    int32_t ctot = 0;
+    const int32_t cpre = block_exclusive_scan(cj, tid, ctot);
+    const int64_t U = a.I * ctot;
+    const int32_t cmax = a.bsz >= 2 ? kRowCost2 : kRowCost1;
+    int64_t G = U / cmax;
+    G = G > a.grid ? a.grid : (G < 1 ? 1 : G);
+    if (tid < J) {
+        s_u0[tid] = a.I * cpre;
+        s_cost[tid] = cj;
+        a.jobs[tid] = s_jobs[tid];
+    }
+    __syncthreads();
+    for (int b = tid; b <= G; b += blockDim.x) {
+        // CTA b's first row: the first row whose first unit is at or past
+        // the CTA's first unit (b == G: one past the last row)
+        const int64_t us = cta_start(b, U, G);
+        int lo = 0, hi = J - 1;  // the last job starting at or before us
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (s_u0[mid] <= us) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t r = (us - s_u0[lo] + s_cost[lo] - 1) / s_cost[lo];
+        a.cta_row[b] = static_cast<int64_t>(lo) * a.I + r;
     }
     if (tid == 0) {
-        int starts = 0;
-        for (int q = 0; q < P; ++q) starts += s_start[q];
-        s_J = nshared_jobs + starts;
+        a.ctl->njobs = J;
+        a.ctl->geff = static_cast<int32_t>(G);
     }
-    __syncthreads();
-    const int J = s_J;
-    const int64_t N = static_cast<int64_t>(J) * a.I;
-    const int64_t G = N < a.grid ? N : a.grid;
-    for (int j = tid; j < J; j += blockDim.x) {  // CTAs b0..b1 cover job j
-        const int64_t b0 = cta_of_row(static_cast<int64_t>(j) * a.I, N, G);
-        const int64_t b1 = cta_of_row(static_cast<int64_t>(j) * a.I + a.I - 1, N, G);
-        s_jobs[j].b0 = static_cast<int32_t>(b0);
-        s_nseg[j] = static_cast<int32_t>(b1 - b0 + 1);
-    }
-    __syncthreads();
-    if (tid < a.bsz) {  // token tid: its partials, job by job
-        int off = 0;
-        for (int j = 0; j < J; ++j) {
-            const Job& jb = s_jobs[j];
-            if (jb.tok[0] == tid) {
-                s_jobs[j].seg_base[0] = off;
-                off += s_nseg[j];
-            } else if (jb.ntok == 2 && jb.tok[1] == tid) {
-                s_jobs[j].seg_base[1] = off;
-                off += s_nseg[j];
-            }
-        }
-        a.ctl->nseg[tid] = off;
-    }
-    __syncthreads();
-    for (int j = tid; j < J; j += blockDim.x) {
-        Job jb = s_jobs[j];
-        if (jb.ntok == 1) jb.seg_base[1] = jb.seg_base[0];
-        jb.pad[0] = jb.pad[1] = 0;
-        a.jobs[j] = jb;
-    }
-    if (tid == 0) a.ctl->njobs = J;
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
@@ -312,7 +319,7 @@ fp9_status check_layer(const fp9_moe_layer* L, int32_t bsz) {
     FP9_CHECK_ARG(L != nullptr, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(bsz >= 1 && bsz <= FP9_MAX_BSZ, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(hidden_ok(L->hidden), FP9_ERR_SHAPE);
-    FP9_CHECK_ARG(L->inter >= 1, FP9_ERR_SHAPE);
+    FP9_CHECK_ARG(L->inter >= 1 && L->inter <= FP9_MAX_INTER, FP9_ERR_SHAPE);
     FP9_CHECK_ARG(L->n_experts >= 1 && L->n_experts <= FP9_MAX_EXPERTS, FP9_ERR_SHAPE);
     FP9_CHECK_ARG(L->n_groups >= 1 && L->n_groups <= FP9_MAX_GROUPS && L->n_experts % L->n_groups == 0,
                   FP9_ERR_SHAPE);
@@ -345,7 +352,6 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.n_groups = L->n_groups;
     a.topk_groups = L->topk_groups;
     a.topk = L->topk;
-    a.n_shared = L->n_shared;
     a.scale = L->route_scale;
     a.ctl = reinterpret_cast<Control*>(ws);
     a.logits = reinterpret_cast<float*>(ws + lay.off_logits);
@@ -354,6 +360,7 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.ids_out = ids_out;
     a.w_out = w_out;
     a.jobs = build ? reinterpret_cast<Job*>(ws + lay.off_jobs) : nullptr;
+    a.cta_row = reinterpret_cast<int64_t*>(ws + lay.off_ctarow);
     a.I = L->inter;
     a.grid = lay.grid;
     const size_t smem = sizeof(float) * bsz * L->n_experts;  // <= 32 KB
@@ -377,8 +384,7 @@ extern "C" size_t fp9_moe_workspace_bytes(const fp9_moe_layer* layer, int32_t bs
     if (check_layer(layer, bsz) != FP9_OK) return 0;
     const int32_t sms = device_sm_count();
     if (sms <= 0) return 0;
-    return moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms)
-        .total;
+    return moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true)).total;
 }
 
 extern "C" fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int32_t bsz, int32_t* ids,
@@ -390,8 +396,7 @@ extern "C" fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int
     FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
     const int32_t sms = device_sm_count();
     FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
-    const WsLayout lay =
-        moe_layout(bsz, layer->n_experts, layer->topk, layer->n_shared, layer->inter, layer->hidden, sms);
+    const WsLayout lay = moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true));
     FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     return launch_router(layer, x, bsz, ids, weights, static_cast<uint8_t*>(ws), lay, false,
                          static_cast<cudaStream_t>(stream));

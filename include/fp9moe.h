@@ -72,6 +72,7 @@ typedef enum fp9_status {
 #define FP9_MAX_GROUPS 32      /* router groups                             */
 #define FP9_MAX_TOPK 16        /* experts chosen per token                  */
 #define FP9_MAX_SHARED 8       /* shared experts per layer                  */
+#define FP9_MAX_INTER 4194304  /* intermediate size I (2^22)                */
 
 /*
  * A bank of n SwiGLU FFNs of equal shape, each three fp9 matrices of
