@@ -588,23 +588,23 @@ struct CombineArgs {
     float* y;
 };
 
-constexpr int kCombineCols = 64;               // columns per CTA: 16 lanes x float4
-constexpr int kCombineWarps = 8;
-constexpr int kCombineLanes = kCombineWarps * 2;  // partial lanes: two per warp
+constexpr int kCombineCols = 16;    // columns per CTA: 4 float4
+constexpr int kCombineThreads = 256;
+constexpr int kCombineLanes = kCombineThreads / 4;  // partial lanes per column: 64
 
 // y[t, c] = the sum of the expert kernel's partials of token t, in CTA
-// order. Partial lane s (= 2 * warp + half-warp) adds the partials of CTAs
-// s, s + 16, ... that hold token t; the sixteen lane sums are then added in
-// lane order.
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
-    __shared__ float4 red[kCombineLanes][16];
+// order. Thread (lane s, float4 q) adds the partials of CTAs s, s + 64, ...
+// that hold token t (all their loads in flight at once); the 64 lane sums
+// are added by a fixed shuffle tree inside each warp (8 lanes per warp),
+// then the 8 warps' sums in warp order.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+    __shared__ float4 red[kCombineThreads / 32][4];
     grid_dependency_wait();  // all partials are written
     grid_launch_dependents();
+    const int q = threadIdx.x & 3, sl = threadIdx.x >> 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int half = lane >> 4, l16 = lane & 15;
-    const int sl = warp * 2 + half;
     const int t = blockIdx.y;
-    const int c = blockIdx.x * kCombineCols + l16 * 4;
+    const int c = blockIdx.x * kCombineCols + q * 4;
     const float* base = a.partial + static_cast<int64_t>(t) * a.grid * a.H + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
@@ -616,19 +616,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
         acc.z += p.z;
         acc.w += p.w;
     }
-    red[sl][l16] = acc;
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {  // the warp's 8 partial lanes of this float4
+        acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, m);
+        acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, m);
+        acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, m);
+        acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, m);
+    }
+    if (lane < 4) red[warp][q] = acc;
     __syncthreads();
-    if (threadIdx.x < 16) {
-        float4 sum = red[0][threadIdx.x];
-        for (int w = 1; w < kCombineLanes; ++w) {
-            const float4 o = red[w][threadIdx.x];
+    if (threadIdx.x < 4) {
+        float4 sum = red[0][q];
+        for (int w = 1; w < kCombineThreads / 32; ++w) {
+            const float4 o = red[w][q];
             sum.x += o.x;
             sum.y += o.y;
             sum.z += o.z;
             sum.w += o.w;
         }
-        reinterpret_cast<float4*>(a.y + static_cast<int64_t>(t) * a.H)[(blockIdx.x * kCombineCols) / 4 +
-                                                                       threadIdx.x] = sum;
+        reinterpret_cast<float4*>(a.y + static_cast<int64_t>(t) * a.H)[c / 4] = sum;
     }
 }
 
@@ -752,7 +758,7 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     c.H = H;
     c.grid = lay.grid;
     c.y = y;
-    FP9_CUDA_TRY(launch_pdl(combine_kernel, dim3(H / kCombineCols, bsz), dim3(kCombineWarps * 32), 0, stream, c));
+    FP9_CUDA_TRY(launch_pdl(combine_kernel, dim3(H / kCombineCols, bsz), dim3(kCombineThreads), 0, stream, c));
     return FP9_OK;
 }
 

@@ -26,6 +26,9 @@ FEWROWS = synth.MoEShape(hidden=256, inter=5, n_experts=8, n_groups=1, topk_grou
 # about as many rows as SMs: CTAs own one or two rows across job boundaries
 NEARSM = synth.MoEShape(hidden=384, inter=37, n_experts=16, n_groups=2, topk_groups=1, topk=3,
                         n_shared=1, route_scale=1.0, router_std=0.05 * (16 / 384) ** 0.5)
+# more than 256 experts (32 per lane in the one-warp routing), 16 groups of 40, top-6
+WIDE = synth.MoEShape(hidden=256, inter=24, n_experts=640, n_groups=16, topk_groups=5, topk=6,
+                      n_shared=1, route_scale=2.0, router_std=0.05)
 
 
 def _run(shape, bsz, base, layer=None, ol=None):
@@ -43,8 +46,8 @@ def _run(shape, bsz, base, layer=None, ol=None):
     return L, ol, x, y, ids, w, ws, status
 
 
-@pytest.mark.parametrize("shape", [synth.TINY, MID, NARROW, FEWROWS, NEARSM],
-                         ids=["tiny", "mid", "narrow", "fewrows", "nearsm"])
+@pytest.mark.parametrize("shape", [synth.TINY, MID, NARROW, FEWROWS, NEARSM, WIDE],
+                         ids=["tiny", "mid", "narrow", "fewrows", "nearsm", "wide"])
 @pytest.mark.parametrize("bsz", [1, 2, 3, 5, 8])
 def test_moe_forward_matches_oracle(shape, bsz):
     L, ol, x, y, ids, w, ws, status = _run(shape, bsz, base=200 + bsz)
