@@ -55,6 +55,23 @@ R8  Shared experts are added with weight 1 (not multiplied by route_scale).
 R9  W_down is stored transposed, as down_t = W_down^T of shape [I, H], so
     that each intermediate row's down weights are contiguous.
 R10 Stack glue between layers: h <- h + MoE(RMSNorm(h)), eps 1e-6, unit gain.
+R11 fp8 checkpoint conversion. The pages say that DeepSeek-V3 is published
+    in fp8 ([MEMOIR-MEM]: about 688 GB on disk) and that its fp8 checkpoints
+    use a 128x128 block-scale format ([QWEN]), and store fp9 weights without
+    scales (R5); they give no formula. Plainest reading: each weight is an
+    fp8 e4m3 byte (the variant without infinities: S.1111.111 is NaN; bias
+    7; subnormals below 2**-6) times the fp32 scale of its 128x128 block of
+    the [rows, cols] matrix (blocks at the right and bottom edges cover what
+    is left); the product is exact in float64 (a 4-bit significand times a
+    24-bit one) and is rounded once to fp9 as in R4, never through an fp32
+    product, which could round it onto an fp9 midpoint first.
+
+[MEMOIR-MEM]  "一鸭三吃" memoir, section "真正埋下伏笔的是内存；R1 之后，问题
+              第一次被改写": the DeepSeek-V3 release format is fp8, about
+              688 GB of weights on disk.
+[QWEN]        same page, section "先用 Qwen3 练级，再让 Qwen3.5 充当高压试炼场":
+              Qwen3's official fp8 checkpoints use the same 128x128
+              block-scale format as DeepSeek-V3.
 """
 
 from __future__ import annotations
@@ -65,7 +82,7 @@ __all__ = [
     "FP9_INF_BODY", "FP9_NAN_BODY", "FP9_MAX", "FP9_OVERFLOW_THRESHOLD",
     "fp9_value", "fp9_encode", "fp9_pack", "fp9_unpack_signs", "fp9_decode",
     "router_scores", "route", "route_margin", "silu", "ffn", "moe", "dense_ffn",
-    "rmsnorm", "stack",
+    "rmsnorm", "stack", "FP8_BLOCK", "e4m3_value", "fp9_encode_exact", "fp8_block_to_fp9",
 ]
 
 FP9_INF_BODY = 0xF8          # e = 31, m = 0
@@ -149,6 +166,28 @@ def fp9_encode(x):
     return sign.reshape(x.shape), body.reshape(x.shape), err.reshape(x.shape)
 
 
+def fp9_encode_exact(x):
+    """fp9_encode for float64 values that are exact as given (such as an
+    fp8 value times an fp32 scale): the same rounding (R4), with no cast to
+    fp32 first."""
+    x = np.asarray(x, dtype=np.float64)
+    flat = x.reshape(-1)
+    sign = np.empty(flat.shape, np.uint8)
+    body = np.empty(flat.shape, np.uint8)
+    err = np.empty(flat.shape, bool)
+    for i in range(0, flat.size, _BLOCK):
+        sign[i:i + _BLOCK], body[i:i + _BLOCK], err[i:i + _BLOCK] = _encode_block(flat[i:i + _BLOCK])
+    return sign.reshape(x.shape), body.reshape(x.shape), err.reshape(x.shape)
+
+
+def _pack_signs(s):
+    """Sign plane [rows, cols/8] from sign bits [rows, cols] (R1, R2)."""
+    rows, cols = s.shape
+    bits = s.reshape(rows, cols // 8, 8).astype(np.uint32)
+    weights_of_bit = (1 << np.arange(8, dtype=np.uint32))
+    return (bits * weights_of_bit).sum(axis=2).astype(np.uint8)
+
+
 def fp9_pack(w):
     """Pack an fp32 matrix [rows, cols] into (body [rows, cols] u8,
     sign [rows, cols/8] u8, any_range_error) [MEMOIR-FP9], with the sign of
@@ -156,12 +195,46 @@ def fp9_pack(w):
     w = np.asarray(w, dtype=np.float32)
     if w.ndim != 2 or w.shape[1] % 8 != 0:
         raise ValueError("fp9_pack wants a 2-D matrix with cols % 8 == 0")
-    rows, cols = w.shape
     s, body, err = fp9_encode(w)
-    bits = s.reshape(rows, cols // 8, 8).astype(np.uint32)
-    weights_of_bit = (1 << np.arange(8, dtype=np.uint32))
-    sign = (bits * weights_of_bit).sum(axis=2).astype(np.uint8)
-    return body, sign, bool(err.any())
+    return body, _pack_signs(s), bool(err.any())
+
+
+FP8_BLOCK = 128   # rows and columns of a scale block (R11)
+
+
+def e4m3_value(code):
+    """Value of fp8 e4m3 bytes as float64 (R11): sign bit 7, exponent bits
+    6..3 with bias 7, mantissa bits 2..0; exponent 0 is subnormal
+    (m / 8 * 2**-6); S.1111.111 is NaN; there are no infinities."""
+    code = np.asarray(code, dtype=np.int64)
+    s = (code >> 7) & 1
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where(s == 1, -mag, mag)
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+def fp8_block_to_fp9(w8, scale_inv):
+    """Convert an fp8 block-scaled matrix to fp9 planes (R11).
+
+    w8: e4m3 bytes [rows, cols] (cols % 8 == 0); scale_inv: fp32
+    [ceil(rows / 128), ceil(cols / 128)], the scale of each 128x128 block.
+    Returns (body [rows, cols] u8, sign [rows, cols / 8] u8, any_range_error).
+    """
+    w8 = np.asarray(w8, dtype=np.uint8)
+    scale = np.asarray(scale_inv, dtype=np.float32).astype(np.float64)
+    rows, cols = w8.shape
+    if cols % 8 != 0:
+        raise ValueError("fp8_block_to_fp9 wants cols % 8 == 0")
+    nbr, nbc = -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK)
+    if scale.shape != (nbr, nbc):
+        raise ValueError("scale_inv must be [ceil(rows/128), ceil(cols/128)]")
+    # the scale of each element: its block's, by the element's row and column
+    per_elem = scale[(np.arange(rows) // FP8_BLOCK)[:, None], (np.arange(cols) // FP8_BLOCK)[None, :]]
+    exact = e4m3_value(w8) * per_elem
+    s, body, err = fp9_encode_exact(exact)
+    return body, _pack_signs(s), bool(err.any())
 
 
 def fp9_unpack_signs(sign, cols):

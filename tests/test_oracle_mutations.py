@@ -77,3 +77,36 @@ def test_weights_normalised_over_all_experts_is_caught(monkeypatch):
         return ids, np.take_along_axis(s, ids.astype(np.int64), axis=1) / s.sum(axis=1, keepdims=True) * scale
     _patch(monkeypatch, "route", bad_route)
     _fails(M.test_routing_weights_sum_to_scale)
+
+
+# --- fp8 block-scale conversion (R11) ---------------------------------------
+
+from tests import test_oracle_fp8 as F8  # noqa: E402
+
+
+def test_wrong_e4m3_bias_is_caught(monkeypatch):
+    good = OM.e4m3_value
+
+    def bad(code):
+        return good(code) / 2.0  # bias 8 instead of 7
+    _patch(monkeypatch, "e4m3_value", bad)
+    _fails(F8.test_e4m3_matches_torch_float8)
+
+
+def test_rounding_through_fp32_product_is_caught(monkeypatch):
+    good = OM.fp9_encode_exact
+    _patch(monkeypatch, "fp9_encode_exact", lambda x: good(np.asarray(x, np.float64).astype(np.float32)))
+    _fails(F8.test_double_rounding_witnesses_round_the_exact_product)
+    _fails(F8.test_golden_worked_examples)
+
+
+def test_transposed_block_index_is_caught(monkeypatch):
+    def bad(w8, scale_inv):
+        w8 = np.asarray(w8, np.uint8)
+        scale = np.asarray(scale_inv, np.float32).astype(np.float64)
+        rows, cols = w8.shape
+        per = scale[(np.arange(cols) // OM.FP8_BLOCK)[None, :], (np.arange(rows) // OM.FP8_BLOCK)[:, None]]
+        s, body, err = OM.fp9_encode_exact(OM.e4m3_value(w8) * per)
+        return body, OM._pack_signs(s), bool(err.any())
+    _patch(monkeypatch, "fp8_block_to_fp9", bad)
+    _fails(F8.test_block_indexing_follows_each_element)
