@@ -292,6 +292,7 @@ def _native(args):
     extra = {}
     if not args.no_extra and world == 1:
         extra = _side_runs(Ls, ws, status, dev, shape)
+        extra["fp8_to_fp9"] = _convert_run(dev, _peaks()[0])
 
     if rank != 0:
         return None
@@ -382,6 +383,52 @@ def _side_runs(Ls, ws, status, dev, shape):
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
                             "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
     return res
+
+
+def _convert_run(dev, peak):
+    """fp9_from_fp8 on 24 DeepSeek-V3 expert matrices (fp8 e4m3 + 128x128
+    scales -> fp9 planes): HBM GB/s of the bytes it must move (1 B read and
+    1.125 B written per weight, plus the scales). The input is made like a
+    block-scaled checkpoint (torch's e4m3 conversion makes the bytes)."""
+    import torch
+
+    from fp9_weight_expert_gb300 import binding
+    n, rows, cols = 24, 2048, 7168
+    # checkpoint-like input: N(0, 0.02) weights quantised to e4m3 with the
+    # scale of each 128x128 block = its largest magnitude / 448
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    w8 = torch.empty((n * rows, cols), dtype=torch.uint8, device=dev)
+    scale = torch.empty((n * rows // 128, cols // 128), dtype=torch.float32, device=dev)
+    for i in range(n):
+        w = torch.randn((rows, cols), generator=g, device=dev) * 0.02
+        blocks = w.view(rows // 128, 128, cols // 128, 128)
+        sc = blocks.abs().amax(dim=(1, 3)) / 448.0
+        scale[i * rows // 128:(i + 1) * rows // 128] = sc
+        q = (blocks / sc[:, None, :, None]).to(torch.float8_e4m3fn)
+        w8[i * rows:(i + 1) * rows] = q.view(rows, cols).view(torch.uint8)
+    body = torch.empty((n * rows, cols), dtype=torch.uint8, device=dev)
+    sign = torch.empty((n * rows, cols // 8), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        binding.fp9_from_fp8(w8, scale, body, sign, status)
+    torch.cuda.synchronize()
+    K = 20
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        binding.fp9_from_fp8(w8, scale, body, sign, status)
+    b.record()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("fp9_from_fp8 status: " + binding.status_str(int(status.item())))
+    us = a.elapsed_time(b) / K * 1e3
+    weights = n * rows * cols
+    nbytes = weights * (1 + 1.125) + scale.numel() * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"weights_per_call": weights, "us_per_call": round(us, 1), "bytes_per_call": int(nbytes),
+            "gbs": round(gbs, 1), "peak": peak, "frac": round(gbs / peak, 4), "bound": "hbm",
+            "inputs_vs_l2": "752 MB per call, larger than L2"}
 
 
 # ------------------------------------------------------------- CPU oracle

@@ -72,6 +72,8 @@ _SIGS = {
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_from_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(MoELayerC), ctypes.c_int32]),
     "fp9_dense_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(FFNBankC), ctypes.c_int32]),
     "moe_router": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int32,
@@ -155,6 +157,15 @@ def fp9_pack(src: torch.Tensor, body: torch.Tensor, sign: torch.Tensor,
     rows = src.numel() // cols if cols else 0
     _check(load().fp9_pack(_ptr(src), rows, cols, _ptr(body), _ptr(sign), _ptr(status),
                            _stream(stream)), "fp9_pack")
+
+
+def fp9_from_fp8(w8: torch.Tensor, scale_inv: torch.Tensor, body: torch.Tensor, sign: torch.Tensor,
+                 status: torch.Tensor | None = None, stream=None) -> None:
+    """Converts fp8 e4m3 bytes [rows, cols] (uint8) with fp32 block scales
+    [ceil(rows/128), ceil(cols/128)] into body [rows, cols] and sign [rows, cols/8]."""
+    rows, cols = w8.shape[-2], w8.shape[-1]
+    _check(load().fp9_from_fp8(_ptr(w8), _ptr(scale_inv), rows, cols, _ptr(body), _ptr(sign), _ptr(status),
+                               _stream(stream)), "fp9_from_fp8")
 
 
 def fp9_decode(body: torch.Tensor, sign: torch.Tensor, dst: torch.Tensor, stream=None) -> None:

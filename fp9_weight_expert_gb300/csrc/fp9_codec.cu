@@ -6,6 +6,7 @@
 // mantissa bits; the 8-bit body eeeeemmm is kept per weight and the signs of
 // 8 weights are packed into one byte of a separate plane (least significant
 // bit = lowest column).
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -19,7 +20,12 @@ namespace fp9 {
 // Round the fp32 value with bits `xbits` (sign ignored) to the nearest fp9
 // body, ties to the even mantissa, in integer arithmetic on the fp32 fields.
 // Sets `range` for Inf, NaN and magnitudes that round up to 2^16 or beyond.
-__device__ __forceinline__ uint32_t encode_body(uint32_t xbits, bool& range) {
+// `tie` is for a value known more exactly than its fp32 bits: the sign of
+// (exact magnitude - this magnitude). It matters only when this magnitude
+// is exactly halfway between two fp9 values: then it picks the side (0:
+// the even mantissa). The exact value is within half an fp32 unit of this
+// one, and every fp9 midpoint is an fp32 value, so no other case moves.
+__device__ __forceinline__ uint32_t encode_body(uint32_t xbits, int tie, bool& range) {
     const uint32_t mag = xbits & 0x7FFFFFFFu;
     if (mag >= 0x7F800000u) {  // Inf or NaN
         range = true;
@@ -33,7 +39,7 @@ __device__ __forceinline__ uint32_t encode_body(uint32_t xbits, bool& range) {
         // mantissa moves to the next binade by plain addition.
         uint32_t code = (static_cast<uint32_t>(E - 112) << 3) | (M >> 20);
         const uint32_t rem = M & 0xFFFFFu;
-        if (rem > 0x80000u || (rem == 0x80000u && (code & 1u))) code += 1u;
+        if (rem > 0x80000u || (rem == 0x80000u && (tie > 0 || (tie == 0 && (code & 1u))))) code += 1u;
         if (code >= 0xF8u) {
             range = true;
             return 0xF8u;
@@ -49,7 +55,7 @@ __device__ __forceinline__ uint32_t encode_body(uint32_t xbits, bool& range) {
     uint32_t q = sig >> sh;
     const uint32_t rem = sig & ((1u << sh) - 1u);
     const uint32_t half = 1u << (sh - 1);
-    if (rem > half || (rem == half && (q & 1u))) q += 1u;  // q = 8 is the smallest normal
+    if (rem > half || (rem == half && (tie > 0 || (tie == 0 && (q & 1u))))) q += 1u;  // q = 8: smallest normal
     return q;
 }
 
@@ -67,13 +73,101 @@ __global__ void __launch_bounds__(256) pack_kernel(const float4* __restrict__ sr
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t bits = __float_as_uint(v[i]);
-            const uint32_t code = encode_body(bits, range);
+            const uint32_t code = encode_body(bits, 0, range);
             if (i < 4) lo |= code << (8 * i);
             else hi |= code << (8 * (i - 4));
             s |= (bits >> 31) << i;
         }
         body[g] = make_uint2(lo, hi);
         sign[g] = static_cast<uint8_t>(s);
+    }
+    if (range) record_status(status, FP9_ERR_RANGE);
+}
+
+// fp9 body of the exact product x * s, where x and s are fp32 values (x has
+// at most 4 significant bits: an fp8 e4m3 value). p = x * s is rounded to
+// fp32, and its error fma(x, s, -p) is exact, so p plus that error is the
+// exact product; it is rounded once to fp9. The error can only matter when
+// p lies exactly on an fp9 midpoint (every midpoint is an fp32 value and
+// the exact product is within half an fp32 unit of p), so it is computed
+// only then. Fast path: 2^-14 <= |p| < 63488, a normal fp9 that cannot
+// overflow; everything else goes through encode_body.
+__device__ __forceinline__ uint32_t encode_product(float x, float s, uint32_t& sign_bit, bool& range) {
+    const float p = x * s;
+    const uint32_t bits = __float_as_uint(p), mag = bits & 0x7FFFFFFFu;
+    sign_bit = bits >> 31;
+    if (mag - 0x38800000u < 0x47780000u - 0x38800000u) {
+        uint32_t code = (mag >> 20) - (112u << 3);
+        const uint32_t rem = mag & 0xFFFFFu;
+        if (rem == 0x80000u) {
+            const float d = fmaf(x, s, -p);
+            const float dm = sign_bit ? -d : d;  // exact magnitude - |p|
+            code += dm > 0.0f ? 1u : (dm < 0.0f ? 0u : (code & 1u));
+        } else {
+            code += rem > 0x80000u ? 1u : 0u;
+        }
+        return code;
+    }
+    const float d = fmaf(x, s, -p);
+    const float dm = sign_bit ? -d : d;
+    return encode_body(bits, (dm > 0.0f) - (dm < 0.0f), range);
+}
+
+template <int G>
+__device__ __forceinline__ void convert_group(const uint32_t (&in)[G / 4], float s, uint32_t (&out)[G / 4],
+                                              uint32_t& sb, bool& range) {
+    sb = 0;
+#pragma unroll
+    for (int w = 0; w < G / 4; ++w) {
+        out[w] = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // bytes 4w + 2h, 4w + 2h + 1
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((in[w] >> (16 * h)) & 0xFFFFu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            uint32_t s0, s1;
+            const uint32_t c0 = encode_product(x.x, s, s0, range);
+            const uint32_t c1 = encode_product(x.y, s, s1, range);
+            out[w] |= (c0 << (16 * h)) | (c1 << (16 * h + 8));
+            sb |= (s0 << (4 * w + 2 * h)) | (s1 << (4 * w + 2 * h + 1));
+        }
+    }
+}
+
+// fp8 checkpoint -> fp9: one thread per group of G (8 or 16) consecutive
+// weights of a row, all in one 128x128 scale block. The pages say the
+// DeepSeek-V3 release is fp8 ("一鸭三吃" memoir, section "真正埋下伏笔的是内存；
+// R1 之后，问题第一次被改写") with 128x128 block scales (section "先用 Qwen3 练级，
+// 再让 Qwen3.5 充当高压试炼场"). Each e4m3 byte becomes its exact fp16
+// (hardware conversion), then fp32; each weight is that value times the
+// block's scale, rounded once to fp9 (encode_product).
+template <int G>
+__global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restrict__ w8,
+                                                         const float* __restrict__ scale, uint32_t ngroups,
+                                                         uint32_t groups_per_row, uint32_t scale_cols,
+                                                         uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
+                                                         int32_t* status) {
+    constexpr int kWords = G / 4;
+    bool range = false;
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += gridDim.x * blockDim.x) {
+        const uint32_t row = g / groups_per_row, gc = g - row * groups_per_row;
+        const float sc = __ldg(scale + (row / 128u) * scale_cols + (gc * G) / 128u);
+        uint32_t in[kWords], out[kWords], sb;
+        if constexpr (G == 16) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8) + g);
+            in[0] = q.x, in[1] = q.y, in[2] = q.z, in[3] = q.w;
+        } else {
+            const uint2 q = __ldcs(reinterpret_cast<const uint2*>(w8) + g);
+            in[0] = q.x, in[1] = q.y;
+        }
+        convert_group<G>(in, sc, out, sb, range);
+        if constexpr (G == 16) {
+            __stcs(reinterpret_cast<uint4*>(body) + g, make_uint4(out[0], out[1], out[2], out[3]));
+            reinterpret_cast<uint16_t*>(sign)[g] = static_cast<uint16_t>(sb);
+        } else {
+            __stcs(reinterpret_cast<uint2*>(body) + g, make_uint2(out[0], out[1]));
+            sign[g] = static_cast<uint8_t>(sb);
+        }
     }
     if (range) record_status(status, FP9_ERR_RANGE);
 }
@@ -127,6 +221,30 @@ extern "C" fp9_status fp9_pack(const float* src, int64_t rows, int64_t cols, uin
     const int64_t ngroups = rows * (cols / 8);
     pack_kernel<<<elementwise_grid(ngroups), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(src), ngroups, reinterpret_cast<uint2*>(body), sign, d_status);
+    FP9_CUDA_TRY(cudaGetLastError());
+    return FP9_OK;
+}
+
+extern "C" fp9_status fp9_from_fp8(const uint8_t* w8, const float* scale_inv, int64_t rows, int64_t cols,
+                                   uint8_t* body, uint8_t* sign, int32_t* d_status, void* stream) {
+    FP9_CHECK_ARG(rows >= 0 && cols >= 0, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(cols % 8 == 0, FP9_ERR_SHAPE);
+    if (rows == 0 || cols == 0) return FP9_OK;
+    FP9_CHECK_ARG(w8 != nullptr && scale_inv != nullptr && body != nullptr && sign != nullptr,
+                  FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(w8, 8) && aligned(body, 8) && aligned(scale_inv, 4), FP9_ERR_ALIGN);
+    FP9_CHECK_ARG(rows * (cols / 8) <= 0xFFFFFFFFll, FP9_ERR_SHAPE);  // 32-bit group index
+    const bool wide = cols % 16 == 0 && aligned(w8, 16) && aligned(body, 16) && aligned(sign, 2);
+    const int G = wide ? 16 : 8;
+    const int64_t gpr = cols / G, ngroups = rows * gpr;
+    const uint32_t scols = static_cast<uint32_t>((cols + 127) / 128);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (wide)
+        fp8_to_fp9_kernel<16><<<elementwise_grid(ngroups), 256, 0, st>>>(
+            w8, scale_inv, static_cast<uint32_t>(ngroups), static_cast<uint32_t>(gpr), scols, body, sign, d_status);
+    else
+        fp8_to_fp9_kernel<8><<<elementwise_grid(ngroups), 256, 0, st>>>(
+            w8, scale_inv, static_cast<uint32_t>(ngroups), static_cast<uint32_t>(gpr), scols, body, sign, d_status);
     FP9_CUDA_TRY(cudaGetLastError());
     return FP9_OK;
 }

@@ -137,6 +137,27 @@ fp9_status fp9_pack(const float* src, int64_t rows, int64_t cols,
                     uint8_t* body, uint8_t* sign, int32_t* d_status, void* stream);
 
 /*
+ * fp9_from_fp8: convert an fp8 block-scaled checkpoint matrix to fp9 planes.
+ * The pages say the DeepSeek-V3 release is fp8 (about 688 GB; the page of
+ * [MEMOIR-FP9], section "真正埋下伏笔的是内存；R1 之后，问题第一次被改写")
+ * with the 128x128 block-scale format also used by Qwen3's fp8 checkpoints
+ * (same page, section "先用 Qwen3 练级，再让 Qwen3.5 充当高压试炼场"); fp9
+ * stores no scale.
+ *   w8        device uint8 [rows, cols]: fp8 e4m3 bytes (bias 7, no
+ *             infinities, S.1111.111 = NaN), 8-byte aligned.
+ *   scale_inv device fp32 [ceil(rows/128), ceil(cols/128)]: the scale of
+ *             each 128x128 block (row-major; edge blocks cover what is left).
+ *   body, sign as in fp9_pack (body 8-byte aligned). cols % 8 == 0.
+ *   Each weight e4m3(w8[r, c]) * scale_inv[r/128, c/128] is rounded once,
+ *   from the exact product, to the nearest fp9 (ties to the even mantissa),
+ *   as fp9_pack rounds an fp32 value; magnitudes >= 63488 and NaN are
+ *   recorded as FP9_ERR_RANGE in *d_status (stored as Inf / NaN codes).
+ */
+fp9_status fp9_from_fp8(const uint8_t* w8, const float* scale_inv, int64_t rows,
+                        int64_t cols, uint8_t* body, uint8_t* sign,
+                        int32_t* d_status, void* stream);
+
+/*
  * fp9_decode: fp9 planes -> fp32 [rows, cols], bit-exact: each value is
  * the IEEE fp16 with bits (body << 7 | sign << 15), widened [MEMOIR-FP9].
  *   body, sign as in fp9_pack (device); dst device fp32 [rows, cols],

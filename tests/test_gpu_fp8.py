@@ -1,0 +1,95 @@
+"""GPU parity for fp9_from_fp8 (fp8 e4m3 block-scale checkpoint -> fp9)
+against the oracle: bit-exact body and sign planes, the range status, on
+random codes and scales, ragged shapes (partial scale blocks, one group),
+the hand-derived worked examples, products whose fp32 rounding lands on an
+fp9 midpoint, and a full DeepSeek-V3 expert matrix."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from fp9_weight_expert_gb300 import binding
+from tests import test_oracle_fp8 as F8
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(w8, scale):
+    rows, cols = w8.shape
+    body = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    sign = torch.empty((rows, cols // 8), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.fp9_from_fp8(torch.from_numpy(w8).cuda(), torch.from_numpy(scale).cuda(), body, sign, status)
+    torch.cuda.synchronize()
+    return body.cpu().numpy(), sign.cpu().numpy(), int(status.item())
+
+
+def _check(w8, scale):
+    b, s, st = _gpu(w8, scale)
+    rb, rs, rerr = O.fp8_block_to_fp9(w8, scale)
+    assert np.array_equal(b, rb)
+    assert np.array_equal(s, rs)
+    assert (st == binding.FP9_ERR_RANGE) == rerr and st in (0, binding.FP9_ERR_RANGE)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (128, 128), (200, 136), (129, 264), (300, 1024)])
+def test_random_codes_and_block_scales(rows, cols):
+    rng = np.random.default_rng(rows * 1000 + cols)
+    w8 = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3C  # no NaN here (NaN is tested apart)
+    nbr, nbc = -(-rows // 128), -(-cols // 128)
+    scale = (np.exp2(rng.uniform(-14, 6, size=(nbr, nbc))) * rng.choice([1, -1], size=(nbr, nbc))).astype(np.float32)
+    _check(w8, scale)
+
+
+def test_worked_examples_and_midpoint_witnesses():
+    for code, sbits, sign, body, err in F8._golden():
+        w8 = np.full((1, 8), code, np.uint8)
+        scale = np.array([[F8._f32(sbits)]], np.float32)
+        b, s, st = _gpu(w8, scale)
+        assert int(b[0, 0]) == body and int(s[0, 0] & 1) == sign, (hex(code), hex(sbits))
+        assert (st == binding.FP9_ERR_RANGE) == bool(err)
+    # every witness the oracle's search finds, as one matrix per scale
+    for code in range(256):
+        x = float(O.e4m3_value(code))
+        if not np.isfinite(x) or x == 0:
+            continue
+        for mid in [1.0625 + 0.125 * j for j in range(8)]:
+            s0 = np.float32(mid / abs(x))
+            for step in (-2, -1, 1, 2):
+                sc = s0
+                for _ in range(abs(step)):
+                    sc = np.nextafter(sc, np.float32(np.inf) if step > 0 else np.float32(-np.inf))
+                if abs(float(np.float32(x) * sc)) != mid or abs(x * float(sc)) == mid:
+                    continue
+                _check(np.full((1, 8), code, np.uint8), np.array([[sc]], np.float32))
+
+
+def test_nan_and_overflow_set_the_range_status():
+    b, _, st = _gpu(np.full((1, 8), 0x7F, np.uint8), np.array([[1.0]], np.float32))
+    assert st == binding.FP9_ERR_RANGE and b[0, 0] == O.FP9_NAN_BODY
+    b, _, st = _gpu(np.full((1, 8), 0x7E, np.uint8), np.array([[256.0]], np.float32))
+    assert st == binding.FP9_ERR_RANGE and b[0, 0] == O.FP9_INF_BODY
+    _, _, st = _gpu(np.full((1, 8), 0x7E, np.uint8), np.array([[128.0]], np.float32))
+    assert st == 0
+
+
+def test_every_code_at_many_scales():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)[:248]
+    rng = np.random.default_rng(3)
+    w8 = np.tile(codes, (64, 1))
+    scale = np.exp2(rng.uniform(-18, 8, size=(1, 2))).astype(np.float32)
+    for _ in range(6):
+        scale = np.exp2(rng.uniform(-18, 8, size=(1, 2))).astype(np.float32)
+        _check(w8, scale)
+
+
+def test_full_dsv3_expert_matrix():
+    rng = np.random.default_rng(17)
+    rows, cols = 2048, 7168
+    w8 = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3C
+    # checkpoint-like scales: weight magnitudes around 1e-2 after scaling
+    scale = (np.exp2(rng.uniform(-14, -10, size=(rows // 128, cols // 128)))).astype(np.float32)
+    _check(w8, scale)
