@@ -293,6 +293,7 @@ def _native(args):
     if not args.no_extra and world == 1:
         extra = _side_runs(Ls, ws, status, dev, shape)
         extra["fp8_to_fp9"] = _convert_run(dev, _peaks()[0])
+        extra["stack12"] = _stack_run(dev, shape)
 
     if rank != 0:
         return None
@@ -383,6 +384,76 @@ def _side_runs(Ls, ws, status, dev, shape):
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
                             "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
     return res
+
+
+def _stack_run(dev, shape, n_layers=12, K=40):
+    """The 12-layer stack of the workload (config 5): 12 distinct resident
+    DeepSeek-V3 MoE layers (153 GB) with the residual + RMSNorm glue between
+    them, h <- h + MoE_l(RMSNorm(h)); the whole stack step is captured once
+    in a CUDA graph and replayed. Tokens/s through all 12 layers."""
+    import torch
+
+    from fp9_weight_expert_gb300 import Workspace, binding, layers, synth
+    H, I = shape.hidden, shape.inter
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    Ls = []
+    for l in range(n_layers):
+        L = layers.MoELayer(H, I, shape.n_experts, shape.n_groups, shape.topk_groups, shape.topk,
+                            shape.n_shared, shape.route_scale, dev)
+        kinds = (synth.ROUTED, synth.SHARED)
+        L.fill(lambda b, k, m: synth.ffn_weight(shape, I, H, synth.seed_for(7000, l, kinds[b], k, m), dev),
+               synth.normal((shape.n_experts, H), shape.router_std, synth.seed_for(7000, l, synth.ROUTER), dev),
+               status)
+        Ls.append(L)
+    out = {"layers": n_layers, "resident_gb": round(n_layers * 3 * H * I * (shape.n_experts + shape.n_shared)
+                                                    * FP9_BYTES_PER_WEIGHT / 1e9, 1)}
+    for bsz in (1, 2):
+        h0 = synth.tokens(bsz, H, synth.seed_for(7100, bsz, synth.TOKENS), dev) * 2.0
+        h = h0.clone()
+        x = torch.empty_like(h)
+        y = torch.empty_like(h)
+        ids = torch.empty((n_layers, bsz, shape.topk), dtype=torch.int32, device=dev)
+        ws = Workspace.for_moe(Ls[0], bsz, dev)
+
+        def step():
+            binding.fp9_residual_rmsnorm(h, None, x)
+            for l, L in enumerate(Ls):
+                binding.fp9_moe_forward(L, x, y, ws.tensor, status, ids[l])
+                binding.fp9_residual_rmsnorm(h, y, x)
+
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("stack status: " + binding.status_str(int(status.item())))
+        ms = a.elapsed_time(b) / K
+        idc = ids.cpu()
+        experts = sum(len(set(idc[l].flatten().tolist())) + shape.n_shared for l in range(n_layers))
+        wbytes = experts * 3 * I * H * FP9_BYTES_PER_WEIGHT
+        out[f"bsz{bsz}"] = {"tok_s": round(bsz / (ms / 1e3), 1), "us_per_stack_step": round(ms * 1e3, 1),
+                            "us_per_layer": round(ms * 1e3 / n_layers, 2),
+                            "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+                            "experts_streamed": experts}
+    del Ls
+    torch.cuda.empty_cache()
+    return out
 
 
 def _convert_run(dev, peak):

@@ -83,3 +83,42 @@ def test_stack_of_three_layers_matches_oracle():
     assert checked >= 1
     ref_h = O.stack(h_in, [o.kwargs() for o in Os])
     assert support.max_rel_err(h.cpu().numpy(), ref_h) <= 1e-3   # end-to-end drift
+
+
+def test_stack_in_a_cuda_graph_matches_eager():
+    """The same three-layer stack captured once in a CUDA graph (kernels
+    launched with programmatic dependent launch become graph nodes) and
+    replayed gives bit-identical hidden states."""
+    shape, bsz = synth.TINY, 2
+    Ls = [support.build_layer(shape, base=60, layer=l) for l in range(3)]
+    Os = [support.OracleLayer(shape, base=60, layer=l) for l in range(3)]
+    h0 = support.safe_tokens(shape, Os[0].w_router, bsz, 61, device="cuda") * 2.0
+    ws = Workspace.for_moe(Ls[0], bsz)
+    h = h0.clone()
+    x = torch.empty_like(h)
+    y = torch.empty_like(h)
+
+    def run():
+        binding.fp9_residual_rmsnorm(h, None, x)
+        for L in Ls:
+            binding.fp9_moe_forward(L, x, y, ws.tensor)
+            binding.fp9_residual_rmsnorm(h, y, x)
+
+    run()  # eager (also sets the kernels' attributes before capture)
+    torch.cuda.synchronize()
+    eager = h.clone()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        h.copy_(h0)
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        h.copy_(h0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(h, eager)
