@@ -80,6 +80,17 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense bf16 tensor TFLOP/s timed alone (burst), measured on this GPU
+    model, else the fallback figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 # ------------------------------------------------------------ clock sampler
 
 class ClockSampler:
@@ -294,6 +305,7 @@ def _native(args):
         extra = _side_runs(Ls, ws, status, dev, shape)
         extra["fp8_to_fp9"] = _convert_run(dev, _peaks()[0])
         extra["stack12"] = _stack_run(dev, shape)
+        extra["prefill"] = _prefill_run(dev, _tensor_peak())
 
     if rank != 0:
         return None
@@ -500,6 +512,50 @@ def _convert_run(dev, peak):
     return {"weights_per_call": weights, "us_per_call": round(us, 1), "bytes_per_call": int(nbytes),
             "gbs": round(gbs, 1), "peak": peak, "frac": round(gbs / peak, 4), "bound": "hbm",
             "inputs_vs_l2": "752 MB per call, larger than L2"}
+
+
+def _prefill_run(dev, peaks):
+    """fp9_ffn_prefill (the FFN over many prompt tokens on the tensor cores)
+    for the pages' long prompt (1481 tokens) and a 4096-token one, through
+    the dense FFN (7168 / 18432) and through DeepSeek-V3 experts (7168 /
+    2048, 8 experts rotated so their 396 MB of weights exceed L2): tensor
+    TFLOP/s of 2 * m * 3 * hidden * inter flops against the measured dense
+    bf16 peak (fp16 runs at the bf16 rate)."""
+    import torch
+
+    from fp9_weight_expert_gb300 import FFNBank, Workspace, binding, synth
+    peak, peak_src = peaks
+    out = {"peak_source": peak_src}
+    for name, n, H, I in (("dense_7168x18432", 1, 7168, 18432), ("expert_7168x2048", 8, 7168, 2048)):
+        f = FFNBank(n, I, H, dev)
+        for k in range(n):
+            for m in range(3):
+                f.pack(k, m, synth.ffn_weight(None, I, H, synth.seed_for(17, 0, synth.DENSE, k, m), dev))
+        for m in (1481, 4096):
+            x = synth.tokens(m, H, 5, dev)
+            y = torch.empty_like(x)
+            ws = Workspace.for_prefill(f, m, dev).tensor
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+            for i in range(3):
+                binding.fp9_ffn_prefill(f, x, y, ws, i % n, status)
+            torch.cuda.synchronize()
+            K = 20
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(K):
+                binding.fp9_ffn_prefill(f, x, y, ws, i % n, status)
+            b.record()
+            torch.cuda.synchronize()
+            if int(status.item()) != 0:
+                raise RuntimeError("fp9_ffn_prefill status: " + binding.status_str(int(status.item())))
+            us = a.elapsed_time(b) / K * 1e3
+            tf = 2.0 * m * 3 * H * I / (us * 1e-6) / 1e12
+            out[f"{name}_m{m}"] = {"us_per_call": round(us, 1), "tflops": round(tf, 1),
+                                   "tok_per_s": round(m / (us * 1e-6)), "peak_tflops": peak,
+                                   "frac": round(tf / peak, 4), "bound": "tensor", "dtype": "fp16 x fp9->fp16"}
+        del f
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle

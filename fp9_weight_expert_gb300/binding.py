@@ -27,6 +27,8 @@ FP9_ERR_TIMEOUT = 7
 
 FP9_MAX_BSZ = 8
 FP9_MAX_HIDDEN = 7168
+FP9_MAX_PREFILL_TOKENS = 1048576
+FP9_MAX_PREFILL_HIDDEN = 32768
 
 
 class Fp9Error(RuntimeError):
@@ -97,6 +99,10 @@ _SIGS = {
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "fp9_ffn_prefill": (ctypes.c_int, [ctypes.POINTER(FFNBankC), ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(FFNBankC), ctypes.c_int64]),
 }
 
 
@@ -241,3 +247,16 @@ def fp9_moe_forward_noalloc(layer, x: torch.Tensor, y: torch.Tensor, status: tor
 
 def noalloc_scratch_bytes() -> int:
     return int(load().fp9_moe_noalloc_scratch_bytes())
+
+
+def prefill_workspace_bytes(ffn, m: int) -> int:
+    return int(load().fp9_prefill_workspace_bytes(ctypes.byref(ffn.c_struct()), m))
+
+
+def fp9_ffn_prefill(ffn, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, k: int = 0,
+                    status: torch.Tensor | None = None, stream=None) -> None:
+    """y [m, hidden] = FFN k of the bank ``ffn`` applied to x [m, hidden]
+    (fp32), on the tensor cores (x and h rounded to fp16, fp32 accumulation)."""
+    _check(load().fp9_ffn_prefill(ctypes.byref(ffn.c_struct()), k, _ptr(x), x.shape[0], _ptr(y), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+           "fp9_ffn_prefill")

@@ -115,3 +115,10 @@ class Workspace:
         if n == 0:
             raise binding.Fp9Error(binding.FP9_ERR_INVALID_ARG, "dense_workspace_bytes")
         return cls(n, device)
+
+    @classmethod
+    def for_prefill(cls, ffn: FFNBank, m: int, device="cuda"):
+        n = binding.prefill_workspace_bytes(ffn, m)
+        if n == 0:
+            raise binding.Fp9Error(binding.FP9_ERR_INVALID_ARG, "prefill_workspace_bytes")
+        return cls(n, device)

@@ -209,6 +209,39 @@ fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
                          void* stream);
 
 /*
+ * fp9_ffn_prefill: y = FFN_k(x) for m tokens at once (prompt prefill), on
+ * the tensor cores. The pages run the same fp9 FFN over every prompt token
+ * and list their prefill kernel as far below the hardware's compute peak
+ * (the page of [MEMOIR-FP9], section "最终结果", its list of limitations);
+ * with m tokens the FFN is two dense GEMMs (gate/up with SwiGLU, then down).
+ *   ffn    host struct of a bank (device planes); k in [0, ffn->n) selects
+ *          the FFN (e.g. the dense FFN, or one expert of a bank).
+ *   x      device fp32 [m, hidden]; y device fp32 [m, hidden]; both
+ *          16-byte aligned. y may alias x (x is read, as fp16, before y
+ *          is written). 0 <= m <= FP9_MAX_PREFILL_TOKENS
+ *          (m = 0 is a no-op).
+ *   Shape: hidden % 256 == 0 (256 <= hidden <= FP9_MAX_PREFILL_HIDDEN),
+ *          inter % 128 == 0 (inter <= FP9_MAX_INTER), else FP9_ERR_SHAPE.
+ *   ws     device, >= fp9_prefill_workspace_bytes(ffn, m), 256-byte aligned
+ *          (holds x and h = SiLU(W_gate x) * (W_up x) as fp16).
+ *   Arithmetic: the fp9 weights are exact in fp16 (body << 7 | sign << 15
+ *   is their fp16, [MEMOIR-FP9]); x and h are rounded to fp16 (round to
+ *   nearest even), the MMA operand type, and products are accumulated in
+ *   fp32, so y differs from the exact FFN by about the fp16 unit roundoff
+ *   (2^-11) relative to sum |terms|. An x or h whose fp16 is not finite
+ *   (|v| >= 65520, Inf, NaN) is recorded as FP9_ERR_RANGE in *d_status.
+ */
+#define FP9_MAX_PREFILL_TOKENS 1048576
+#define FP9_MAX_PREFILL_HIDDEN 32768
+fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t k, const float* x,
+                           int64_t m, float* y, void* ws, size_t ws_bytes,
+                           int32_t* d_status, void* stream);
+
+/* Workspace bytes of fp9_ffn_prefill for m tokens (0 if the arguments are
+ * invalid). */
+size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m);
+
+/*
  * fp9_residual_rmsnorm: stack glue between layers, per token t:
  *   h[t] += y[t] (skipped when y is NULL);
  *   x_out[t] = h[t] / sqrt(mean(h[t]^2) + eps)   (unit gain).

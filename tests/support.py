@@ -97,3 +97,68 @@ def max_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     for g, r in zip(gpu, ref):
         out = max(out, float(np.max(np.abs(g - r)) / max(np.max(np.abs(r)), 1e-30)))
     return out
+
+
+# ---------------------------------------------------------------- prefill ---
+# fp9_ffn_prefill rounds x and h = SiLU(g) * u to fp16 (the tensor cores'
+# operand type; the fp9 weights are exact in fp16) and accumulates in fp32.
+# Its tolerance against the exact FFN comes from that arithmetic:
+#   * element-wise, a worst-case first-order bound (prefill_error_bound);
+#   * in aggregate, the relative L2 error of two independent fp16 roundings
+#     of the GEMM operands: each contributes about u16 / sqrt(3) = 2.8e-4
+#     relative, together about 3.7e-4 (measured on an fp16 emulation of the
+#     path at three shapes). The limits below leave 1.6x (global) and 2.3x
+#     (per row) headroom, and reject rounding h to bf16 (1.7e-3) or dropping
+#     one 64-wide K chunk (>= 0.08).
+PREFILL_FRO = 6e-4    # ||y - y_exact||_F / ||y_exact||_F over a whole output
+PREFILL_ROW = 1.2e-3  # the same for each token row
+U16 = 2.0 ** -11      # unit roundoff of fp16, round to nearest even
+F16_SUB = 2.0 ** -25  # half the spacing of fp16 subnormals
+
+
+def prefill_error_bound(x, wg, wu, wd):
+    """Worst-case |y_path - y_exact| per element for the fp16-operand path.
+
+    x [m, H] (fp64), wg/wu [I, H] and wd = down_t [I, H] decoded weights.
+    Terms: fp16 rounding of x (relative U16, or F16_SUB absolute for
+    subnormals); fp32 accumulation of K exact products, allowing one ulp per
+    addition (gamma = K * 2^-23); |SiLU'| <= 1.1; a few fp32 ulps for the
+    SiLU and the product; fp16 rounding of h; then the same accumulation
+    bound for the down GEMM over I terms.
+    """
+    x = np.asarray(x, np.float64)
+    K, I = x.shape[1], wg.shape[0]
+    gk, gi = K * 2.0 ** -23, I * 2.0 ** -23
+    ax = np.abs(x)
+    awg, awu, awd = np.abs(wg), np.abs(wu), np.abs(wd)
+    g, u = x @ wg.T, x @ wu.T
+    dg = (U16 + gk * (1 + U16)) * (ax @ awg.T) + F16_SUB * awg.sum(1) * (1 + gk)
+    du = (U16 + gk * (1 + U16)) * (ax @ awu.T) + F16_SUB * awu.sum(1) * (1 + gk)
+    s = g / (1.0 + np.exp(-g))
+    h = s * u
+    dh0 = 1.1 * dg * (np.abs(u) + du) + np.abs(s) * du + 4 * 2.0 ** -24 * np.abs(h)
+    dh = dh0 + U16 * (np.abs(h) + dh0) + F16_SUB
+    return dh @ awd + gi * ((np.abs(h) + dh) @ awd)
+
+
+def prefill_errors(y, y_exact):
+    """(global relative L2 error, largest per-row relative L2 error)."""
+    y = np.asarray(y, np.float64)
+    y_exact = np.asarray(y_exact, np.float64)
+    d = y - y_exact
+    fro = float(np.linalg.norm(d) / max(np.linalg.norm(y_exact), 1e-300))
+    rows = np.linalg.norm(d, axis=1) / np.maximum(np.linalg.norm(y_exact, axis=1), 1e-300)
+    return fro, float(rows.max())
+
+
+def check_prefill(y, x, wg, wu, wd, y_exact=None):
+    """Asserts the prefill tolerance for y [m, H] given the exact inputs."""
+    if y_exact is None:
+        y_exact = O.ffn(x, wg, wu, wd)
+    bound = prefill_error_bound(x, wg, wu, wd)
+    over = np.abs(np.asarray(y, np.float64) - y_exact) - bound
+    assert over.max() <= 0.0, f"element-wise bound exceeded by {over.max():.3e}"
+    fro, row = prefill_errors(y, y_exact)
+    assert fro <= PREFILL_FRO, f"relative L2 error {fro:.3e} > {PREFILL_FRO}"
+    assert row <= PREFILL_ROW, f"per-row relative L2 error {row:.3e} > {PREFILL_ROW}"
+    return fro, row

@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ["fp9_pack", "fp9_decode", "moe_router", "fp9_moe_forward", "fp9_dense_ffn",
               "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
-              "fp9_selftest_timeout", "fp9_status_str"]:
+              "fp9_selftest_timeout", "fp9_status_str", "fp9_from_fp8", "fp9_ffn_prefill",
+              "fp9_prefill_workspace_bytes"]:
         assert n in names, n
 
 
@@ -104,3 +105,31 @@ def test_dense_and_norm_argument_checks(lib):
     assert lib.fp9_residual_rmsnorm(P, None, P, 0, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_INVALID_ARG
     assert lib.fp9_residual_rmsnorm(P + 4, None, P, 1, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_ALIGN
     assert lib.fp9_selftest_timeout(P, 1 << 20, None, 100, None) == binding.FP9_ERR_INVALID_ARG
+
+
+def test_prefill_argument_checks(lib):
+    b = _bank(2, 128, 512)
+
+    def call(bank=b, k=0, x=P, m=4, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 30):
+        return lib.fp9_ffn_prefill(ctypes.byref(bank) if bank is not None else None, k, x, m, y, ws, ws_bytes,
+                                   None, None)
+
+    need = lib.fp9_prefill_workspace_bytes(ctypes.byref(b), 4)
+    assert need == 4 * 512 * 2 + 1024            # x and h as fp16, each 256-byte aligned
+    assert call(bank=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(k=2) == binding.FP9_ERR_INVALID_ARG
+    assert call(k=-1) == binding.FP9_ERR_INVALID_ARG
+    assert call(bank=_bank(2, 128, 384)) == binding.FP9_ERR_SHAPE        # hidden % 256
+    assert call(bank=_bank(2, 100, 512)) == binding.FP9_ERR_SHAPE        # inter % 128
+    assert call(bank=_bank(2, 128, 65536)) == binding.FP9_ERR_SHAPE      # > FP9_MAX_PREFILL_HIDDEN
+    assert call(bank=_bank(2, 128, 512, base=P + 8)) == binding.FP9_ERR_ALIGN
+    assert call(m=-1) == binding.FP9_ERR_INVALID_ARG
+    assert call(m=binding.FP9_MAX_PREFILL_TOKENS + 1) == binding.FP9_ERR_INVALID_ARG
+    assert call(m=0, x=None, y=None, ws=None) == binding.FP9_OK           # empty: no-op
+    assert call(x=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(x=P + 4) == binding.FP9_ERR_ALIGN
+    assert call(y=P + 8) == binding.FP9_ERR_ALIGN
+    assert call(ws=P + 16) == binding.FP9_ERR_ALIGN
+    assert call(ws_bytes=need - 1) == binding.FP9_ERR_WORKSPACE
+    assert lib.fp9_prefill_workspace_bytes(ctypes.byref(_bank(2, 128, 384)), 4) == 0
+    assert lib.fp9_prefill_workspace_bytes(ctypes.byref(b), -1) == 0
