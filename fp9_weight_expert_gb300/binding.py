@@ -103,6 +103,10 @@ _SIGS = {
                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                        ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(FFNBankC), ctypes.c_int64]),
+    "fp9_moe_prefill": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_moe_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(MoELayerC), ctypes.c_int64]),
 }
 
 
@@ -260,3 +264,17 @@ def fp9_ffn_prefill(ffn, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, k: 
     _check(load().fp9_ffn_prefill(ctypes.byref(ffn.c_struct()), k, _ptr(x), x.shape[0], _ptr(y), _ptr(ws),
                                   ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
            "fp9_ffn_prefill")
+
+
+def moe_prefill_workspace_bytes(layer, m: int) -> int:
+    return int(load().fp9_moe_prefill_workspace_bytes(ctypes.byref(layer.c_struct()), m))
+
+
+def fp9_moe_prefill(layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
+                    status: torch.Tensor | None = None, ids: torch.Tensor | None = None,
+                    weights: torch.Tensor | None = None, stream=None) -> None:
+    """y [m, hidden] = the MoE layer applied to m tokens x (fp32) at once,
+    expert FFNs on the tensor cores (fp16 operands, fp32 accumulation)."""
+    _check(load().fp9_moe_prefill(ctypes.byref(layer.c_struct()), _ptr(x), x.shape[0], _ptr(y), _ptr(ids),
+                                  _ptr(weights), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                  _stream(stream)), "fp9_moe_prefill")

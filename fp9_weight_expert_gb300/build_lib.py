@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfp9moe.so")
 
-SOURCES = ["fp9_codec.cu", "fp9_router.cu", "fp9_expert.cu", "fp9_stack.cu", "fp9_prefill.cu"]
+SOURCES = ["fp9_codec.cu", "fp9_router.cu", "fp9_expert.cu", "fp9_stack.cu", "fp9_prefill.cu", "fp9_moe_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

@@ -28,10 +28,10 @@
 //   raw  the fp9 planes of 128 K columns of both weight operands (bodies and
 //        sign planes), loaded by TMA as they lie in memory;
 //   B    the decoded weights of 64 K columns in the MMA's operand layout.
-// Warp roles: warps 0-7 decode raw -> B (one 16-byte fp16 chunk of 8 weights
-// per task) and run the epilogue; warp 8 issues the activation loads, warp
-// 9 the raw weight loads (so the HBM weight stream runs ahead of the MMAs by
-// up to the raw ring's depth), warp 10 one thread issues the MMAs and
+// Warp roles: warps 0-15 decode raw -> B (one 16-byte fp16 chunk of 8
+// weights per task) and run the epilogue; warp 16 issues the activation
+// loads, warp 17 the raw weight loads (so the HBM weight stream runs ahead
+// of the MMAs by up to the raw ring's depth), warp 18 one thread issues the MMAs and
 // commits each A and B slot back through an mbarrier. gate/up weight rows
 // are K-major; down_t tiles are MN-major (K = inter runs across rows), read
 // through the transposed-B bit. Every wait is bounded: a timeout records
@@ -48,52 +48,61 @@
 #include "fp9_device.cuh"
 #include "fp9_host.h"
 #include "fp9_plan.h"
+#include "fp9_prefill.h"
 #include "fp9_tc.cuh"
 #include "fp9moe.h"
 
 namespace fp9 {
 namespace {
 
-constexpr int kTileRows = 128;                        // rows of one MMA tile = TMEM lanes
+constexpr int kTileRows = 128;                        // token rows of one MMA tile = TMEM lanes
 constexpr int kChunkK = 64;                           // K per A / B slot: 128 bytes of fp16
 constexpr int kRawK = 128;                            // K per raw slot (16 sign bytes per row)
-constexpr int kTileBytes = kTileRows * kChunkK * 2;   // 16 KiB: one 128 x 64 fp16 tile
-constexpr int kBSlotBytes = 2 * kTileBytes;           // two weight operands
-constexpr int kRawBodyBytes = 2 * kTileRows * kRawK;  // 32 KiB of fp9 bodies
-constexpr int kRawSlotBytes = kRawBodyBytes + 2 * kTileRows * (kRawK / 8);  // + 4 KiB of signs
-constexpr int kDecoderWarps = 8;
+constexpr int kTileBytes = kTileRows * kChunkK * 2;   // 16 KiB: one 128 x 64 fp16 activation tile
+constexpr int kDecoderWarps = 16;
 constexpr int kDecoderThreads = kDecoderWarps * 32;
-constexpr int kActWarp = 8, kRawWarp = 9, kMmaWarp = 10;
-constexpr int kThreads = 11 * 32;
+constexpr int kActWarp = kDecoderWarps, kRawWarp = kDecoderWarps + 1, kMmaWarp = kDecoderWarps + 2;
+constexpr int kThreads = (kDecoderWarps + 3) * 32;
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kGroupM = 8;                            // M tiles per CTA-order group
 constexpr uint64_t kTimeoutNs = 1000000000ull;        // 1 s per wait
-constexpr int kTasks = 2 * kTileRows * kChunkK / 8 / kDecoderThreads;  // 8 decode tasks per thread per chunk
-// MN-major 128-byte-swizzle operand (down_t tiles): 64 output columns x 8 K
-// rows per 1024-byte atom; the two 64-column atoms of a 128-column half sit
-// 1024 bytes apart, 8-row K groups 2048 bytes apart.
+// Weight tile of a CTA: 2 x 128 rows = one N = 256 MMA operand.
+//   gate/up: 128 rows of W_gate then 128 rows of W_up, K-major with the
+//            128-byte swizzle (rows 128 B apart in 8-row groups of 1024 B);
+//   down:    256 output columns of down_t, MN-major with the 128-byte
+//            swizzle: atoms of 64 columns x 8 K rows (1024 B), the 4 atoms
+//            of a K group 1024 B apart, 8-row K groups 4096 B apart.
+// One M = 128, N = 256, K = 16 MMA per 16 K columns and 128 tokens: the
+// tensor core takes about as long for N = 128 as for N = 256, so the two
+// operands of a tile go through one instruction.
+constexpr int kNR = 128;                              // weight rows per operand
+constexpr int kBTile = kNR * 128;                     // 16 KiB: one operand, 64 K columns, fp16
+constexpr int kBSlot = 2 * kBTile;                    // the N = 256 operand
+constexpr int kRawBody = 256 * kNR;                   // 32 KiB of bodies per raw slot
+constexpr int kRawSlot = 288 * kNR;                   // + 4 KiB of signs
+constexpr int kTasks = 16 * kNR / kDecoderThreads;    // 4 decode tasks of 8 weights per thread per chunk
 constexpr uint32_t kMnAtomStride = 1024;
-constexpr uint32_t kMnGroupStride = 2048;
+constexpr uint32_t kMnGroupStride = 4096;
 
-// Ring depths: the raw and B rings by tile height, the A ring takes what is
-// left of the shared memory.
+// Ring depths. 128-token tiles: three activation slots, two decoded slots,
+// three raw slots (two in flight while one is decoded: four 64-wide chunks
+// of weights). 256-token tiles (twice the MMA time per chunk): two of each.
 template <int MH>
 struct Cfg {
-    static constexpr int kRawSlots = MH == 1 ? 3 : 2;
-    static constexpr int kBSlots = 2;
     static constexpr int kASlotBytes = MH * kTileBytes;
-    static constexpr int kFixed = 1024 + kCtlBytes + kRawSlots * kRawSlotBytes + kBSlots * kBSlotBytes;
-    static constexpr int kASlots = (kSmemMax - kFixed) / kASlotBytes;
-    static constexpr int kSmem = kFixed + kASlots * kASlotBytes;
+    static constexpr int kASlots = MH == 1 ? 3 : 2;
+    static constexpr int kBSlots = 2;
+    static constexpr int kRawSlots = MH == 1 ? 3 : 2;
+    static constexpr int kSmem = 1024 + kCtlBytes + kASlots * kASlotBytes + kBSlots * kBSlot + kRawSlots * kRawSlot;
     static constexpr uint32_t kTmemCols = MH * 256;
-    static_assert(kASlots >= 2 && kASlots <= 8, "activation ring");
+    static_assert(kSmem <= kSmemMax, "shared memory");
 };
 
 struct Ctl {
     uint64_t a_full[8], a_empty[8];   // activation ring: TMA bytes / MMA commit
-    uint64_t w_full[4], w_empty[4];   // raw ring: TMA bytes / 8 decoder warps
-    uint64_t b_full[4], b_empty[4];   // decoded ring: 8 decoder warps / MMA commit
+    uint64_t w_full[4], w_empty[4];   // raw ring: TMA bytes / the decoder warps
+    uint64_t b_full[4], b_empty[4];   // decoded ring: the decoder warps / MMA commit
     uint64_t done;                    // every MMA of the CTA finished
     uint32_t tmem;
     int abort;
@@ -103,13 +112,15 @@ static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 // 2-D tiled tensor maps (TMA descriptors) of one launch.
 struct PrefillMaps {
-    CUtensorMap act;       // fp16 [m, K], box 64 x 128, 128-byte swizzle
+    CUtensorMap act;       // fp16 [rows, K], box 64 x 128, 128-byte swizzle
     CUtensorMap body[2];   // gate/up: W_gate, W_up bodies, box 64 x 128; down: down_t, box 256 x 128
     CUtensorMap sign[2];   // the sign planes, box 16 x 128 (gate/up) or 32 x 128 (down)
+    CUtensorMap body_sh[2];  // grouped launches: the same for the shared-expert bank
+    CUtensorMap sign_sh[2];
 };
 
 struct PrefillArgs {
-    int32_t m;               // tokens
+    int32_t m;               // tokens (rows of act and out)
     int32_t mtiles, ntiles;  // CTA tiles along tokens / output columns
     int32_t nk;              // K / 64
     int32_t wrow0;           // first weight row of the FFN in the planes
@@ -117,6 +128,12 @@ struct PrefillArgs {
     int64_t ldo;             // row stride of out (elements)
     int32_t* status;
     uint64_t timeout_ns;
+    // grouped launches (GroupTableDev): token tile -> FFN and rows
+    const int32_t* g_row;
+    const int32_t* g_cnt;
+    const int32_t* g_mtile;
+    int32_t n_groups, n_routed;
+    int32_t inter;           // weight rows per FFN
 };
 
 // CTA order: groups of kGroupM token tiles walk the output tiles together,
@@ -173,12 +190,13 @@ __device__ __forceinline__ uint4 decode8_half(uint2 w, uint32_t s8) {
 }
 
 // Decodes K half `h` (64 columns) of raw slot `raw` into B slot `sB`.
-// Task u = t + 256 i of decoder thread t (8 per thread) is 8 weights:
+// Task u = t + 512 i of decoder thread t (4 per thread) is 8 weights:
 //   gate/up: operand u / 1024, row (u / 8) mod 128, K columns 8 (u mod 8)
-//            + [0, 8) -> chunk u mod 8 of the row in the K-major layout.
+//            + [0, 8) -> chunk u mod 8 of tile row 128 * operand + row.
 //            Raw bodies: [operand][half][row][64 B], signs [operand][row][16 B].
-//   down:    K row u / 32, output columns 8 (u mod 32) + [0, 8) -> chunk of
-//            the MN-major layout. Raw bodies: [K row][256 B], signs [K row][32 B].
+//   down:    K row u / 32, output columns 8 (u mod 32) + [0, 8) -> chunk
+//            u mod 8 of atom (u / 8) mod 4. Raw bodies: [K row][256 B],
+//            signs [K row][32 B].
 // The 8 threads of a quarter warp write 8 chunks of one row (or one atom
 // row), which the swizzle spreads over 8 bank groups; a half warp reads
 // 128 contiguous raw bytes.
@@ -189,16 +207,15 @@ __device__ __forceinline__ void decode_chunk(int t, uint32_t raw, int h, uint32_
         const uint32_t u = static_cast<uint32_t>(t + kDecoderThreads * i);
         if (!kDown) {
             const uint32_t b = u >> 10, row = (u >> 3) & 127u, c = u & 7u;
-            const uint2 w = ld_shared_v2(raw + b * (kTileRows * kRawK) + h * (kTileRows * 64) + row * 64u + c * 8u);
-            const uint32_t s = ld_shared_u8(raw + kRawBodyBytes + b * (kTileRows * 16) + row * 16u + h * 8u + c);
-            st_shared_v4(sB + b * kTileBytes + sw128_offset(row, c * 8u), decode8_half(w, s));
+            const uint2 w = ld_shared_v2(raw + b * (kNR * kRawK) + h * (kNR * 64) + row * 64u + c * 8u);
+            const uint32_t s = ld_shared_u8(raw + kRawBody + b * (kNR * 16) + row * 16u + h * 8u + c);
+            st_shared_v4(sB + b * kBTile + sw128_offset(row, c * 8u), decode8_half(w, s));
         } else {
-            const uint32_t kr = u >> 5, c = u & 31u, rr = h * 64u + kr;
+            const uint32_t kr = u >> 5, c = u & 31u, rr = h * 64u + kr, x = kr & 7u;
             const uint2 w = ld_shared_v2(raw + rr * 256u + c * 8u);
-            const uint32_t s = ld_shared_u8(raw + kRawBodyBytes + rr * 32u + c);
-            const uint32_t x = kr & 7u;
-            const uint32_t dst = sB + (c >> 4) * kTileBytes + (kr >> 3) * kMnGroupStride + ((c >> 3) & 1u) * kMnAtomStride +
-                                 x * 128u + (((c & 7u) ^ x) << 4);
+            const uint32_t s = ld_shared_u8(raw + kRawBody + rr * 32u + c);
+            const uint32_t dst = sB + (kr >> 3) * kMnGroupStride + (c >> 3) * kMnAtomStride + x * 128u +
+                                 (((c & 7u) ^ x) << 4);
             st_shared_v4(dst, decode8_half(w, s));
         }
     }
@@ -222,17 +239,51 @@ __device__ __forceinline__ void fail(Ctl& ctl, int32_t* status) {
     ctl.abort = 1;
 }
 
-template <bool kDown, int MH>
+template <bool kDown, int MH, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillMaps maps,
                                                               const PrefillArgs p) {
     using C = Cfg<MH>;
+    static_assert(!kGrouped || MH == 1, "grouped tiles are 128 rows");
+    // The CTA's tile: rows [arow0, arow0 + nvalid) of act and out (rows past
+    // nvalid are computed but not stored), output columns from n0, weight
+    // rows of its FFN from wrow0 in the routed or the shared planes.
+    int arow0, nvalid, n0, wrow0;
+    bool shared_bank = false;
+    if (kGrouped) {
+        grid_dependency_wait();  // the group table comes from the previous launches
+        const int total = p.g_mtile[p.n_groups] * p.ntiles;
+        if (static_cast<int>(blockIdx.x) >= total) return;  // the grid is an upper bound
+        const int q = blockIdx.x / p.ntiles, nt = blockIdx.x - q * p.ntiles;
+        int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.g_mtile + mid) <= q) lo = mid;
+            else hi = mid - 1;
+        }
+        const int mt = q - __ldg(p.g_mtile + lo);
+        arow0 = __ldg(p.g_row + lo) + mt * kTileRows;
+        nvalid = __ldg(p.g_cnt + lo) - mt * kTileRows;
+        shared_bank = lo >= p.n_routed;
+        wrow0 = (shared_bank ? lo - p.n_routed : lo) * p.inter;
+        n0 = nt * (kDown ? 2 * kNR : kNR);
+    } else {
+        int mt, nt;
+        tile_of(blockIdx.x, p.mtiles, p.ntiles, mt, nt);
+        arow0 = mt * kTileRows * MH;
+        nvalid = p.m - arow0;
+        wrow0 = p.wrow0;
+        // output columns: 128 intermediate rows (gate/up) or 256 hidden columns (down)
+        n0 = nt * (kDown ? 2 * kNR : kNR);
+    }
+    const CUtensorMap* bmap = shared_bank ? maps.body_sh : maps.body;
+    const CUtensorMap* smap = shared_bank ? maps.sign_sh : maps.sign;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw0 = smem_addr(smem_raw);
     const uint32_t base = (raw0 + 1023u) & ~1023u;
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw + (base - raw0));
     const uint32_t ringA = base + kCtlBytes;                           // 1024-aligned slots
     const uint32_t ringB = ringA + C::kASlots * C::kASlotBytes;
-    const uint32_t ringW = ringB + C::kBSlots * kBSlotBytes;
+    const uint32_t ringW = ringB + C::kBSlots * kBSlot;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -255,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     if (warp == kActWarp && lane == 0) prefetch_map(&maps.act);
     if (warp == kRawWarp && lane == 0) {
-        prefetch_map(&maps.body[0]);
-        prefetch_map(&maps.sign[0]);
+        prefetch_map(&bmap[0]);
+        prefetch_map(&smap[0]);
         if (!kDown) {
-            prefetch_map(&maps.body[1]);
-            prefetch_map(&maps.sign[1]);
+            prefetch_map(&bmap[1]);
+            prefetch_map(&smap[1]);
         }
     }
     if (warp == 0) tc_alloc(smem_addr(&ctl.tmem), C::kTmemCols);
@@ -268,11 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
 
-    int mt, nt;
-    tile_of(blockIdx.x, p.mtiles, p.ntiles, mt, nt);
-    const int m0 = mt * kTileRows * MH;
-    // output columns: 128 intermediate rows (gate/up) or 256 hidden columns (down)
-    const int n0 = nt * (kDown ? 2 * kTileRows : kTileRows);
     const int nk = p.nk;
 
     if (warp == kActWarp) {
@@ -292,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int mh = 0; mh < MH; ++mh)
                     tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act, kc * kChunkK,
-                                m0 + mh * kTileRows, bar);
+                                arow0 + mh * kTileRows, bar);
                 issued = kc + 1;
             }
             // the copies this thread issued land before the CTA may exit
@@ -315,22 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 const uint32_t bar = smem_addr(&ctl.w_full[s]);
-                const uint32_t slot = ringW + s * kRawSlotBytes;
-                mbar_arrive_expect_tx(bar, kRawSlotBytes);
+                const uint32_t slot = ringW + s * kRawSlot;
+                mbar_arrive_expect_tx(bar, kRawSlot);
                 if (!kDown) {
-                    const int row = p.wrow0 + n0;
+                    const int row = wrow0 + n0;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
-                        tma_load_2d(slot + b * (kTileRows * kRawK), &maps.body[b], kw * kRawK, row, bar);
-                        tma_load_2d(slot + b * (kTileRows * kRawK) + kTileRows * 64, &maps.body[b], kw * kRawK + 64,
-                                    row, bar);
-                        tma_load_2d(slot + kRawBodyBytes + b * (kTileRows * 16), &maps.sign[b], kw * (kRawK / 8), row,
-                                    bar);
+                        tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kw * kRawK, row, bar);
+                        tma_load_2d(slot + b * (kNR * kRawK) + kNR * 64, &bmap[b], kw * kRawK + 64, row, bar);
+                        tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kw * (kRawK / 8), row, bar);
                     }
                 } else {
-                    const int row = p.wrow0 + kw * kRawK;
-                    tma_load_2d(slot, &maps.body[0], n0, row, bar);
-                    tma_load_2d(slot + kRawBodyBytes, &maps.sign[0], n0 / 8, row, bar);
+                    const int row = wrow0 + kw * kRawK;
+                    tma_load_2d(slot, &bmap[0], n0, row, bar);
+                    tma_load_2d(slot + kRawBody, &smap[0], n0 / 8, row, bar);
                 }
                 issued = kw + 1;
             }
@@ -342,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA ---
         if (lane == 0) {
-            const uint32_t idesc = tc_idesc_f16(kTileRows, kTileRows) | (kDown ? (1u << 16) : 0u);
+            const uint32_t idesc = tc_idesc_f16(kTileRows, 2 * kNR) | (kDown ? (1u << 16) : 0u);
             for (int kc = 0; kc < nk; ++kc) {
                 const int sa = kc % C::kASlots, sb = kc % C::kBSlots;
                 if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kc / C::kASlots) & 1, p.timeout_ns, &ctl.abort) ||
@@ -352,20 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t sA = ringA + sa * C::kASlotBytes;
-                const uint32_t sB = ringB + sb * kBSlotBytes;
+                const uint32_t sB = ringB + sb * kBSlot;
 #pragma unroll
                 for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
+                    const uint64_t bd = kDown ? tc_desc_sw128_mn(sB + 2u * kMnGroupStride * k16, kMnAtomStride,
+                                                                 kMnGroupStride)
+                                              : tc_desc_sw128(sB + 32u * k16);
 #pragma unroll
                     for (int mh = 0; mh < MH; ++mh) {
                         const uint64_t ad = tc_desc_sw128(sA + mh * kTileBytes + 32u * k16);
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const uint64_t bd =
-                                kDown ? tc_desc_sw128_mn(sB + b * kTileBytes + 2u * kMnGroupStride * k16,
-                                                         kMnAtomStride, kMnGroupStride)
-                                      : tc_desc_sw128(sB + b * kTileBytes + 32u * k16);
-                            tc_mma_f16(tmem + (mh * 2 + b) * kTileRows, ad, bd, idesc, kc > 0 || k16 > 0);
-                        }
+                        tc_mma_f16(tmem + mh * 2 * kNR, ad, bd, idesc, kc > 0 || k16 > 0);
                     }
                 }
                 tc_commit(smem_addr(&ctl.a_empty[sa]));
@@ -388,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (ok && kc >= C::kBSlots)
                 ok = warp_wait(smem_addr(&ctl.b_empty[sb]), ((kc / C::kBSlots) + 1) & 1, p.timeout_ns, &ctl.abort);
             if (!ok) break;
-            decode_chunk<kDown>(t, ringW + sw * kRawSlotBytes, h, ringB + sb * kBSlotBytes);
+            decode_chunk<kDown>(t, ringW + sw * kRawSlot, h, ringB + sb * kBSlot);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -400,26 +440,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ----------------------------------------------------- epilogue ---
         if (warp_wait(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.abort)) {
             tc_fence_after();
+            // warp w reads TMEM lanes 32 (w mod 4) + [0, 32); the four warps
+            // of a lane quarter split the 32-column blocks: gate/up block
+            // w / 4 of both accumulators (warps past kNR / 32 blocks idle),
+            // down blocks (w / 4) (kNR / 64) + [0, kNR / 64) of the 2 kNR / 32
             const int lq = warp & 3, sel = warp >> 2;
             const uint32_t tl = tmem + ((static_cast<uint32_t>(lq) * 32u) << 16);
             bool bad = false;  // a stored h whose fp16 is not finite
 #pragma unroll
             for (int mh = 0; mh < MH; ++mh) {
-                const int64_t grow = static_cast<int64_t>(m0) + mh * kTileRows + lq * 32 + lane;
-                const bool valid = grow < p.m;
+                const int r = mh * kTileRows + lq * 32 + lane;
+                const int64_t grow = static_cast<int64_t>(arow0) + r;
+                const bool valid = r < nvalid;
                 if (!kDown) {
-                    __half* out = static_cast<__half*>(p.out) + grow * p.ldo + n0;
-#pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const int cb = 2 * sel + c2;
+                    if (sel < kNR / 32) {
+                        __half* out = static_cast<__half*>(p.out) + grow * p.ldo + n0;
+                        const int cb = sel;
                         float g[32], u[32];
-                        tc_ld32(tl + (mh * 2 + 0) * kTileRows + cb * 32, g);
-                        tc_ld32(tl + (mh * 2 + 1) * kTileRows + cb * 32, u);
+                        tc_ld32(tl + (mh * 2 + 0) * kNR + cb * 32, g);
+                        tc_ld32(tl + (mh * 2 + 1) * kNR + cb * 32, u);
                         uint32_t hw[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const __half2 h2 = __floats2half2_rn(silu(g[2 * i]) * u[2 * i],
-                                                                 silu(g[2 * i + 1]) * u[2 * i + 1]);
+                            const __half2 h2 =
+                                __floats2half2_rn(silu(g[2 * i]) * u[2 * i], silu(g[2 * i + 1]) * u[2 * i + 1]);
                             hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
                             bad = bad || (valid && !half2_finite(hw[i]));
                         }
@@ -431,13 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         }
                     }
                 } else {
-                    float* out = static_cast<float*>(p.out) + grow * p.ldo + n0 + sel * kTileRows;
 #pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
+                    for (int c2 = 0; c2 < kNR / 64; ++c2) {
+                        const int j = sel * (kNR / 64) + c2;
+                        const int b = j / (kNR / 32), cb = j % (kNR / 32);
+                        float* out = static_cast<float*>(p.out) + grow * p.ldo + n0 + b * kNR + cb * 32;
                         float v[32];
-                        tc_ld32(tl + (mh * 2 + sel) * kTileRows + cb * 32, v);
+                        tc_ld32(tl + (mh * 2 + b) * kNR + cb * 32, v);
                         if (valid) {
-                            float4* o = reinterpret_cast<float4*>(out + cb * 32);
+                            float4* o = reinterpret_cast<float4*>(out);
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -506,8 +552,8 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint
 
 // Token tiles of 128 * MH rows: MH = 2 halves the activation traffic per
 // flop; MH = 1 keeps more CTAs when the grid would not fill the GPU. Picks
-// the MH with fewer (waves x tile work), counting a 256-row tile as 1.8 of
-// a 128-row one.
+// the MH with fewer (waves x tile work), counting a 256-token tile as 1.8
+// of a 128-token one.
 int choose_mh(int64_t m, int64_t ntiles, int sms) {
     auto waves = [&](int mh) {
         const int64_t ctas = ntiles * ((m + kTileRows * mh - 1) / (kTileRows * mh));
@@ -516,9 +562,9 @@ int choose_mh(int64_t m, int64_t ntiles, int sms) {
     return waves(2) * 1.8 <= waves(1) ? 2 : 1;
 }
 
-template <bool kDown, int MH>
+template <bool kDown, int MH, bool kGrouped>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(prefill_kernel<kDown, MH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(prefill_kernel<kDown, MH, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg<MH>::kSmem);
 }
 
@@ -528,56 +574,79 @@ fp9_status ensure_attrs() {
     FP9_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
     if (!configured[dev]) {
-        if (device_max_smem_optin() < Cfg<1>::kSmem || device_max_smem_optin() < Cfg<2>::kSmem)
-            return FP9_ERR_CUDA;
-        FP9_CUDA_TRY((set_smem_attr<false, 1>()));
-        FP9_CUDA_TRY((set_smem_attr<false, 2>()));
-        FP9_CUDA_TRY((set_smem_attr<true, 1>()));
-        FP9_CUDA_TRY((set_smem_attr<true, 2>()));
+        const int optin = device_max_smem_optin();
+        if (optin < Cfg<1>::kSmem || optin < Cfg<2>::kSmem) return FP9_ERR_CUDA;
+        FP9_CUDA_TRY((set_smem_attr<false, 1, false>()));
+        FP9_CUDA_TRY((set_smem_attr<false, 2, false>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, false>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 2, false>()));
+        FP9_CUDA_TRY((set_smem_attr<false, 1, true>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, true>()));
         configured[dev] = true;
     }
     return FP9_OK;
 }
 
-// One GEMM launch: activations act [m, K] fp16; weight rows [wrow0, ...)
-// of planes with plane_rows rows of `hidden` columns (gate/up: body/sign
-// [0..1] = W_gate, W_up; down: body/sign[0] = down_t).
-fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const uint8_t* const body[2],
-                       const uint8_t* const sign[2], int64_t plane_rows, int64_t hidden, int64_t wrow0,
-                       int32_t ntiles, void* out, int64_t ldo, int32_t* status, int sms, cudaStream_t stream) {
-    PrefillMaps maps;
-    if (!make_map(&maps.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, static_cast<uint64_t>(K), static_cast<uint64_t>(m),
-                  static_cast<uint64_t>(K) * 2, kChunkK, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B))
-        return FP9_ERR_CUDA;
+// Tensor maps of one weight bank for a GEMM: gate/up read the bodies in
+// boxes of 64 K columns x 128 rows and the signs 128 K columns at a time;
+// down reads down_t in boxes of 256 output columns x 128 K rows.
+bool make_weight_maps(bool down, const uint8_t* const body[2], const uint8_t* const sign[2], int64_t plane_rows,
+                      int64_t hidden, CUtensorMap* bmaps, CUtensorMap* smaps) {
     for (int b = 0; b < (down ? 1 : 2); ++b) {
-        if (!make_map(&maps.body[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, body[b], static_cast<uint64_t>(hidden),
-                      static_cast<uint64_t>(plane_rows), static_cast<uint64_t>(hidden), down ? 2 * kTileRows : 64,
-                      kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !make_map(&maps.sign[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, sign[b], static_cast<uint64_t>(hidden / 8),
+        if (!make_map(&bmaps[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, body[b], static_cast<uint64_t>(hidden),
+                      static_cast<uint64_t>(plane_rows), static_cast<uint64_t>(hidden), down ? 2 * kNR : 64,
+                      down ? kRawK : kNR, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map(&smaps[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, sign[b], static_cast<uint64_t>(hidden / 8),
                       static_cast<uint64_t>(plane_rows), static_cast<uint64_t>(hidden / 8),
-                      down ? 2 * kTileRows / 8 : kRawK / 8, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return FP9_ERR_CUDA;
+                      down ? 2 * kNR / 8 : kRawK / 8, down ? kRawK : kNR, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
     }
     if (down) {
-        maps.body[1] = maps.body[0];
-        maps.sign[1] = maps.sign[0];
+        bmaps[1] = bmaps[0];
+        smaps[1] = smaps[0];
     }
+    return true;
+}
+
+bool make_act_map(CUtensorMap* map, const __half* act, int64_t rows, int64_t K) {
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
+                    static_cast<uint64_t>(K) * 2, kChunkK, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+PrefillArgs base_args(int64_t m, int64_t K, int32_t ntiles, void* out, int64_t ldo, int32_t* status) {
     PrefillArgs p{};
     p.m = static_cast<int32_t>(m);
     p.ntiles = ntiles;
     p.nk = static_cast<int32_t>(K / kChunkK);
-    p.wrow0 = static_cast<int32_t>(wrow0);
     p.out = out;
     p.ldo = ldo;
     p.status = status;
     p.timeout_ns = kTimeoutNs;
+    return p;
+}
+
+// One GEMM launch: activations act [m, K] fp16; weight rows [wrow0, ...)
+// of planes with plane_rows rows of `hidden` columns (gate/up: body/sign
+// [0..1] = W_gate, W_up, `ncols` = inter output columns; down:
+// body/sign[0] = down_t, `ncols` = hidden).
+fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const uint8_t* const body[2],
+                       const uint8_t* const sign[2], int64_t plane_rows, int64_t hidden, int64_t wrow0, int64_t ncols,
+                       void* out, int64_t ldo, int32_t* status, int sms, cudaStream_t stream) {
+    const int32_t ntiles = static_cast<int32_t>(ncols / (down ? 2 * kNR : kNR));
+    PrefillMaps maps;
+    if (!make_act_map(&maps.act, act, m, K) || !make_weight_maps(down, body, sign, plane_rows, hidden, maps.body, maps.sign))
+        return FP9_ERR_CUDA;
+    maps.body_sh[0] = maps.body_sh[1] = maps.body[0];
+    maps.sign_sh[0] = maps.sign_sh[1] = maps.sign[0];
+    PrefillArgs p = base_args(m, K, ntiles, out, ldo, status);
+    p.wrow0 = static_cast<int32_t>(wrow0);
     const int mh = choose_mh(m, ntiles, sms);
     p.mtiles = static_cast<int32_t>((m + kTileRows * mh - 1) / (kTileRows * mh));
     const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles;
     if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
     void (*k)(const PrefillMaps, const PrefillArgs) =
-        down ? (mh == 2 ? prefill_kernel<true, 2> : prefill_kernel<true, 1>)
-             : (mh == 2 ? prefill_kernel<false, 2> : prefill_kernel<false, 1>);
+        down ? (mh == 2 ? prefill_kernel<true, 2, false> : prefill_kernel<true, 1, false>)
+             : (mh == 2 ? prefill_kernel<false, 2, false> : prefill_kernel<false, 1, false>);
     const int smem = mh == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem;
     FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, maps, p));
     return FP9_OK;
@@ -604,6 +673,51 @@ fp9_status check_prefill_bank(const fp9_ffn_bank* f, int64_t index) {
 }
 
 }  // namespace
+
+fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* shared, const GroupTableDev& tab,
+                              int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows,
+                              int32_t* status, int sms, cudaStream_t stream) {
+    (void)sms;
+    const int64_t H = routed.hidden, I = routed.inter;
+    if (max_mtiles <= 0 || rows <= 0) return FP9_OK;
+    fp9_status st = ensure_attrs();
+    if (st != FP9_OK) return st;
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool down = pass == 1;
+        PrefillMaps maps;
+        const uint8_t* rb[2] = {down ? routed.down_body : routed.gate_body, down ? routed.down_body : routed.up_body};
+        const uint8_t* rs[2] = {down ? routed.down_sign : routed.gate_sign, down ? routed.down_sign : routed.up_sign};
+        if (!make_act_map(&maps.act, down ? h : x16, rows, down ? I : H) ||
+            !make_weight_maps(down, rb, rs, routed.n * I, H, maps.body, maps.sign))
+            return FP9_ERR_CUDA;
+        if (shared != nullptr && shared->n > 0) {
+            const uint8_t* sb[2] = {down ? shared->down_body : shared->gate_body,
+                                    down ? shared->down_body : shared->up_body};
+            const uint8_t* ss[2] = {down ? shared->down_sign : shared->gate_sign,
+                                    down ? shared->down_sign : shared->up_sign};
+            if (!make_weight_maps(down, sb, ss, shared->n * I, H, maps.body_sh, maps.sign_sh)) return FP9_ERR_CUDA;
+        } else {
+            maps.body_sh[0] = maps.body_sh[1] = maps.body[0];
+            maps.sign_sh[0] = maps.sign_sh[1] = maps.sign[0];
+        }
+        const int32_t ntiles = static_cast<int32_t>(down ? H / (2 * kNR) : I / kNR);
+        PrefillArgs p = base_args(rows, down ? I : H, ntiles, down ? static_cast<void*>(y) : static_cast<void*>(h),
+                                  down ? H : I, status);
+        p.g_row = tab.row;
+        p.g_cnt = tab.cnt;
+        p.g_mtile = tab.mtile;
+        p.n_groups = tab.n_groups;
+        p.n_routed = tab.n_routed;
+        p.inter = static_cast<int32_t>(I);
+        const int64_t ctas = max_mtiles * ntiles;
+        if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
+        void (*k)(const PrefillMaps, const PrefillArgs) =
+            down ? prefill_kernel<true, 1, true> : prefill_kernel<false, 1, true>;
+        FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), Cfg<1>::kSmem, stream, maps, p));
+    }
+    return FP9_OK;
+}
+
 }  // namespace fp9
 
 using namespace fp9;
@@ -642,11 +756,9 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
     const size_t wg = static_cast<size_t>(index) * static_cast<size_t>(I) * static_cast<size_t>(H);
     const uint8_t* gu_body[2] = {ffn->gate_body + wg, ffn->up_body + wg};
     const uint8_t* gu_sign[2] = {ffn->gate_sign + wg / 8, ffn->up_sign + wg / 8};
-    st = launch_gemm(false, x16, m, H, gu_body, gu_sign, I, H, 0, static_cast<int32_t>(I / kTileRows), h, I, d_status,
-                     sms, s);
+    st = launch_gemm(false, x16, m, H, gu_body, gu_sign, I, H, 0, I, h, I, d_status, sms, s);
     if (st != FP9_OK) return st;
     const uint8_t* d_body[2] = {ffn->down_body + wg, ffn->down_body + wg};
     const uint8_t* d_sign[2] = {ffn->down_sign + wg / 8, ffn->down_sign + wg / 8};
-    return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, static_cast<int32_t>(H / (2 * kTileRows)), y, H,
-                       d_status, sms, s);
+    return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, H, y, H, d_status, sms, s);
 }

@@ -122,3 +122,10 @@ class Workspace:
         if n == 0:
             raise binding.Fp9Error(binding.FP9_ERR_INVALID_ARG, "prefill_workspace_bytes")
         return cls(n, device)
+
+    @classmethod
+    def for_moe_prefill(cls, layer: MoELayer, m: int, device="cuda"):
+        n = binding.moe_prefill_workspace_bytes(layer, m)
+        if n == 0:
+            raise binding.Fp9Error(binding.FP9_ERR_INVALID_ARG, "moe_prefill_workspace_bytes")
+        return cls(n, device)

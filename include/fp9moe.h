@@ -242,6 +242,35 @@ fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t k, const float* x,
 size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m);
 
 /*
+ * fp9_moe_prefill: y = MoE(x) for m tokens at once (prompt prefill): the
+ * layer of fp9_moe_forward, with the expert FFNs on the tensor cores. The
+ * router is the decode step's (fp32 logits, then the same selection rules
+ * and weight formula); each token's slots are grouped by expert, every
+ * expert with tokens runs its FFN once over all of them as a GEMM (x and h
+ * rounded to fp16, fp32 accumulation: the arithmetic of fp9_ffn_prefill),
+ * and y[t] = sum_k w[t,k] FFN_{id[t,k]}(x[t]) + sum_s FFN_shared_s(x[t]) is
+ * added in slot, then shared-expert order (deterministic for a device).
+ *   layer  as for fp9_moe_forward, plus hidden % 256 == 0 and inter % 128
+ *          == 0 (FP9_ERR_SHAPE).
+ *   x, y   device fp32 [m, hidden], 16-byte aligned, y may not alias x;
+ *          0 <= m <= FP9_MAX_PREFILL_TOKENS (0 is a no-op).
+ *   ids, weights  optional device outputs [m, topk] (NULL to skip).
+ *   ws     device, >= fp9_moe_prefill_workspace_bytes(layer, m), 256-byte
+ *          aligned, zeroed once after allocation (its counter resets
+ *          itself). It holds the routing, and x, h and the per-expert
+ *          outputs of every (token, expert) pair: about
+ *          m * (topk + n_shared) * (6 * hidden + 2 * inter) bytes.
+ *   A token value or h whose fp16 is not finite is FP9_ERR_RANGE.
+ */
+fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x,
+                           int64_t m, float* y, int32_t* ids, float* weights,
+                           void* ws, size_t ws_bytes, int32_t* d_status,
+                           void* stream);
+
+/* Workspace bytes of fp9_moe_prefill for m tokens (0 if invalid). */
+size_t fp9_moe_prefill_workspace_bytes(const fp9_moe_layer* layer, int64_t m);
+
+/*
  * fp9_residual_rmsnorm: stack glue between layers, per token t:
  *   h[t] += y[t] (skipped when y is NULL);
  *   x_out[t] = h[t] / sqrt(mean(h[t]^2) + eps)   (unit gain).

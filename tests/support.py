@@ -162,3 +162,44 @@ def check_prefill(y, x, wg, wu, wd, y_exact=None):
     assert fro <= PREFILL_FRO, f"relative L2 error {fro:.3e} > {PREFILL_FRO}"
     assert row <= PREFILL_ROW, f"per-row relative L2 error {row:.3e} > {PREFILL_ROW}"
     return fro, row
+
+
+def decoded(planes):
+    """(W_gate, W_up, down_t) as float64 from an FFN's six packed planes."""
+    return tuple(O.fp9_decode(planes[2 * i], planes[2 * i + 1]) for i in range(3))
+
+
+def moe_prefill_bound(x, ol, ids, wts):
+    """Element-wise bound for fp9_moe_prefill: each expert term's
+    prefill_error_bound times |its routing weight| (1 for shared experts),
+    plus fp32 rounding of the weighted sum (one ulp of the summed
+    magnitudes per term)."""
+    x = np.asarray(x, np.float64)
+    m, topk = ids.shape
+    bound = np.zeros_like(x)
+    mag = np.zeros_like(x)
+    for e in np.unique(ids):
+        ts, ks = np.nonzero(ids == e)
+        wg, wu, wd = decoded(ol.planes(0, int(e)))
+        b = prefill_error_bound(x[ts], wg, wu, wd)
+        y = O.ffn(x[ts], wg, wu, wd)
+        w = np.abs(wts[ts, ks])[:, None]
+        np.add.at(bound, ts, w * b)
+        np.add.at(mag, ts, w * np.abs(y))
+    for s in range(ol.shape.n_shared):
+        wg, wu, wd = decoded(ol.planes(1, s))
+        bound += prefill_error_bound(x, wg, wu, wd)
+        mag += np.abs(O.ffn(x, wg, wu, wd))
+    return bound + (topk + ol.shape.n_shared) * 2.0 ** -23 * mag
+
+
+def check_moe_prefill(y, x, ol, ids, wts, y_exact):
+    """Asserts the prefill tolerance (element-wise bound, relative L2) for
+    an MoE layer's output y [m, H]."""
+    bound = moe_prefill_bound(x, ol, ids, wts)
+    over = np.abs(np.asarray(y, np.float64) - y_exact) - bound
+    assert over.max() <= 0.0, f"element-wise bound exceeded by {over.max():.3e}"
+    fro, row = prefill_errors(y, y_exact)
+    assert fro <= PREFILL_FRO, f"relative L2 error {fro:.3e} > {PREFILL_FRO}"
+    assert row <= PREFILL_ROW, f"per-row relative L2 error {row:.3e} > {PREFILL_ROW}"
+    return fro, row

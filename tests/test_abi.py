@@ -30,7 +30,7 @@ def test_header_declares_the_entry_points():
     for n in ["fp9_pack", "fp9_decode", "moe_router", "fp9_moe_forward", "fp9_dense_ffn",
               "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
               "fp9_selftest_timeout", "fp9_status_str", "fp9_from_fp8", "fp9_ffn_prefill",
-              "fp9_prefill_workspace_bytes"]:
+              "fp9_prefill_workspace_bytes", "fp9_moe_prefill", "fp9_moe_prefill_workspace_bytes"]:
         assert n in names, n
 
 
@@ -133,3 +133,22 @@ def test_prefill_argument_checks(lib):
     assert call(ws_bytes=need - 1) == binding.FP9_ERR_WORKSPACE
     assert lib.fp9_prefill_workspace_bytes(ctypes.byref(_bank(2, 128, 384)), 4) == 0
     assert lib.fp9_prefill_workspace_bytes(ctypes.byref(b), -1) == 0
+
+
+def test_moe_prefill_argument_checks(lib):
+    def call(layer, m=16, x=P, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 40):
+        return lib.fp9_moe_prefill(ctypes.byref(layer), x, m, y, None, None, ws, ws_bytes, None, None)
+
+    L = _layer()
+    need = lib.fp9_moe_prefill_workspace_bytes(ctypes.byref(L), 16)
+    assert need > 16 * 3 * (6 * 256 + 2 * 128)
+    assert lib.fp9_moe_prefill(None, P, 4, P, None, None, P, 1, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert call(_layer(hidden=384, routed=_bank(8, 128, 384), shared=_bank(1, 128, 384))) == binding.FP9_ERR_SHAPE
+    assert call(_layer(inter=64, routed=_bank(8, 64, 256), shared=_bank(1, 64, 256))) == binding.FP9_ERR_SHAPE
+    assert call(_layer(topk=17)) == binding.FP9_ERR_SHAPE
+    assert call(L, m=-1) == binding.FP9_ERR_INVALID_ARG
+    assert call(L, m=0, x=None, y=None, ws=None) == binding.FP9_OK
+    assert call(L, x=P + 4) == binding.FP9_ERR_ALIGN
+    assert call(L, ws=P + 16) == binding.FP9_ERR_ALIGN
+    assert call(L, ws_bytes=need - 1) == binding.FP9_ERR_WORKSPACE
+    assert lib.fp9_moe_prefill_workspace_bytes(ctypes.byref(_layer(topk=17)), 16) == 0
