@@ -395,6 +395,31 @@ def _side_runs(Ls, ws, status, dev, shape):
         gbs = units * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT / (ms / 1e3) / 1e9
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
                             "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
+    # the MoE layer over a whole prompt at once (fp9_moe_prefill): the pages'
+    # long prompt (1481 tokens) and a 4096-token one, on the resident layers
+    # in turn; every expert has tokens, so each call streams all 257 experts
+    for m in (1481, 4096):
+        x = synth.tokens(m, shape.hidden, synth.seed_for(3100, m, synth.TOKENS), dev)
+        y = torch.empty_like(x)
+        wp = Workspace.for_moe_prefill(Ls[0], m, dev)
+        for i in range(2):
+            binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status)
+        torch.cuda.synchronize()
+        K = 8
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(K):
+            binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / K
+        wbytes = (shape.n_experts + shape.n_shared) * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT
+        res[f"moe_prefill_m{m}"] = {"us_per_layer": round(ms * 1e3, 1), "tok_s": round(m / (ms / 1e3)),
+                                    "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1)}
+        del wp
+        torch.cuda.empty_cache()
+    if int(status.item()) != 0:
+        raise RuntimeError("side runs status: " + binding.status_str(int(status.item())))
     return res
 
 
