@@ -63,6 +63,7 @@ constexpr int kDecoderWarps = 16;
 constexpr int kDecoderThreads = kDecoderWarps * 32;
 constexpr int kActWarp = kDecoderWarps, kRawWarp = kDecoderWarps + 1, kMmaWarp = kDecoderWarps + 2;
 constexpr int kThreads = (kDecoderWarps + 3) * 32;
+constexpr int kGuThreads = (kDecoderWarps + 4) * 32;   // gate/up with weights in TMEM: two MMA warps
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kGroupM = 8;                            // M tiles per CTA-order group
@@ -501,6 +502,279 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == 0) tc_dealloc(tmem, C::kTmemCols);
 }
 
+// ---------------------------------------------- gate/up, weights in TMEM ---
+//
+// The gate/up GEMM with the roles of the operands swapped: the decoded
+// weights are the MMA's A operand in tensor memory (M = 128 weight rows, two
+// fp16 per 32-bit column, written by the decoder warps with tcgen05.st) and
+// the tokens are N (the activation tile in shared memory). The decoded
+// weights never go through shared memory, which otherwise carries ~5 bytes
+// of traffic per weight byte (raw in, raw out, fp16 in, fp16 out to the
+// tensor core) and bounds the kernel; and the MMA's N is the tile's valid
+// tokens rounded up to 16, so its work follows the tokens an FFN has.
+//
+// One CTA: 128 intermediate rows of W_gate and of W_up x up to 128 tokens.
+// TMEM (512 columns): D_gate [0, 128), D_up [128, 256) (lane = weight row,
+// column = token), then 4 slots of decoded weights of 64 K columns: gate in
+// the first 32 columns, up in the next 32.
+constexpr int kGuTokens = 128;
+constexpr int kGuActSlots = 4, kGuRawSlots = 4, kGuWSlots = 4;
+constexpr int kGuActSlot = kGuTokens * kChunkK * 2;  // 16 KiB
+constexpr int kGuSmem = 1024 + kCtlBytes + kGuActSlots * kGuActSlot + kGuRawSlots * kRawSlot;
+constexpr uint32_t kGuWCol0 = 256;
+static_assert(kGuSmem <= kSmemMax, "shared memory");
+
+// Decodes the 32 weights of K half `kh` of chunk half `h` of weight row
+// `row` of operand `b` in raw slot `raw` into 16 columns of half2 (low half
+// the even K). Raw bodies: [operand][row][128 B] with the 128-byte swizzle
+// (16-byte chunk j of row r at j ^ (r mod 8): the 8 rows a quarter warp
+// reads fall in 8 bank groups); signs [operand][row][16 B].
+__device__ __forceinline__ void decode_row32(uint32_t raw, uint32_t b, uint32_t row, uint32_t h, uint32_t kh,
+                                             uint32_t (&r)[16]) {
+    const uint32_t j0 = 4u * h + 2u * kh, x = row & 7u;
+    const uint32_t rb = raw + b * (kNR * kRawK) + row * kRawK;
+    uint4 v[2];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w)
+                 : "r"(rb + ((j0 ^ x) << 4))
+                 : "memory");
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[1].x), "=r"(v[1].y), "=r"(v[1].z), "=r"(v[1].w)
+                 : "r"(rb + (((j0 + 1u) ^ x) << 4))
+                 : "memory");
+    uint32_t s32;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(s32) : "r"(raw + kRawBody + b * (kNR * 16) + row * 16u + 8u * h + 4u * kh)
+                 : "memory");
+    const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) fp9_to_half4(w[i], spread_sign_nibble((s32 >> (4 * i)) & 0xFu), r[2 * i], r[2 * i + 1]);
+}
+
+template <bool kGrouped>
+__global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_constant__ PrefillMaps maps,
+                                                             const PrefillArgs p) {
+    int arow0, nvalid, n0, wrow0;
+    bool shared_bank = false;
+    if (kGrouped) {
+        grid_dependency_wait();  // the group table comes from the previous launches
+        const int total = p.g_mtile[p.n_groups] * p.ntiles;
+        if (static_cast<int>(blockIdx.x) >= total) return;  // the grid is an upper bound
+        const int q = blockIdx.x / p.ntiles, nt = blockIdx.x - q * p.ntiles;
+        int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.g_mtile + mid) <= q) lo = mid;
+            else hi = mid - 1;
+        }
+        const int mt = q - __ldg(p.g_mtile + lo);
+        arow0 = __ldg(p.g_row + lo) + mt * kGuTokens;
+        nvalid = __ldg(p.g_cnt + lo) - mt * kGuTokens;
+        shared_bank = lo >= p.n_routed;
+        wrow0 = (shared_bank ? lo - p.n_routed : lo) * p.inter;
+        n0 = nt * kNR;
+    } else {
+        int mt, nt;
+        tile_of(blockIdx.x, p.mtiles, p.ntiles, mt, nt);
+        arow0 = mt * kGuTokens;
+        nvalid = p.m - arow0;
+        wrow0 = p.wrow0;
+        n0 = nt * kNR;
+    }
+    // the MMA's N: the tile's valid tokens rounded up to 16
+    const uint32_t n_mma = static_cast<uint32_t>((min(nvalid, kGuTokens) + 15) / 16 * 16);
+    const CUtensorMap* bmap = shared_bank ? maps.body_sh : maps.body;
+    const CUtensorMap* smap = shared_bank ? maps.sign_sh : maps.sign;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw0 = smem_addr(smem_raw);
+    const uint32_t base = (raw0 + 1023u) & ~1023u;
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw + (base - raw0));
+    const uint32_t ringA = base + kCtlBytes;
+    const uint32_t ringW = ringA + kGuActSlots * kGuActSlot;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGuActSlots; ++s) {
+            mbar_init(smem_addr(&ctl.a_full[s]), 1);
+            mbar_init(smem_addr(&ctl.a_empty[s]), 2);
+        }
+        for (int s = 0; s < kGuRawSlots; ++s) {
+            mbar_init(smem_addr(&ctl.w_full[s]), 1);
+            mbar_init(smem_addr(&ctl.w_empty[s]), kDecoderWarps);
+        }
+        for (int s = 0; s < kGuWSlots; ++s) {  // decoded weights in TMEM
+            mbar_init(smem_addr(&ctl.b_full[s]), kDecoderWarps);
+            mbar_init(smem_addr(&ctl.b_empty[s]), 2);
+        }
+        mbar_init(smem_addr(&ctl.done), 2);
+        ctl.abort = 0;
+        ctl.never = 0;
+        fence_mbar_init();
+    }
+    if (warp == kActWarp && lane == 0) prefetch_map(&maps.act);
+    if (warp == kRawWarp && lane == 0) {
+        prefetch_map(&bmap[0]);
+        prefetch_map(&smap[0]);
+        prefetch_map(&bmap[1]);
+        prefetch_map(&smap[1]);
+    }
+    if (warp == 0) tc_alloc(smem_addr(&ctl.tmem), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    const int nk = p.nk;
+
+    if (warp == kActWarp) {
+        // -------------------------------------------- activation loads ---
+        if (lane == 0) {
+            grid_dependency_wait();  // the activations come from the previous launch
+            int issued = 0;
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kGuActSlots;
+                if (kc >= kGuActSlots &&
+                    !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((kc / kGuActSlots) + 1) & 1, p.timeout_ns,
+                                       &ctl.abort)) {
+                    fail(ctl, p.status);
+                    break;
+                }
+                const uint32_t bar = smem_addr(&ctl.a_full[s]);
+                mbar_arrive_expect_tx(bar, kGuActSlot);
+                tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * kChunkK, arow0, bar);
+                issued = kc + 1;
+            }
+            for (int j = issued > kGuActSlots ? issued - kGuActSlots : 0; j < issued; ++j)
+                (void)mbar_wait_bounded(smem_addr(&ctl.a_full[j % kGuActSlots]), (j / kGuActSlots) & 1, p.timeout_ns,
+                                        &ctl.never);
+        }
+        __syncwarp();
+    } else if (warp == kRawWarp) {
+        // ------------------------------------------------ weight loads ---
+        if (lane == 0) {
+            const int nw = nk / 2;
+            int issued = 0;
+            for (int kw = 0; kw < nw; ++kw) {
+                const int s = kw % kGuRawSlots;
+                if (kw >= kGuRawSlots &&
+                    !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / kGuRawSlots) + 1) & 1, p.timeout_ns,
+                                       &ctl.abort)) {
+                    fail(ctl, p.status);
+                    break;
+                }
+                const uint32_t bar = smem_addr(&ctl.w_full[s]);
+                const uint32_t slot = ringW + s * kRawSlot;
+                mbar_arrive_expect_tx(bar, kRawSlot);
+                const int row = wrow0 + n0;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kw * kRawK, row, bar);
+                    tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kw * (kRawK / 8), row, bar);
+                }
+                issued = kw + 1;
+            }
+            for (int j = issued > kGuRawSlots ? issued - kGuRawSlots : 0; j < issued; ++j)
+                (void)mbar_wait_bounded(smem_addr(&ctl.w_full[j % kGuRawSlots]), (j / kGuRawSlots) & 1, p.timeout_ns,
+                                        &ctl.never);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ---------------------------------------------------------- MMA ---
+        // warp kMmaWarp issues the gate MMAs, the next warp the up MMAs (one
+        // issuing thread is part of the per-instruction cost); each commits
+        // its own, so every slot and `done` take two arrivals
+        const uint32_t ob = static_cast<uint32_t>(warp - kMmaWarp);
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc_f16(kTileRows, n_mma);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int sa = kc % kGuActSlots, sw = kc % kGuWSlots;
+                if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kc / kGuActSlots) & 1, p.timeout_ns, &ctl.abort) ||
+                    !mbar_wait_bounded(smem_addr(&ctl.b_full[sw]), (kc / kGuWSlots) & 1, p.timeout_ns, &ctl.abort)) {
+                    fail(ctl, p.status);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sA = ringA + sa * kGuActSlot;
+                const uint32_t wcol = tmem + kGuWCol0 + sw * 64u;
+#pragma unroll
+                for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
+                    const uint64_t bd = tc_desc_sw128(sA + 32u * k16);
+                    tc_mma_f16_tmem_a(tmem + ob * kNR, wcol + ob * 32u + 8u * k16, bd, idesc, kc > 0 || k16 > 0);
+                }
+                tc_commit(smem_addr(&ctl.a_empty[sa]));
+                tc_commit(smem_addr(&ctl.b_empty[sw]));
+            }
+            tc_commit(smem_addr(&ctl.done));
+            if (!mbar_wait_bounded(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.never))
+                record_status(p.status, FP9_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------------------------------- decoders ---
+        // warp w writes TMEM lanes 32 (w mod 4) + [0, 32): weight row
+        // 32 (w mod 4) + lane of operand (w / 8) (0 gate, 1 up), K half
+        // (w / 4) mod 2 of each 64-wide chunk
+        const uint32_t q = warp & 3, sel = warp >> 2, b = sel >> 1, kh = sel & 1;
+        const uint32_t row = 32u * q + lane;
+        const uint32_t tlane = tmem + ((32u * q) << 16);
+        // Both 64-wide chunks of a raw slot per iteration: two TMEM stores,
+        // then one wait for their completion.
+        bool ok = true;
+        for (int kw = 0; kw < nk / 2 && ok; ++kw) {
+            const int sr = kw % kGuRawSlots;
+            const int kc0 = 2 * kw, sw0 = kc0 % kGuWSlots, sw1 = (kc0 + 1) % kGuWSlots;
+            ok = warp_wait(smem_addr(&ctl.w_full[sr]), (kw / kGuRawSlots) & 1, p.timeout_ns, &ctl.abort);
+            if (ok && kc0 >= kGuWSlots)
+                ok = warp_wait(smem_addr(&ctl.b_empty[sw0]), ((kc0 / kGuWSlots) + 1) & 1, p.timeout_ns, &ctl.abort);
+            if (ok && kc0 + 1 >= kGuWSlots)
+                ok = warp_wait(smem_addr(&ctl.b_empty[sw1]), (((kc0 + 1) / kGuWSlots) + 1) & 1, p.timeout_ns,
+                               &ctl.abort);
+            if (!ok) break;
+            const uint32_t raw = ringW + sr * kRawSlot;
+            uint32_t r[16];
+            decode_row32(raw, b, row, 0, kh, r);
+            tc_st16(tlane + kGuWCol0 + sw0 * 64u + b * 32u + kh * 16u, r);
+            decode_row32(raw, b, row, 1, kh, r);
+            tc_st16(tlane + kGuWCol0 + sw1 * 64u + b * 32u + kh * 16u, r);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_addr(&ctl.b_full[sw0]));
+                mbar_arrive(smem_addr(&ctl.b_full[sw1]));
+                mbar_arrive(smem_addr(&ctl.w_empty[sr]));
+            }
+        }
+        if (!ok && lane == 0) fail(ctl, p.status);
+        // ----------------------------------------------------- epilogue ---
+        // warp w: weight rows 32 (w mod 4) + [0, 32), tokens 32 (w / 4) +
+        // [0, 32); h[token, n0 + row] = SiLU(gate) * up, 32 lanes writing 32
+        // consecutive intermediate columns of a token row
+        if (warp_wait(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.abort)) {
+            tc_fence_after();
+            const int cb = static_cast<int>(sel);
+            float g[32], u[32];
+            tc_ld32(tlane + cb * 32, g);
+            tc_ld32(tlane + kNR + cb * 32, u);
+            __half* out = static_cast<__half*>(p.out) + n0 + row;
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = cb * 32 + j;
+                if (t < nvalid) {
+                    const __half hv = __float2half_rn(silu(g[j]) * u[j]);
+                    bad = bad || __hisinf(hv) || __hisnan(hv);
+                    out[(static_cast<int64_t>(arow0) + t) * p.ldo] = hv;
+                }
+            }
+            if (bad) record_status(p.status, FP9_ERR_RANGE);
+        }
+    }
+
+    grid_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, 512);
+}
+
 // x fp32 -> fp16 (round to nearest even); a value whose fp16 is not finite
 // is recorded as FP9_ERR_RANGE.
 __global__ void to_half_kernel(const float4* __restrict__ x, uint2* __restrict__ h, int64_t n4, int32_t* status) {
@@ -580,8 +854,8 @@ fp9_status ensure_attrs() {
         FP9_CUDA_TRY((set_smem_attr<false, 2, false>()));
         FP9_CUDA_TRY((set_smem_attr<true, 1, false>()));
         FP9_CUDA_TRY((set_smem_attr<true, 2, false>()));
-        FP9_CUDA_TRY((set_smem_attr<false, 1, true>()));
         FP9_CUDA_TRY((set_smem_attr<true, 1, true>()));
+        FP9_CUDA_TRY(cudaFuncSetAttribute(gateup_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGuSmem));
         configured[dev] = true;
     }
     return FP9_OK;
@@ -604,6 +878,23 @@ bool make_weight_maps(bool down, const uint8_t* const body[2], const uint8_t* co
     if (down) {
         bmaps[1] = bmaps[0];
         smaps[1] = smaps[0];
+    }
+    return true;
+}
+
+// Tensor maps of the W_gate and W_up planes for gate/up with weights in
+// TMEM: bodies in boxes of 128 K columns x 128 rows with the 128-byte
+// swizzle, signs in boxes of 16 bytes x 128 rows.
+bool make_gateup_maps(const uint8_t* const body[2], const uint8_t* const sign[2], int64_t plane_rows, int64_t hidden,
+                      CUtensorMap* bmaps, CUtensorMap* smaps) {
+    for (int b = 0; b < 2; ++b) {
+        if (!make_map(&bmaps[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, body[b], static_cast<uint64_t>(hidden),
+                      static_cast<uint64_t>(plane_rows), static_cast<uint64_t>(hidden), kRawK, kNR,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&smaps[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, sign[b], static_cast<uint64_t>(hidden / 8),
+                      static_cast<uint64_t>(plane_rows), static_cast<uint64_t>(hidden / 8), kRawK / 8, kNR,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
     }
     return true;
 }
@@ -687,15 +978,19 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         PrefillMaps maps;
         const uint8_t* rb[2] = {down ? routed.down_body : routed.gate_body, down ? routed.down_body : routed.up_body};
         const uint8_t* rs[2] = {down ? routed.down_sign : routed.gate_sign, down ? routed.down_sign : routed.up_sign};
+        auto maps_of = [&](const uint8_t* const bb[2], const uint8_t* const ss[2], int64_t rows_, CUtensorMap* bm,
+                           CUtensorMap* sm) {
+            return down ? make_weight_maps(true, bb, ss, rows_, H, bm, sm) : make_gateup_maps(bb, ss, rows_, H, bm, sm);
+        };
         if (!make_act_map(&maps.act, down ? h : x16, rows, down ? I : H) ||
-            !make_weight_maps(down, rb, rs, routed.n * I, H, maps.body, maps.sign))
+            !maps_of(rb, rs, routed.n * I, maps.body, maps.sign))
             return FP9_ERR_CUDA;
         if (shared != nullptr && shared->n > 0) {
             const uint8_t* sb[2] = {down ? shared->down_body : shared->gate_body,
                                     down ? shared->down_body : shared->up_body};
             const uint8_t* ss[2] = {down ? shared->down_sign : shared->gate_sign,
                                     down ? shared->down_sign : shared->up_sign};
-            if (!make_weight_maps(down, sb, ss, shared->n * I, H, maps.body_sh, maps.sign_sh)) return FP9_ERR_CUDA;
+            if (!maps_of(sb, ss, shared->n * I, maps.body_sh, maps.sign_sh)) return FP9_ERR_CUDA;
         } else {
             maps.body_sh[0] = maps.body_sh[1] = maps.body[0];
             maps.sign_sh[0] = maps.sign_sh[1] = maps.sign[0];
@@ -711,9 +1006,9 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         p.inter = static_cast<int32_t>(I);
         const int64_t ctas = max_mtiles * ntiles;
         if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
-        void (*k)(const PrefillMaps, const PrefillArgs) =
-            down ? prefill_kernel<true, 1, true> : prefill_kernel<false, 1, true>;
-        FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), Cfg<1>::kSmem, stream, maps, p));
+        void (*k)(const PrefillMaps, const PrefillArgs) = down ? prefill_kernel<true, 1, true> : gateup_kernel<true>;
+        FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(down ? kThreads : kGuThreads),
+                                down ? Cfg<1>::kSmem : kGuSmem, stream, maps, p));
     }
     return FP9_OK;
 }
