@@ -7,7 +7,7 @@
 // FFNs run as grouped GEMMs on the tensor cores (fp9_prefill.cu):
 //
 //   1. logits   [m, E] = x W_g^T in fp32 (a tiled FFMA GEMM, K split into
-//               up to 4 parts added in order by the selection);
+//               up to 8 parts added in order by the selection);
 //   2. select   one warp per token: sigmoid, group scores, top groups,
 //               top-k, weights (the decode router's rules and order);
 //   3. rank     one CTA per expert: the rank of each (token, slot) among
@@ -426,13 +426,14 @@ __global__ void __launch_bounds__(kRowThreads) moe_combine_kernel(const CombineA
 
 // -------------------------------------------------------------- host ---
 
-constexpr int kMaxLogitSplits = 4;
+constexpr int kMaxLogitSplits = 8;
 
-// K splits of the logits GEMM: enough CTAs for the GPU, at most 4.
+// K splits of the logits GEMM: about four CTAs per SM (eight warps each, so
+// that the shared-memory latency of the FFMA loop is hidden), at most 8.
 int logit_splits(int64_t m, int32_t E, int64_t H, int sms) {
     const int64_t tiles = ((m + kLogitTile - 1) / kLogitTile) * ((E + kLogitTile - 1) / kLogitTile);
     int s = 1;
-    while (s < kMaxLogitSplits && tiles * s < sms && (H / (2 * s)) % kLogitK == 0) s *= 2;
+    while (s < kMaxLogitSplits && tiles * s < 4 * static_cast<int64_t>(sms) && (H / (2 * s)) % kLogitK == 0) s *= 2;
     return s;
 }
 
