@@ -444,7 +444,9 @@ def _stack_run(dev, shape, n_layers=12, K=40):
         Ls.append(L)
     out = {"layers": n_layers, "resident_gb": round(n_layers * 3 * H * I * (shape.n_experts + shape.n_shared)
                                                     * FP9_BYTES_PER_WEIGHT / 1e9, 1)}
-    for bsz in (1, 2):
+    # bsz 2: an MTP pair (confirmed + draft token) in lockstep; bsz 5: a
+    # speculative verify block of 5 rows
+    for bsz in (1, 2, 5):
         h0 = synth.tokens(bsz, H, synth.seed_for(7100, bsz, synth.TOKENS), dev) * 2.0
         h = h0.clone()
         x = torch.empty_like(h)

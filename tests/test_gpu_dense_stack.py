@@ -58,8 +58,9 @@ def test_residual_rmsnorm_matches_oracle(bsz):
     assert support.max_rel_err(x2.cpu().numpy(), ref) <= 1e-5
 
 
-def test_stack_of_three_layers_matches_oracle():
-    shape, bsz = synth.TINY, 2
+@pytest.mark.parametrize("bsz", [2, 5])   # an MTP pair, and a 5-row verify block
+def test_stack_of_three_layers_matches_oracle(bsz):
+    shape = synth.TINY
     Ls = [support.build_layer(shape, base=50, layer=l) for l in range(3)]
     Os = [support.OracleLayer(shape, base=50, layer=l) for l in range(3)]
     h = support.safe_tokens(shape, Os[0].w_router, bsz, 51, device="cuda") * 2.0
