@@ -107,6 +107,8 @@ _SIGS = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_moe_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(MoELayerC), ctypes.c_int64]),
+    "fp9_prefill_selftest_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                                    ctypes.c_int32, ctypes.c_void_p]),
 }
 
 
@@ -278,3 +280,9 @@ def fp9_moe_prefill(layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
     _check(load().fp9_moe_prefill(ctypes.byref(layer.c_struct()), _ptr(x), x.shape[0], _ptr(y), _ptr(ids),
                                   _ptr(weights), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
                                   _stream(stream)), "fp9_moe_prefill")
+
+
+def fp9_prefill_selftest_timeout(ws: torch.Tensor, status: torch.Tensor, timeout_us: int = 2000,
+                                 stream=None) -> None:
+    _check(load().fp9_prefill_selftest_timeout(_ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                               timeout_us, _stream(stream)), "fp9_prefill_selftest_timeout")

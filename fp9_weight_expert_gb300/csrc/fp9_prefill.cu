@@ -129,6 +129,7 @@ struct PrefillArgs {
     int64_t ldo;             // row stride of out (elements)
     int32_t* status;
     uint64_t timeout_ns;
+    int32_t no_copy;         // failure self-test: the weight copies are not issued
     // grouped launches (GroupTableDev): token tile -> FFN and rows
     const int32_t* g_row;
     const int32_t* g_cnt;
@@ -364,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const uint32_t bar = smem_addr(&ctl.w_full[s]);
                 const uint32_t slot = ringW + s * kRawSlot;
                 mbar_arrive_expect_tx(bar, kRawSlot);
-                if (!kDown) {
+                if (p.no_copy) {
+                    // the bytes never arrive: every wait on this slot runs out
+                } else if (!kDown) {
                     const int row = wrow0 + n0;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
@@ -1056,4 +1059,36 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
     const uint8_t* d_body[2] = {ffn->down_body + wg, ffn->down_body + wg};
     const uint8_t* d_sign[2] = {ffn->down_sign + wg / 8, ffn->down_sign + wg / 8};
     return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, H, y, H, d_status, sms, s);
+}
+
+extern "C" fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status, int32_t timeout_us,
+                                                   void* stream) {
+    FP9_CHECK_ARG(ws != nullptr && d_status != nullptr, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(ws, 256), FP9_ERR_ALIGN);
+    FP9_CHECK_ARG(timeout_us >= 1 && timeout_us <= 1000000, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(ws_bytes >= (static_cast<size_t>(1) << 17), FP9_ERR_WORKSPACE);
+    fp9_status st = ensure_attrs();
+    if (st != FP9_OK) return st;
+    // one gate/up CTA: 128 tokens, hidden 256, inter 128; x (fp16) at the
+    // start of ws, h after it, and the weight maps over the last 32 KiB
+    // (never read: no weight copy is issued)
+    constexpr int64_t H = 256, I = 128, m = 128;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const __half* x16 = reinterpret_cast<const __half*>(w);
+    __half* h = reinterpret_cast<__half*>(w + 65536);
+    const uint8_t* planes[2] = {w + 98304, w + 98304};
+    PrefillMaps maps;
+    if (!make_act_map(&maps.act, x16, m, H) || !make_weight_maps(false, planes, planes, I, H, maps.body, maps.sign))
+        return FP9_ERR_CUDA;
+    for (int b = 0; b < 2; ++b) {
+        maps.body_sh[b] = maps.body[b];
+        maps.sign_sh[b] = maps.sign[b];
+    }
+    PrefillArgs p = base_args(m, H, 1, h, I, d_status);
+    p.mtiles = 1;
+    p.no_copy = 1;
+    p.timeout_ns = static_cast<uint64_t>(timeout_us) * 1000ull;
+    FP9_CUDA_TRY(launch_pdl(prefill_kernel<false, 1, false>, dim3(1), dim3(kThreads), Cfg<1>::kSmem,
+                            static_cast<cudaStream_t>(stream), maps, p));
+    return FP9_OK;
 }

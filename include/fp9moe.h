@@ -291,6 +291,20 @@ fp9_status fp9_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status,
                                 int32_t timeout_us, void* stream);
 
 /*
+ * fp9_prefill_selftest_timeout: failure-detection check of the prefill
+ * kernels' bounded waits. Launches one gate/up CTA of fp9_ffn_prefill (128
+ * tokens, hidden 256, inter 128) with its weight copies switched off, so
+ * every wait on the weights runs out after timeout_us microseconds; the
+ * kernel records FP9_ERR_TIMEOUT in *d_status, waits (bounded) for its own
+ * copies and MMAs, frees its tensor memory and returns with the context
+ * intact. ws: device, >= 128 KiB, 256-byte aligned (scratch); timeout_us in
+ * [1, 1000000].
+ */
+fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes,
+                                        int32_t* d_status, int32_t timeout_us,
+                                        void* stream);
+
+/*
  * fp9_moe_forward_noalloc: fp9_moe_forward for callers that cannot
  * allocate device memory (a runtime whose device memory is owned and
  * capped by another framework, a plugin handed only its input and output

@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     for n in ["fp9_pack", "fp9_decode", "moe_router", "fp9_moe_forward", "fp9_dense_ffn",
               "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
               "fp9_selftest_timeout", "fp9_status_str", "fp9_from_fp8", "fp9_ffn_prefill",
-              "fp9_prefill_workspace_bytes", "fp9_moe_prefill", "fp9_moe_prefill_workspace_bytes"]:
+              "fp9_prefill_workspace_bytes", "fp9_moe_prefill", "fp9_moe_prefill_workspace_bytes",
+              "fp9_prefill_selftest_timeout"]:
         assert n in names, n
 
 
@@ -105,6 +106,10 @@ def test_dense_and_norm_argument_checks(lib):
     assert lib.fp9_residual_rmsnorm(P, None, P, 0, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_INVALID_ARG
     assert lib.fp9_residual_rmsnorm(P + 4, None, P, 1, 8, ctypes.c_float(1e-6), None) == binding.FP9_ERR_ALIGN
     assert lib.fp9_selftest_timeout(P, 1 << 20, None, 100, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_prefill_selftest_timeout(P, 1 << 20, None, 100, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_prefill_selftest_timeout(P, 1 << 16, P, 100, None) == binding.FP9_ERR_WORKSPACE
+    assert lib.fp9_prefill_selftest_timeout(P + 16, 1 << 20, P, 100, None) == binding.FP9_ERR_ALIGN
+    assert lib.fp9_prefill_selftest_timeout(P, 1 << 20, P, 0, None) == binding.FP9_ERR_INVALID_ARG
 
 
 def test_prefill_argument_checks(lib):
