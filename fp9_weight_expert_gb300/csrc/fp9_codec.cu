@@ -113,54 +113,106 @@ __device__ __forceinline__ uint32_t encode_product(float x, float s, uint32_t& s
     return encode_body(bits, (dm > 0.0f) - (dm < 0.0f), range);
 }
 
+// fp8 checkpoint -> fp9 by 128x128 scale blocks. The pages say the
+// DeepSeek-V3 release is fp8 ("一鸭三吃" memoir, section "真正埋下伏笔的是内存；
+// R1 之后，问题第一次被改写") with 128x128 block scales (section "先用 Qwen3 练级，
+// 再让 Qwen3.5 充当高压试炼场"). Every weight of a block is its e4m3 value times
+// the block's scale s, rounded once to fp9 (encode_product), so the body
+// depends only on the code's magnitude: per block the CTA encodes the 128
+// magnitudes |e4m3(c)| * |s| into a table (128 bytes: one shared-memory
+// word per bank, so any 32 lookups take one wavefront), then each weight is
+// one lookup. Rounding to nearest is symmetric, so the product's sign is
+// the code's sign xor the scale's sign; a NaN product (a NaN code, 0 * Inf,
+// a NaN scale) is the canonical NaN of the multiply, sign 0.
+//
 template <int G>
-__device__ __forceinline__ void convert_group(const uint32_t (&in)[G / 4], float s, uint32_t (&out)[G / 4],
-                                              uint32_t& sb, bool& range) {
-    sb = 0;
+struct Fp8Block {
+    static constexpr int kUnits = 128 * 128 / G / 256;  // units of G weights per thread
+    uint32_t in[kUnits][G / 4];
+    int64_t g[kUnits];  // group index (-1: none)
+    float scale;
+};
+
+template <int G>
+__device__ __forceinline__ void fp8_block_load(const uint8_t* __restrict__ w8, const float* __restrict__ scale,
+                                               int64_t rows, int64_t cols, int64_t nbx, int64_t blk,
+                                               Fp8Block<G>& B) {
+    const int64_t by = blk / nbx, bx = blk - by * nbx;
+    const int64_t r0 = by * 128, c0 = bx * 128;
+    B.scale = __ldg(scale + blk);
+    const int64_t bh = rows - r0 < 128 ? rows - r0 : 128, bw = cols - c0 < 128 ? cols - c0 : 128;
+    const int per_row = static_cast<int>(bw / G);
+    const int units = static_cast<int>(bh) * per_row;
 #pragma unroll
-    for (int w = 0; w < G / 4; ++w) {
-        out[w] = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // bytes 4w + 2h, 4w + 2h + 1
-            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((in[w] >> (16 * h)) & 0xFFFFu);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            uint32_t s0, s1;
-            const uint32_t c0 = encode_product(x.x, s, s0, range);
-            const uint32_t c1 = encode_product(x.y, s, s1, range);
-            out[w] |= (c0 << (16 * h)) | (c1 << (16 * h + 8));
-            sb |= (s0 << (4 * w + 2 * h)) | (s1 << (4 * w + 2 * h + 1));
+    for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
+        const int u = threadIdx.x + 256 * j;
+        B.g[j] = -1;
+        if (u < units) {
+            // a full block has 128 / G units per row (a power of two)
+            constexpr int kShift = G == 16 ? 3 : 4;
+            const int rr = bw == 128 ? (u >> kShift) : u / per_row;
+            const int cu = u - rr * per_row;
+            B.g[j] = ((r0 + rr) * cols + c0) / G + cu;
+            if constexpr (G == 16) {
+                const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8) + B.g[j]);
+                B.in[j][0] = q.x, B.in[j][1] = q.y, B.in[j][2] = q.z, B.in[j][3] = q.w;
+            } else {
+                const uint2 q = __ldcs(reinterpret_cast<const uint2*>(w8) + B.g[j]);
+                B.in[j][0] = q.x, B.in[j][1] = q.y;
+            }
         }
     }
 }
 
-// fp8 checkpoint -> fp9: one thread per group of G (8 or 16) consecutive
-// weights of a row, all in one 128x128 scale block. The pages say the
-// DeepSeek-V3 release is fp8 ("一鸭三吃" memoir, section "真正埋下伏笔的是内存；
-// R1 之后，问题第一次被改写") with 128x128 block scales (section "先用 Qwen3 练级，
-// 再让 Qwen3.5 充当高压试炼场"). Each e4m3 byte becomes its exact fp16
-// (hardware conversion), then fp32; each weight is that value times the
-// block's scale, rounded once to fp9 (encode_product).
+// Encodes the block's table (threads 0..127) and converts the block's units
+// of this thread; returns whether any weight landed on an Inf or NaN body.
 template <int G>
-__global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restrict__ w8,
-                                                         const float* __restrict__ scale, uint32_t ngroups,
-                                                         uint32_t groups_per_row, uint32_t scale_cols,
-                                                         uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
-                                                         int32_t* status) {
-    constexpr int kWords = G / 4;
+__device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t* tab, uint8_t* __restrict__ body,
+                                                  uint8_t* __restrict__ sign) {
     bool range = false;
-    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += gridDim.x * blockDim.x) {
-        const uint32_t row = g / groups_per_row, gc = g - row * groups_per_row;
-        const float sc = __ldg(scale + (row / 128u) * scale_cols + (gc * G) / 128u);
-        uint32_t in[kWords], out[kWords], sb;
-        if constexpr (G == 16) {
-            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8) + g);
-            in[0] = q.x, in[1] = q.y, in[2] = q.z, in[3] = q.w;
-        } else {
-            const uint2 q = __ldcs(reinterpret_cast<const uint2*>(w8) + g);
-            in[0] = q.x, in[1] = q.y;
+    __syncthreads();  // the previous block's lookups are done
+    if (threadIdx.x < 128) {
+        // |e4m3(c)| for c < 128: the hardware conversion of the code pair
+        // (c, c) to fp16, then fp32
+        const __half2_raw hr =
+            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(threadIdx.x * 0x101u), __NV_E4M3);
+        const float x = __low2float(*reinterpret_cast<const __half2*>(&hr));
+        uint32_t sb;
+        tab[threadIdx.x] = static_cast<uint8_t>(encode_product(x, fabsf(B.scale), sb, range));
+    }
+    // a block whose table holds an Inf or NaN body checks its weights
+    const int special = __syncthreads_or(range ? 1 : 0);
+    // all-ones over the unit's sign bits when the scale is negative
+    const uint32_t sflip = (__float_as_uint(B.scale) >> 31) ? (1u << G) - 1u : 0u;
+    bool hit = false;
+#pragma unroll
+    for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
+        if (B.g[j] < 0) continue;
+        const int64_t g = B.g[j];
+        uint32_t out[G / 4], sb = 0;
+#pragma unroll
+        for (int w = 0; w < G / 4; ++w) {
+            const uint32_t v = B.in[j][w];
+            const uint32_t m = v & 0x7F7F7F7Fu;  // the 4 code magnitudes
+            const uint32_t b0 = tab[m & 0xFFu], b1 = tab[__byte_perm(m, 0u, 0x4441u)];
+            const uint32_t b2 = tab[__byte_perm(m, 0u, 0x4442u)], b3 = tab[m >> 24];
+            out[w] = __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
+            // the 4 code signs (bit 7 of each byte) land in bits 28..31
+            sb |= (((v & 0x80808080u) * 0x00204081u) >> 28) << (4 * w);
         }
-        convert_group<G>(in, sc, out, sb, range);
+        sb ^= sflip;
+        if (special) {
+            // bytes 0xF8..0xFF (Inf 0xF8, NaN 0xFC): flag them; NaN is unsigned
+#pragma unroll
+            for (int w = 0; w < G / 4; ++w) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t bk = (out[w] >> (8 * k)) & 0xFFu;
+                    if ((bk & 0xF8u) == 0xF8u) hit = true;
+                    if (bk == 0xFCu) sb &= ~(1u << (4 * w + k));
+                }
+            }
+        }
         if constexpr (G == 16) {
             __stcs(reinterpret_cast<uint4*>(body) + g, make_uint4(out[0], out[1], out[2], out[3]));
             reinterpret_cast<uint16_t*>(sign)[g] = static_cast<uint16_t>(sb);
@@ -169,7 +221,21 @@ __global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restri
             sign[g] = static_cast<uint8_t>(sb);
         }
     }
-    if (range) record_status(status, FP9_ERR_RANGE);
+    return hit;
+}
+
+template <int G>
+__global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restrict__ w8,
+                                                         const float* __restrict__ scale, int64_t rows,
+                                                         int64_t cols, int64_t nbx, int64_t nblocks,
+                                                         uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
+                                                         int32_t* status) {
+    __shared__ uint8_t tab[128];
+    // one block per CTA; the block's codes are loaded first, so they are in
+    // flight while its table is built
+    Fp8Block<G> A;
+    fp8_block_load<G>(w8, scale, rows, cols, nbx, blockIdx.x, A);
+    if (fp8_block_convert<G>(A, tab, body, sign)) record_status(status, FP9_ERR_RANGE);
 }
 
 __global__ void __launch_bounds__(256) decode_kernel(const uint2* __restrict__ body,
@@ -233,18 +299,17 @@ extern "C" fp9_status fp9_from_fp8(const uint8_t* w8, const float* scale_inv, in
     FP9_CHECK_ARG(w8 != nullptr && scale_inv != nullptr && body != nullptr && sign != nullptr,
                   FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(w8, 8) && aligned(body, 8) && aligned(scale_inv, 4), FP9_ERR_ALIGN);
-    FP9_CHECK_ARG(rows * (cols / 8) <= 0xFFFFFFFFll, FP9_ERR_SHAPE);  // 32-bit group index
     const bool wide = cols % 16 == 0 && aligned(w8, 16) && aligned(body, 16) && aligned(sign, 2);
-    const int G = wide ? 16 : 8;
-    const int64_t gpr = cols / G, ngroups = rows * gpr;
-    const uint32_t scols = static_cast<uint32_t>((cols + 127) / 128);
+    const int64_t nbx = (cols + 127) / 128, nblocks = ((rows + 127) / 128) * nbx;
+    FP9_CHECK_ARG(nblocks <= 0x7FFFFFFF, FP9_ERR_SHAPE);  // one CTA per scale block
+    const int64_t ctas = nblocks;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (wide)
-        fp8_to_fp9_kernel<16><<<elementwise_grid(ngroups), 256, 0, st>>>(
-            w8, scale_inv, static_cast<uint32_t>(ngroups), static_cast<uint32_t>(gpr), scols, body, sign, d_status);
+        fp8_to_fp9_kernel<16><<<static_cast<unsigned>(ctas), 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nblocks,
+                                                                           body, sign, d_status);
     else
-        fp8_to_fp9_kernel<8><<<elementwise_grid(ngroups), 256, 0, st>>>(
-            w8, scale_inv, static_cast<uint32_t>(ngroups), static_cast<uint32_t>(gpr), scols, body, sign, d_status);
+        fp8_to_fp9_kernel<8><<<static_cast<unsigned>(ctas), 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nblocks,
+                                                                          body, sign, d_status);
     FP9_CUDA_TRY(cudaGetLastError());
     return FP9_OK;
 }
