@@ -7,6 +7,7 @@ turn, so every step streams its 446 MB of fp9 expert weights from HBM
 than the 129 MB L2).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+  python bench.py --leg fp8_to_fp9|prefill|moe_prefill   (one side measurement alone)
 
 Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on
 the host cores instead (one token through one expert FFN per step, scaled
@@ -44,6 +45,10 @@ def _args():
                    help="routed experts per layer (smaller layers for profiling captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the bsz-2 / dense side runs")
+    p.add_argument("--leg", choices=["fp8_to_fp9", "prefill", "moe_prefill"], default=None,
+                   help="run one side measurement alone and print its record (profiling captures)")
+    p.add_argument("--tokens", type=int, nargs="+", default=[1481, 4096],
+                   help="prompt lengths of the moe_prefill leg")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -197,6 +202,10 @@ def _native(args):
         shape = dataclasses.replace(shape, n_experts=args.experts)
     H, I, bsz = shape.hidden, shape.inter, args.bsz
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.leg == "fp8_to_fp9":
+        return {"leg": args.leg, **_convert_run(dev, _peaks()[0])}
+    if args.leg == "prefill":
+        return {"leg": args.leg, **_prefill_run(dev, _tensor_peak())}
 
     def make_layer(l):
         L = layers.MoELayer(H, I, shape.n_experts, shape.n_groups, shape.topk_groups, shape.topk,
@@ -213,6 +222,9 @@ def _native(args):
     if int(status.item()) != 0:
         raise RuntimeError("packing failed: " + binding.status_str(int(status.item())))
     setup_s = time.time() - t0
+    if args.leg == "moe_prefill":
+        return {"leg": args.leg, "experts": shape.n_experts,
+                **_moe_prefill_run(Ls, status, dev, shape, args.tokens)}
 
     n_tok = 64
     xs = synth.tokens(n_tok * bsz, H, synth.seed_for(2000 + rank, 0, synth.TOKENS), dev).view(n_tok, bsz, H)
@@ -395,10 +407,22 @@ def _side_runs(Ls, ws, status, dev, shape):
         gbs = units * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT / (ms / 1e3) / 1e9
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
                             "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
-    # the MoE layer over a whole prompt at once (fp9_moe_prefill): the pages'
-    # long prompt (1481 tokens) and a 4096-token one, on the resident layers
-    # in turn; every expert has tokens, so each call streams all 257 experts
-    for m in (1481, 4096):
+    res.update(_moe_prefill_run(Ls, status, dev, shape, (1481, 4096)))
+    if int(status.item()) != 0:
+        raise RuntimeError("side runs status: " + binding.status_str(int(status.item())))
+    return res
+
+
+def _moe_prefill_run(Ls, status, dev, shape, lengths):
+    """The MoE layer over a whole prompt at once (fp9_moe_prefill) for each
+    prompt length, on the resident layers in turn; with the pages' long
+    prompt (1481 tokens) every expert has tokens, so each call streams all
+    routed and shared experts."""
+    import torch
+
+    from fp9_weight_expert_gb300 import Workspace, binding, synth
+    res = {}
+    for m in lengths:
         x = synth.tokens(m, shape.hidden, synth.seed_for(3100, m, synth.TOKENS), dev)
         y = torch.empty_like(x)
         wp = Workspace.for_moe_prefill(Ls[0], m, dev)
@@ -419,7 +443,7 @@ def _side_runs(Ls, ws, status, dev, shape):
         del wp
         torch.cuda.empty_cache()
     if int(status.item()) != 0:
-        raise RuntimeError("side runs status: " + binding.status_str(int(status.item())))
+        raise RuntimeError("moe prefill status: " + binding.status_str(int(status.item())))
     return res
 
 

@@ -119,49 +119,72 @@ __device__ __forceinline__ uint32_t encode_product(float x, float s, uint32_t& s
 // 再让 Qwen3.5 充当高压试炼场"). Every weight of a block is its e4m3 value times
 // the block's scale s, rounded once to fp9 (encode_product), so the body
 // depends only on the code's magnitude: per block the CTA encodes the 128
-// magnitudes |e4m3(c)| * |s| into a table (128 bytes: one shared-memory
-// word per bank, so any 32 lookups take one wavefront), then each weight is
-// one lookup. Rounding to nearest is symmetric, so the product's sign is
-// the code's sign xor the scale's sign; a NaN product (a NaN code, 0 * Inf,
-// a NaN scale) is the canonical NaN of the multiply, sign 0.
+// magnitudes |e4m3(c)| * |s| into a table indexed by the whole code byte
+// (256 bytes, each body stored for both signs, so no mask is needed before
+// a lookup), then each weight is one shared-memory byte read. Rounding to
+// nearest is symmetric, so the product's sign is the code's sign xor the
+// scale's sign; a NaN product (a NaN code, 0 * Inf, a NaN scale) is the
+// canonical NaN of the multiply, sign 0.
 //
+// Grid: x = block column, y = block row (a CTA walks the block rows
+// blockIdx.y, + gridDim.y, ... so any row count fits the 65535 limit).
+// 256 threads; a thread converts kUnits units of G consecutive weights of
+// a row (G = 16, or 8 when cols % 16 != 0).
 template <int G>
 struct Fp8Block {
     static constexpr int kUnits = 128 * 128 / G / 256;  // units of G weights per thread
     uint32_t in[kUnits][G / 4];
-    int64_t g[kUnits];  // group index (-1: none)
+    int64_t g[kUnits];  // unit index in the matrix (-1: none)
     float scale;
 };
 
 template <int G>
 __device__ __forceinline__ void fp8_block_load(const uint8_t* __restrict__ w8, const float* __restrict__ scale,
-                                               int64_t rows, int64_t cols, int64_t nbx, int64_t blk,
+                                               int64_t rows, int64_t cols, int64_t nbx, int64_t by,
                                                Fp8Block<G>& B) {
-    const int64_t by = blk / nbx, bx = blk - by * nbx;
+    const int64_t bx = blockIdx.x;
     const int64_t r0 = by * 128, c0 = bx * 128;
-    B.scale = __ldg(scale + blk);
+    B.scale = __ldg(scale + by * nbx + bx);
     const int64_t bh = rows - r0 < 128 ? rows - r0 : 128, bw = cols - c0 < 128 ? cols - c0 : 128;
-    const int per_row = static_cast<int>(bw / G);
-    const int units = static_cast<int>(bh) * per_row;
+    if (bh == 128 && bw == 128) {
+        // a full block: 128 / G units per row, so unit threadIdx.x + 256 j
+        // sits 256 G / 128 = 2 G rows below unit threadIdx.x (2 cols units)
+        constexpr int kShift = G == 16 ? 3 : 4;
+        const int64_t g0 =
+            ((r0 + (threadIdx.x >> kShift)) * cols + c0) / G + (threadIdx.x & ((1 << kShift) - 1));
 #pragma unroll
-    for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
-        const int u = threadIdx.x + 256 * j;
-        B.g[j] = -1;
-        if (u < units) {
-            // a full block has 128 / G units per row (a power of two)
-            constexpr int kShift = G == 16 ? 3 : 4;
-            const int rr = bw == 128 ? (u >> kShift) : u / per_row;
-            const int cu = u - rr * per_row;
-            B.g[j] = ((r0 + rr) * cols + c0) / G + cu;
-            if constexpr (G == 16) {
-                const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8) + B.g[j]);
-                B.in[j][0] = q.x, B.in[j][1] = q.y, B.in[j][2] = q.z, B.in[j][3] = q.w;
-            } else {
-                const uint2 q = __ldcs(reinterpret_cast<const uint2*>(w8) + B.g[j]);
-                B.in[j][0] = q.x, B.in[j][1] = q.y;
-            }
+        for (int j = 0; j < Fp8Block<G>::kUnits; ++j) B.g[j] = g0 + 2 * j * cols;
+    } else {
+        const int per_row = static_cast<int>(bw / G);
+        const int units = static_cast<int>(bh) * per_row;
+#pragma unroll
+        for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
+            const int u = threadIdx.x + 256 * j;
+            const int rr = u / per_row;
+            B.g[j] = u < units ? ((r0 + rr) * cols + c0) / G + (u - rr * per_row) : -1;
         }
     }
+#pragma unroll
+    for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
+        if (B.g[j] < 0) continue;
+        if constexpr (G == 16) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8) + B.g[j]);
+            B.in[j][0] = q.x, B.in[j][1] = q.y, B.in[j][2] = q.z, B.in[j][3] = q.w;
+        } else {
+            const uint2 q = __ldcs(reinterpret_cast<const uint2*>(w8) + B.g[j]);
+            B.in[j][0] = q.x, B.in[j][1] = q.y;
+        }
+    }
+}
+
+// The sign bits (bit 7 of each byte) of two code words v0, v1 as 8 bits:
+// byte k of v0 at bit 24 + k, byte k of v1 at bit 28 + k. v0's signs are
+// moved down to bits 8k + 3, beside v1's at 8k + 7; the multiply by
+// 2^0 + 2^7 + 2^14 + 2^21 adds the copy shifted by 7 (3 - k), which takes
+// 8k + 3 to 24 + k and 8k + 7 to 28 + k. All 32 shifted copies of the 8
+// bits fall on distinct positions, so no carry disturbs them.
+__device__ __forceinline__ uint32_t gather_signs8(uint32_t v0, uint32_t v1) {
+    return ((v1 & 0x80808080u) | ((v0 >> 4) & 0x08080808u)) * 0x00204081u;
 }
 
 // Encodes the block's table (threads 0..127) and converts the block's units
@@ -178,7 +201,9 @@ __device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t*
             __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(threadIdx.x * 0x101u), __NV_E4M3);
         const float x = __low2float(*reinterpret_cast<const __half2*>(&hr));
         uint32_t sb;
-        tab[threadIdx.x] = static_cast<uint8_t>(encode_product(x, fabsf(B.scale), sb, range));
+        const uint8_t e = static_cast<uint8_t>(encode_product(x, fabsf(B.scale), sb, range));
+        tab[threadIdx.x] = e;
+        tab[threadIdx.x + 128] = e;
     }
     // a block whose table holds an Inf or NaN body checks its weights
     const int special = __syncthreads_or(range ? 1 : 0);
@@ -189,17 +214,21 @@ __device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t*
     for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
         if (B.g[j] < 0) continue;
         const int64_t g = B.g[j];
-        uint32_t out[G / 4], sb = 0;
+        uint32_t out[G / 4];
 #pragma unroll
         for (int w = 0; w < G / 4; ++w) {
             const uint32_t v = B.in[j][w];
-            const uint32_t m = v & 0x7F7F7F7Fu;  // the 4 code magnitudes
-            const uint32_t b0 = tab[m & 0xFFu], b1 = tab[__byte_perm(m, 0u, 0x4441u)];
-            const uint32_t b2 = tab[__byte_perm(m, 0u, 0x4442u)], b3 = tab[m >> 24];
-            out[w] = __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
-            // the 4 code signs (bit 7 of each byte) land in bits 28..31
-            sb |= (((v & 0x80808080u) * 0x00204081u) >> 28) << (4 * w);
+            const uint32_t b0 = tab[v & 0xFFu], b1 = tab[__byte_perm(v, 0u, 0x4441u)];
+            const uint32_t b2 = tab[__byte_perm(v, 0u, 0x4442u)], b3 = tab[__umulhi(v, 256u)];
+            // the bytes do not overlap, so the adds are ors; written as
+            // multiply-adds they can share the integer multiply pipe
+            out[w] = (b3 * 256u + b2) * 65536u + (b1 * 256u + b0);
         }
+        uint32_t sb;
+        if constexpr (G == 16)
+            sb = __byte_perm(gather_signs8(B.in[j][0], B.in[j][1]), gather_signs8(B.in[j][2], B.in[j][3]), 0x0073u);
+        else
+            sb = gather_signs8(B.in[j][0], B.in[j][1]) >> 24;
         sb ^= sflip;
         if (special) {
             // bytes 0xF8..0xFF (Inf 0xF8, NaN 0xFC): flag them; NaN is unsigned
@@ -227,15 +256,19 @@ __device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t*
 template <int G>
 __global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restrict__ w8,
                                                          const float* __restrict__ scale, int64_t rows,
-                                                         int64_t cols, int64_t nbx, int64_t nblocks,
+                                                         int64_t cols, int64_t nbx, int64_t nby,
                                                          uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
                                                          int32_t* status) {
-    __shared__ uint8_t tab[128];
-    // one block per CTA; the block's codes are loaded first, so they are in
-    // flight while its table is built
-    Fp8Block<G> A;
-    fp8_block_load<G>(w8, scale, rows, cols, nbx, blockIdx.x, A);
-    if (fp8_block_convert<G>(A, tab, body, sign)) record_status(status, FP9_ERR_RANGE);
+    __shared__ uint8_t tab[256];
+    bool hit = false;
+    // a block's codes are loaded before its table is built, so they are in
+    // flight meanwhile
+    for (int64_t by = blockIdx.y; by < nby; by += gridDim.y) {
+        Fp8Block<G> A;
+        fp8_block_load<G>(w8, scale, rows, cols, nbx, by, A);
+        hit |= fp8_block_convert<G>(A, tab, body, sign);
+    }
+    if (hit) record_status(status, FP9_ERR_RANGE);
 }
 
 __global__ void __launch_bounds__(256) decode_kernel(const uint2* __restrict__ body,
@@ -300,16 +333,14 @@ extern "C" fp9_status fp9_from_fp8(const uint8_t* w8, const float* scale_inv, in
                   FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(w8, 8) && aligned(body, 8) && aligned(scale_inv, 4), FP9_ERR_ALIGN);
     const bool wide = cols % 16 == 0 && aligned(w8, 16) && aligned(body, 16) && aligned(sign, 2);
-    const int64_t nbx = (cols + 127) / 128, nblocks = ((rows + 127) / 128) * nbx;
-    FP9_CHECK_ARG(nblocks <= 0x7FFFFFFF, FP9_ERR_SHAPE);  // one CTA per scale block
-    const int64_t ctas = nblocks;
+    const int64_t nbx = (cols + 127) / 128, nby = (rows + 127) / 128;
+    FP9_CHECK_ARG(nbx <= 0x7FFFFFFF, FP9_ERR_SHAPE);  // one grid column per block column
+    const dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(nby < 65535 ? nby : 65535));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (wide)
-        fp8_to_fp9_kernel<16><<<static_cast<unsigned>(ctas), 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nblocks,
-                                                                           body, sign, d_status);
+        fp8_to_fp9_kernel<16><<<grid, 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nby, body, sign, d_status);
     else
-        fp8_to_fp9_kernel<8><<<static_cast<unsigned>(ctas), 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nblocks,
-                                                                          body, sign, d_status);
+        fp8_to_fp9_kernel<8><<<grid, 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nby, body, sign, d_status);
     FP9_CUDA_TRY(cudaGetLastError());
     return FP9_OK;
 }

@@ -93,3 +93,22 @@ def test_full_dsv3_expert_matrix():
     # checkpoint-like scales: weight magnitudes around 1e-2 after scaling
     scale = (np.exp2(rng.uniform(-14, -10, size=(rows // 128, cols // 128)))).astype(np.float32)
     _check(w8, scale)
+
+
+@pytest.mark.parametrize("cols", [8, 16])
+def test_more_block_rows_than_one_grid_pass(cols):
+    # 65539 block rows: the grid holds 65535 of them, so the CTAs of the
+    # first 4 block rows also convert the last 4 (the last one ragged)
+    rows = 65538 * 128 + 40
+    rng = np.random.default_rng(cols)
+    w8 = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3C
+    scale = (np.exp2(rng.uniform(-14, 6, size=(-(-rows // 128), 1))) *
+             rng.choice([1, -1], size=(-(-rows // 128), 1))).astype(np.float32)
+    b, s, st = _gpu(w8, scale)
+    assert st == 0
+    for r0, r1 in ((0, 4 * 128), (65534 * 128, rows)):
+        rb, rs, rerr = O.fp8_block_to_fp9(w8[r0:r1], scale[r0 // 128:-(-r1 // 128)])
+        assert not rerr
+        assert np.array_equal(b[r0:r1], rb)
+        assert np.array_equal(s[r0:r1], rs)
