@@ -20,15 +20,18 @@
 // R = NW / 2 rows as three stages, one per ring slot: slot 0 the gate rows,
 // slot 1 the up rows, slot 2 the down rows (bodies, then signs; bulk copies
 // completing on mbarriers).
-//   gate/up: the 2R rows of a chunk are dealt to the warps, one row each; a
-//     warp computes its row against x (staged in shared memory), so the
-//     only reduction is a 5-step warp sum; lane 0 publishes the sum.
+//   gate/up: the R rows of the gate stage are cut into 2R half rows, one
+//     per warp; a warp computes its half row against x (staged in shared
+//     memory), so the only reduction is a 5-step warp sum; lane 0
+//     publishes the sum. Then the same for the up stage.
 //   down: each thread owns 16 consecutive hidden columns and keeps y for
 //     them in registers: an axpy with no reduction.
-// Per chunk c a warp does its gate/up rows, arrives at c's publish barrier,
+// Per chunk c a warp does its gate half row (and releases the gate slot),
+// its up half row (releases the up slot), arrives at c's publish barrier,
 // processes the down rows of chunk c - 1 (whose h is known), then waits for
-// c's barrier and forms h = SiLU(g) * u * w_route. The producer streams
-// gate c, up c, then down c - 1.
+// c's barrier and forms h = SiLU(g) * u * w_route from the halves' sums.
+// The producer streams gate c, up c, then down c - 1: the order in which
+// the slots free up, so every refill has two phases of the chunk to land.
 //
 // Every wait is bounded (a timeout sets FP9_ERR_TIMEOUT in the status word
 // and the CTA drains its copies in flight and returns).
@@ -86,7 +89,7 @@ struct SmemCtl {
     uint64_t xbar;           // a job's x staged in shared memory
     int abort;
     int never;               // stays 0: a flag nobody raises
-    float gu[2][2][kMaxRows][kTokensPerJob];  // [chunk parity][gate, up][row][token]
+    float gu[2][2][kMaxRows][2][kTokensPerJob];  // [chunk parity][gate, up][row][half][token]
 };
 
 constexpr uint32_t kCtlBytes = (sizeof(SmemCtl) + 127) / 128 * 128;
@@ -173,14 +176,14 @@ struct Walk {
     }
 };
 
-// Warp w handles the gate/up rows k = w, w + NW, ... of [0, 2R): rows
-// [0, R) are the gate rows and [R, 2R) the up rows. Whether it reads the
-// gate / up stage at all:
-__device__ __forceinline__ bool reads_stage(int w, int NW, int R, int m) {
-    for (int k = w; k < 2 * R; k += NW)
-        if ((k >= R) == (m == kUp)) return true;
-    return false;
-}
+// The gate stage and the up stage of a chunk are each R rows x 2 halves
+// (columns [0, H/2) and [H/2, H)) = 2R tasks; warp w takes tasks
+// k = w, w + NW, ... (row k % R, half k / R) of the gate stage, then the
+// same tasks of the up stage. So every warp is done with the gate slot
+// before it starts on the up slot, and the three slots are released at
+// three different times per chunk (gate, up, down): each refill has two
+// phases of the chunk to land in. Whether warp w reads the stages:
+__device__ __forceinline__ bool reads_stages(int w, int R) { return w < 2 * R; }
 
 // ------------------------------------------------------------- producer ---
 
@@ -261,16 +264,17 @@ __device__ __forceinline__ void release(SmemCtl& ctl, int m, int lane) {
     if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[m]));
 }
 
-// Dot product of one gate/up row of a stage with x, over the whole hidden
-// dimension: lane l takes the 16-column chunks l, l + 32, ...; x comes from
-// shared memory as float4 (plane t * 4 + q holds columns 16 c + 4q .. +3 of
-// chunk c in the order (0, 2, 1, 3), so consecutive lanes read consecutive
-// 16-byte words and each half of the float4 pairs with one decoded weight
-// pair of decode16_pairs). The multiply-adds run two at a time (packed
-// fp32 FMA, each lane of it rounded like fmaf).
+// Dot product of one half of a gate/up row of a stage with x: the
+// 16-column chunks [half * nch / 2, (half + 1) * nch / 2); lane l takes the
+// chunks l, l + 32, ... of that range. x comes from shared memory as float4
+// (plane t * 4 + q holds columns 16 c + 4q .. +3 of chunk c in the order
+// (0, 2, 1, 3), so consecutive lanes read consecutive 16-byte words and
+// each half of the float4 pairs with one decoded weight pair of
+// decode16_pairs). The multiply-adds run two at a time (packed fp32 FMA,
+// each lane of it rounded like fmaf).
 template <int T, int NC>
-__device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, const float4* xs, int nch, int lane,
-                                        float (&acc)[T]) {
+__device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, int half, const float4* xs, int nch,
+                                        int lane, float (&acc)[T]) {
     float2 a0[T], a1[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) a0[t] = a1[t] = make_float2(0.0f, 0.0f);
@@ -291,31 +295,31 @@ __device__ __forceinline__ void row_dot(const uint8_t* st, int H, int R, int r, 
             }
         }
     };
+    const int hn = nch / 2, c0 = half * hn;
     if constexpr (NC > 0) {  // every lane has NC chunks: no bounds test
-#pragma unroll 2
-        for (int i = 0; i < NC; ++i) step(lane + 32 * i);
+#pragma unroll
+        for (int i = 0; i < NC; ++i) step(c0 + lane + 32 * i);
     } else {
 #pragma unroll 2
-        for (int c = lane; c < nch; c += 32) step(c);
+        for (int c = c0 + lane; c < c0 + hn; c += 32) step(c);
     }
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[t] = warp_sum((a0[t].x + a0[t].y) + (a1[t].x + a1[t].y));
 }
 
-// This warp's rows of the gate (m = 0) or up (m = 1) stage of a chunk;
-// lane 0 publishes each row's sums into gu[par][m][row][token].
+// This warp's tasks (row halves) of the gate (m = 0) or up (m = 1) stage of
+// a chunk; lane 0 publishes each half's sums into gu[par][m][row][half][token].
 template <int T, int NC>
 __device__ __forceinline__ void gateup_stage(SmemCtl& ctl, const uint8_t* st, int H, int R, int rows, int m,
                                              uint32_t par, const float4* xs, int nch, int warp, int NW, int lane) {
     for (int k = warp; k < 2 * R; k += NW) {
-        if ((k >= R) != (m == kUp)) continue;
-        const int r = k - m * R;
+        const int r = k % R, half = k / R;
         if (r >= rows) continue;
         float acc[T];
-        row_dot<T, NC>(st, H, R, r, xs, nch, lane, acc);
+        row_dot<T, NC>(st, H, R, r, half, xs, nch, lane, acc);
         if (lane == 0) {
 #pragma unroll
-            for (int t = 0; t < T; ++t) ctl.gu[par][m][r][t] = acc[t];
+            for (int t = 0; t < T; ++t) ctl.gu[par][m][r][half][t] = acc[t];
         }
     }
 }
@@ -427,7 +431,7 @@ template <int HC>
 struct Shape {
     static constexpr int kNch = HC / 16;
     static constexpr int kNW = (HC / kDownCols + 31) / 32;
-    static constexpr int kNC = (HC > 0 && kNch % 32 == 0) ? kNch / 32 : 0;
+    static constexpr int kNC = (HC > 0 && kNch % 64 == 0) ? kNch / 64 : 0;  // chunks per lane of a half row
     static constexpr int kRows = HC > 0 ? (kNW / 2 > 4 ? kNW / 2 : 4) : 0;
 };
 
@@ -442,7 +446,7 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
     const int cc = warp * 32 + lane;
     const bool active = cc < H / kDownCols;
     const uint32_t sbytes = stage_bytes(H, R);
-    const bool rd_gate = reads_stage(warp, NW, R, kGate), rd_up = reads_stage(warp, NW, R, kUp);
+    const bool rd_gate = reads_stages(warp, R), rd_up = rd_gate;
     Cols<MT> y;
     zero_cols(y);
     uint32_t written = 0;  // tokens whose partial row this CTA has written
@@ -497,7 +501,9 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
         if (lane < R * T) {
             const int r = lane / T, t = lane % T;
             const float wt = t == 0 ? w.job.w[0] : w.job.w[1];
-            hv = silu(ctl.gu[par][kGate][r][t]) * ctl.gu[par][kUp][r][t] * wt;
+            const float g = ctl.gu[par][kGate][r][0][t] + ctl.gu[par][kGate][r][1][t];
+            const float u = ctl.gu[par][kUp][r][0][t] + ctl.gu[par][kUp][r][1][t];
+            hv = silu(g) * u * wt;
         }
         pending = true;
         p_rows = w.rows;
@@ -555,8 +561,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs
     if (tid == 0) {
         int gate_readers = 0, up_readers = 0;
         for (int w = 0; w < NW; ++w) {
-            gate_readers += reads_stage(w, NW, a.rows, kGate) ? 1 : 0;
-            up_readers += reads_stage(w, NW, a.rows, kUp) ? 1 : 0;
+            gate_readers += reads_stages(w, a.rows) ? 1 : 0;
+            up_readers += reads_stages(w, a.rows) ? 1 : 0;
         }
         for (int m = 0; m < kSlots; ++m) mbar_init(smem_addr(&ctl.full[m]), 1);
         mbar_init(smem_addr(&ctl.empty[kGate]), gate_readers);
