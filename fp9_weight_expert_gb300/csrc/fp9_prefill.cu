@@ -29,10 +29,12 @@
 //        sign planes), loaded by TMA as they lie in memory;
 //   B    the decoded weights of 64 K columns in the MMA's operand layout.
 // Warp roles: warps 0-15 decode raw -> B (one 16-byte fp16 chunk of 8
-// weights per task) and run the epilogue; warp 16 issues the activation
-// loads, warp 17 the raw weight loads (so the HBM weight stream runs ahead
-// of the MMAs by up to the raw ring's depth), warp 18 one thread issues the MMAs and
-// commits each A and B slot back through an mbarrier. gate/up weight rows
+// weights per task) and, in the dense launches, run the epilogue; warp 16
+// issues the activation loads, warp 17 the raw weight loads (so the HBM
+// weight stream runs ahead of the MMAs by up to the raw ring's depth), warp
+// 18 one thread issues the MMAs and commits each A and B slot back through
+// an mbarrier. The grouped (MoE) launch is persistent and has 4 more warps,
+// 19-22, that run the epilogue of one tile while the next one's MMAs run. gate/up weight rows
 // are K-major; down_t tiles are MN-major (K = inter runs across rows), read
 // through the transposed-B bit. Every wait is bounded: a timeout records
 // FP9_ERR_TIMEOUT, raises an abort flag, and the kernel still waits for its
@@ -63,6 +65,10 @@ constexpr int kDecoderWarps = 16;
 constexpr int kDecoderThreads = kDecoderWarps * 32;
 constexpr int kActWarp = kDecoderWarps, kRawWarp = kDecoderWarps + 1, kMmaWarp = kDecoderWarps + 2;
 constexpr int kThreads = (kDecoderWarps + 3) * 32;
+// grouped prefill_kernel: epilogue warps (a multiple of 4: one or more per
+// TMEM lane quarter) besides
+constexpr int kEpiWarp0 = kDecoderWarps + 3, kEpiWarps = 4;
+constexpr int kGroupedThreads = (kDecoderWarps + 3 + kEpiWarps) * 32;
 constexpr int kGuThreads = (kDecoderWarps + 4) * 32;   // gate/up with weights in TMEM: two MMA warps
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemMax = 227 * 1024;
@@ -96,7 +102,6 @@ struct Cfg {
     static constexpr int kBSlots = 2;
     static constexpr int kRawSlots = MH == 1 ? 3 : 2;
     static constexpr int kSmem = 1024 + kCtlBytes + kASlots * kASlotBytes + kBSlots * kBSlot + kRawSlots * kRawSlot;
-    static constexpr uint32_t kTmemCols = MH * 256;
     static_assert(kSmem <= kSmemMax, "shared memory");
 };
 
@@ -105,6 +110,7 @@ struct Ctl {
     uint64_t w_full[4], w_empty[4];   // raw ring: TMA bytes / the decoder warps
     uint64_t b_full[4], b_empty[4];   // decoded ring: the decoder warps / MMA commit
     uint64_t done;                    // every MMA of the CTA finished
+    uint64_t acc_full[2], acc_empty[2];  // prefill_kernel: a tile's accumulator complete / read out
     uint32_t tmem;
     int abort;
     int never;
@@ -223,7 +229,9 @@ __device__ __forceinline__ void decode_chunk(int t, uint32_t raw, int h, uint32_
     }
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the hardware exponential (a few ulp of fp32; h is then
+// rounded to fp16, 2^-11 relative, so that error does not show).
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
 __device__ __forceinline__ bool half2_finite(uint32_t h) {
     return ((h & 0x7C00u) != 0x7C00u) && ((h & 0x7C000000u) != 0x7C000000u);
@@ -241,21 +249,20 @@ __device__ __forceinline__ void fail(Ctl& ctl, int32_t* status) {
     ctl.abort = 1;
 }
 
-template <bool kDown, int MH, bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillMaps maps,
-                                                              const PrefillArgs p) {
-    using C = Cfg<MH>;
-    static_assert(!kGrouped || MH == 1, "grouped tiles are 128 rows");
-    // The CTA's tile: rows [arow0, arow0 + nvalid) of act and out (rows past
-    // nvalid are computed but not stored), output columns from n0, weight
-    // rows of its FFN from wrow0 in the routed or the shared planes.
+// A CTA tile: rows [arow0, arow0 + nvalid) of act and out (rows past
+// nvalid are computed but not stored), output columns from n0, weight rows
+// of its FFN from wrow0 in the routed or the shared planes.
+struct Tile {
     int arow0, nvalid, n0, wrow0;
-    bool shared_bank = false;
+    bool shared_bank;
+};
+
+template <bool kDown, int MH, bool kGrouped>
+__device__ __forceinline__ Tile tile_at(const PrefillArgs& p, int L) {
+    Tile t;
+    t.shared_bank = false;
     if (kGrouped) {
-        grid_dependency_wait();  // the group table comes from the previous launches
-        const int total = p.g_mtile[p.n_groups] * p.ntiles;
-        if (static_cast<int>(blockIdx.x) >= total) return;  // the grid is an upper bound
-        const int q = blockIdx.x / p.ntiles, nt = blockIdx.x - q * p.ntiles;
+        const int q = L / p.ntiles, nt = L - q * p.ntiles;
         int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -263,22 +270,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             else hi = mid - 1;
         }
         const int mt = q - __ldg(p.g_mtile + lo);
-        arow0 = __ldg(p.g_row + lo) + mt * kTileRows;
-        nvalid = __ldg(p.g_cnt + lo) - mt * kTileRows;
-        shared_bank = lo >= p.n_routed;
-        wrow0 = (shared_bank ? lo - p.n_routed : lo) * p.inter;
-        n0 = nt * (kDown ? 2 * kNR : kNR);
+        t.arow0 = __ldg(p.g_row + lo) + mt * kTileRows;
+        t.nvalid = __ldg(p.g_cnt + lo) - mt * kTileRows;
+        t.shared_bank = lo >= p.n_routed;
+        t.wrow0 = (t.shared_bank ? lo - p.n_routed : lo) * p.inter;
+        t.n0 = nt * (kDown ? 2 * kNR : kNR);
     } else {
         int mt, nt;
-        tile_of(blockIdx.x, p.mtiles, p.ntiles, mt, nt);
-        arow0 = mt * kTileRows * MH;
-        nvalid = p.m - arow0;
-        wrow0 = p.wrow0;
+        tile_of(L, p.mtiles, p.ntiles, mt, nt);
+        t.arow0 = mt * kTileRows * MH;
+        t.nvalid = p.m - t.arow0;
+        t.wrow0 = p.wrow0;
         // output columns: 128 intermediate rows (gate/up) or 256 hidden columns (down)
-        n0 = nt * (kDown ? 2 * kNR : kNR);
+        t.n0 = nt * (kDown ? 2 * kNR : kNR);
     }
-    const CUtensorMap* bmap = shared_bank ? maps.body_sh : maps.body;
-    const CUtensorMap* smap = shared_bank ? maps.sign_sh : maps.sign;
+    return t;
+}
+
+// CTA b takes tiles b, b + gridDim.x, ... The dense launches have one CTA
+// per tile, and the decoder warps read the accumulator out once the tile's
+// MMAs are done. The grouped launch (MoE experts: tiles of ~50 tokens and
+// K = inter, each about 20 us of work) is persistent, one CTA per SM: the
+// rings run on across tiles, so the next tile's loads and decoding start
+// while the current tile's last MMAs run, two TMEM accumulators alternate,
+// and the epilogue warps read tile j's while the MMAs of tile j + 1 fill the
+// other. Timed per CTA, a one-tile grouped CTA spent 3.7 us before its
+// first MMA, 2.4 us in its epilogue and 1 us between CTAs out of 25.9.
+template <bool kDown, int MH, bool kGrouped>
+__global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillArgs p) {
+    using C = Cfg<MH>;
+    static_assert(!kGrouped || MH == 1, "grouped tiles are 128 rows");
+    constexpr int kAcc = kGrouped ? 2 : 1;                // accumulators
+    constexpr uint32_t kAccCols = MH * 2 * kNR;           // TMEM columns of one
+    int total;
+    if (kGrouped) {
+        grid_dependency_wait();  // the group table comes from the previous launches
+        total = __ldg(p.g_mtile + p.n_groups) * p.ntiles;
+    } else {
+        total = p.mtiles * p.ntiles;
+    }
+    const int mine = static_cast<int>(blockIdx.x) < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw0 = smem_addr(smem_raw);
     const uint32_t base = (raw0 + 1023u) & ~1023u;
@@ -301,6 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(smem_addr(&ctl.b_full[s]), kDecoderWarps);
             mbar_init(smem_addr(&ctl.b_empty[s]), 1);
         }
+        for (int a = 0; a < kAcc; ++a) {
+            mbar_init(smem_addr(&ctl.acc_full[a]), 1);
+            mbar_init(smem_addr(&ctl.acc_empty[a]), kEpiWarps);
+        }
         mbar_init(smem_addr(&ctl.done), 1);
         ctl.abort = 0;
         ctl.never = 0;
@@ -308,14 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     if (warp == kActWarp && lane == 0) prefetch_map(&maps.act);
     if (warp == kRawWarp && lane == 0) {
-        prefetch_map(&bmap[0]);
-        prefetch_map(&smap[0]);
-        if (!kDown) {
-            prefetch_map(&bmap[1]);
-            prefetch_map(&smap[1]);
+        for (int b = 0; b < (kDown ? 1 : 2); ++b) {
+            prefetch_map(&maps.body[b]);
+            prefetch_map(&maps.sign[b]);
+            if (kGrouped) {
+                prefetch_map(&maps.body_sh[b]);
+                prefetch_map(&maps.sign_sh[b]);
+            }
         }
     }
-    if (warp == 0) tc_alloc(smem_addr(&ctl.tmem), C::kTmemCols);
+    if (warp == 0) tc_alloc(smem_addr(&ctl.tmem), kAcc * kAccCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -323,28 +361,84 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     const int nk = p.nk;
 
+    // Reads tile t's accumulator `acc` out (TMEM lanes 32 (warp mod 4) +
+    // [0, 32): the rows of this warp's lane quarter) for the column blocks
+    // first, first + step, ...: gate/up 8 blocks of 16 intermediate columns
+    // (h = SiLU(g) u rounded to fp16), down 8 blocks of 32 hidden columns.
+    auto read_out = [&](const Tile& t, int acc, int first, int step, bool& bad) {
+        const int lq = warp & 3;
+        const uint32_t tl = tmem + acc * kAccCols + ((static_cast<uint32_t>(lq) * 32u) << 16);
+#pragma unroll
+        for (int mh = 0; mh < MH; ++mh) {
+            const int r = mh * kTileRows + lq * 32 + lane;
+            const int64_t grow = static_cast<int64_t>(t.arow0) + r;
+            const bool valid = r < t.nvalid;
+            if (!kDown) {
+                __half* out = static_cast<__half*>(p.out) + grow * p.ldo + t.n0;
+#pragma unroll 1
+                for (int cb = first; cb < kNR / 16; cb += step) {
+                    float g[16], u[16];
+                    tc_ld16(tl + (mh * 2 + 0) * kNR + cb * 16, g);
+                    tc_ld16(tl + (mh * 2 + 1) * kNR + cb * 16, u);
+                    uint32_t hw[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __half2 h2 =
+                            __floats2half2_rn(silu(g[2 * i]) * u[2 * i], silu(g[2 * i + 1]) * u[2 * i + 1]);
+                        hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                        bad = bad || (valid && !half2_finite(hw[i]));
+                    }
+                    if (valid) {
+                        uint4* o = reinterpret_cast<uint4*>(out + cb * 16);
+                        o[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        o[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int jb = first; jb < 2 * kNR / 32; jb += step) {
+                    const int b = jb / (kNR / 32), cb = jb % (kNR / 32);
+                    float* out = static_cast<float*>(p.out) + grow * p.ldo + t.n0 + b * kNR + cb * 32;
+                    float v[32];
+                    tc_ld32(tl + (mh * 2 + b) * kNR + cb * 32, v);
+                    if (valid) {
+                        float4* o = reinterpret_cast<float4*>(out);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+            }
+        }
+    };
+
     if (warp == kActWarp) {
         // -------------------------------------------- activation loads ---
         if (lane == 0) {
-            grid_dependency_wait();  // the activations come from the previous launch
-            int issued = 0;
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % C::kASlots;
-                if (kc >= C::kASlots &&
-                    !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((kc / C::kASlots) + 1) & 1, p.timeout_ns, &ctl.abort)) {
-                    fail(ctl, p.status);
-                    break;
-                }
-                const uint32_t bar = smem_addr(&ctl.a_full[s]);
-                mbar_arrive_expect_tx(bar, C::kASlotBytes);
+            if (!kGrouped) grid_dependency_wait();  // the activations come from the previous launch
+            int ka = 0;  // chunks issued, over all tiles
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const Tile t = tile_at<kDown, MH, kGrouped>(p, L);
+                for (int kc = 0; kc < nk; ++kc) {
+                    const int s = ka % C::kASlots;
+                    if (ka >= C::kASlots && !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((ka / C::kASlots) + 1) & 1,
+                                                               p.timeout_ns, &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_addr(&ctl.a_full[s]);
+                    mbar_arrive_expect_tx(bar, C::kASlotBytes);
 #pragma unroll
-                for (int mh = 0; mh < MH; ++mh)
-                    tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act, kc * kChunkK,
-                                arow0 + mh * kTileRows, bar);
-                issued = kc + 1;
+                    for (int mh = 0; mh < MH; ++mh)
+                        tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act, kc * kChunkK,
+                                    t.arow0 + mh * kTileRows, bar);
+                    ++ka;
+                }
             }
             // the copies this thread issued land before the CTA may exit
-            for (int j = issued > C::kASlots ? issued - C::kASlots : 0; j < issued; ++j)
+            for (int j = ka > C::kASlots ? ka - C::kASlots : 0; j < ka; ++j)
                 (void)mbar_wait_bounded(smem_addr(&ctl.a_full[j % C::kASlots]), (j / C::kASlots) & 1, p.timeout_ns,
                                         &ctl.never);
         }
@@ -352,37 +446,44 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else if (warp == kRawWarp) {
         // ------------------------------------------------ weight loads ---
         if (lane == 0) {
-            const int nw = nk / 2;
-            int issued = 0;
-            for (int kw = 0; kw < nw; ++kw) {
-                const int s = kw % C::kRawSlots;
-                if (kw >= C::kRawSlots &&
-                    !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / C::kRawSlots) + 1) & 1, p.timeout_ns,
-                                       &ctl.abort)) {
-                    fail(ctl, p.status);
-                    break;
-                }
-                const uint32_t bar = smem_addr(&ctl.w_full[s]);
-                const uint32_t slot = ringW + s * kRawSlot;
-                mbar_arrive_expect_tx(bar, kRawSlot);
-                if (p.no_copy) {
-                    // the bytes never arrive: every wait on this slot runs out
-                } else if (!kDown) {
-                    const int row = wrow0 + n0;
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kw * kRawK, row, bar);
-                        tma_load_2d(slot + b * (kNR * kRawK) + kNR * 64, &bmap[b], kw * kRawK + 64, row, bar);
-                        tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kw * (kRawK / 8), row, bar);
+            const int nw = nk / 2;  // raw chunks of 128 K per tile (K is a multiple of 128)
+            int kw = 0;             // raw chunks issued, over all tiles
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const Tile t = tile_at<kDown, MH, kGrouped>(p, L);
+                const CUtensorMap* bmap = t.shared_bank ? maps.body_sh : maps.body;
+                const CUtensorMap* smap = t.shared_bank ? maps.sign_sh : maps.sign;
+                for (int kr = 0; kr < nw; ++kr) {
+                    const int s = kw % C::kRawSlots;
+                    if (kw >= C::kRawSlots &&
+                        !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / C::kRawSlots) + 1) & 1, p.timeout_ns,
+                                           &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
                     }
-                } else {
-                    const int row = wrow0 + kw * kRawK;
-                    tma_load_2d(slot, &bmap[0], n0, row, bar);
-                    tma_load_2d(slot + kRawBody, &smap[0], n0 / 8, row, bar);
+                    const uint32_t bar = smem_addr(&ctl.w_full[s]);
+                    const uint32_t slot = ringW + s * kRawSlot;
+                    mbar_arrive_expect_tx(bar, kRawSlot);
+                    if (p.no_copy) {
+                        // the bytes never arrive: every wait on this slot runs out
+                    } else if (!kDown) {
+                        const int row = t.wrow0 + t.n0;
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kr * kRawK, row, bar);
+                            tma_load_2d(slot + b * (kNR * kRawK) + kNR * 64, &bmap[b], kr * kRawK + 64, row, bar);
+                            tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kr * (kRawK / 8), row, bar);
+                        }
+                    } else {
+                        const int row = t.wrow0 + kr * kRawK;
+                        tma_load_2d(slot, &bmap[0], t.n0, row, bar);
+                        tma_load_2d(slot + kRawBody, &smap[0], t.n0 / 8, row, bar);
+                    }
+                    ++kw;
                 }
-                issued = kw + 1;
             }
-            for (int j = issued > C::kRawSlots ? issued - C::kRawSlots : 0; j < issued; ++j)
+            for (int j = kw > C::kRawSlots ? kw - C::kRawSlots : 0; j < kw; ++j)
                 (void)mbar_wait_bounded(smem_addr(&ctl.w_full[j % C::kRawSlots]), (j / C::kRawSlots) & 1, p.timeout_ns,
                                         &ctl.never);
         }
@@ -391,29 +492,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------------------------------------------------- MMA ---
         if (lane == 0) {
             const uint32_t idesc = tc_idesc_f16(kTileRows, 2 * kNR) | (kDown ? (1u << 16) : 0u);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int sa = kc % C::kASlots, sb = kc % C::kBSlots;
-                if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kc / C::kASlots) & 1, p.timeout_ns, &ctl.abort) ||
-                    !mbar_wait_bounded(smem_addr(&ctl.b_full[sb]), (kc / C::kBSlots) & 1, p.timeout_ns, &ctl.abort)) {
+            int kg = 0;  // chunks consumed, over all tiles
+            bool ok = true;
+            for (int j = 0; j < mine && ok; ++j) {
+                const int acc = j % kAcc;
+                // the accumulator's previous tile has been read out
+                if (j >= kAcc && !mbar_wait_bounded(smem_addr(&ctl.acc_empty[acc]), ((j / kAcc) - 1) & 1,
+                                                    p.timeout_ns, &ctl.abort)) {
                     fail(ctl, p.status);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sA = ringA + sa * C::kASlotBytes;
-                const uint32_t sB = ringB + sb * kBSlot;
-#pragma unroll
-                for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
-                    const uint64_t bd = kDown ? tc_desc_sw128_mn(sB + 2u * kMnGroupStride * k16, kMnAtomStride,
-                                                                 kMnGroupStride)
-                                              : tc_desc_sw128(sB + 32u * k16);
-#pragma unroll
-                    for (int mh = 0; mh < MH; ++mh) {
-                        const uint64_t ad = tc_desc_sw128(sA + mh * kTileBytes + 32u * k16);
-                        tc_mma_f16(tmem + mh * 2 * kNR, ad, bd, idesc, kc > 0 || k16 > 0);
+                const uint32_t d = tmem + acc * kAccCols;
+                for (int kc = 0; kc < nk; ++kc, ++kg) {
+                    const int sa = kg % C::kASlots, sb = kg % C::kBSlots;
+                    if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kg / C::kASlots) & 1, p.timeout_ns,
+                                           &ctl.abort) ||
+                        !mbar_wait_bounded(smem_addr(&ctl.b_full[sb]), (kg / C::kBSlots) & 1, p.timeout_ns,
+                                           &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t sA = ringA + sa * C::kASlotBytes;
+                    const uint32_t sB = ringB + sb * kBSlot;
+#pragma unroll
+                    for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
+                        const uint64_t bd = kDown ? tc_desc_sw128_mn(sB + 2u * kMnGroupStride * k16, kMnAtomStride,
+                                                                     kMnGroupStride)
+                                                  : tc_desc_sw128(sB + 32u * k16);
+#pragma unroll
+                        for (int mh = 0; mh < MH; ++mh) {
+                            const uint64_t ad = tc_desc_sw128(sA + mh * kTileBytes + 32u * k16);
+                            tc_mma_f16(d + mh * 2 * kNR, ad, bd, idesc, kc > 0 || k16 > 0);
+                        }
+                    }
+                    tc_commit(smem_addr(&ctl.a_empty[sa]));
+                    tc_commit(smem_addr(&ctl.b_empty[sb]));
                 }
-                tc_commit(smem_addr(&ctl.a_empty[sa]));
-                tc_commit(smem_addr(&ctl.b_empty[sb]));
+                if (ok) tc_commit(smem_addr(&ctl.acc_full[acc]));
             }
             tc_commit(smem_addr(&ctl.done));
             // TMEM is freed only after every MMA of this CTA has finished
@@ -421,16 +539,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 record_status(p.status, FP9_ERR_TIMEOUT);
         }
         __syncwarp();
+    } else if (kGrouped && warp >= kEpiWarp0) {
+        // ----------------------------------------------------- epilogue ---
+        // the warps of a lane quarter take alternate column blocks
+        const int eh = (warp - kEpiWarp0) >> 2;
+        bool bad = false;  // a stored h whose fp16 is not finite
+        int j = 0;
+        for (int L = blockIdx.x; L < total; L += gridDim.x, ++j) {
+            const int acc = j % kAcc;
+            if (!warp_wait(smem_addr(&ctl.acc_full[acc]), (j / kAcc) & 1, p.timeout_ns, &ctl.abort)) {
+                if (lane == 0) fail(ctl, p.status);
+                break;
+            }
+            tc_fence_after();
+            read_out(tile_at<kDown, MH, kGrouped>(p, L), acc, eh, kEpiWarps / 4, bad);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[acc]));
+        }
+        if (bad) record_status(p.status, FP9_ERR_RANGE);
     } else {
         // ----------------------------------------------------- decoders ---
         const int t = threadIdx.x;
         bool ok = true;
-        for (int kc = 0; kc < nk && ok; ++kc) {
-            const int kw = kc >> 1, h = kc & 1;
-            const int sw = kw % C::kRawSlots, sb = kc % C::kBSlots;
+        const int nchunks = mine * nk;  // over all of this CTA's tiles
+        for (int kg = 0; kg < nchunks && ok; ++kg) {
+            const int kw = kg >> 1, h = kg & 1;  // every tile has an even number of chunks
+            const int sw = kw % C::kRawSlots, sb = kg % C::kBSlots;
             if (h == 0) ok = warp_wait(smem_addr(&ctl.w_full[sw]), (kw / C::kRawSlots) & 1, p.timeout_ns, &ctl.abort);
-            if (ok && kc >= C::kBSlots)
-                ok = warp_wait(smem_addr(&ctl.b_empty[sb]), ((kc / C::kBSlots) + 1) & 1, p.timeout_ns, &ctl.abort);
+            if (ok && kg >= C::kBSlots)
+                ok = warp_wait(smem_addr(&ctl.b_empty[sb]), ((kg / C::kBSlots) + 1) & 1, p.timeout_ns, &ctl.abort);
             if (!ok) break;
             decode_chunk<kDown>(t, ringW + sw * kRawSlot, h, ringB + sb * kBSlot);
             fence_proxy_async_smem();
@@ -441,59 +579,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
         }
         if (!ok && lane == 0) fail(ctl, p.status);
-        // ----------------------------------------------------- epilogue ---
-        if (warp_wait(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.abort)) {
-            tc_fence_after();
-            // warp w reads TMEM lanes 32 (w mod 4) + [0, 32); the four warps
-            // of a lane quarter split the 32-column blocks: gate/up block
-            // w / 4 of both accumulators (warps past kNR / 32 blocks idle),
-            // down blocks (w / 4) (kNR / 64) + [0, kNR / 64) of the 2 kNR / 32
-            const int lq = warp & 3, sel = warp >> 2;
-            const uint32_t tl = tmem + ((static_cast<uint32_t>(lq) * 32u) << 16);
-            bool bad = false;  // a stored h whose fp16 is not finite
-#pragma unroll
-            for (int mh = 0; mh < MH; ++mh) {
-                const int r = mh * kTileRows + lq * 32 + lane;
-                const int64_t grow = static_cast<int64_t>(arow0) + r;
-                const bool valid = r < nvalid;
-                if (!kDown) {
-                    if (sel < kNR / 32) {
-                        __half* out = static_cast<__half*>(p.out) + grow * p.ldo + n0;
-                        const int cb = sel;
-                        float g[32], u[32];
-                        tc_ld32(tl + (mh * 2 + 0) * kNR + cb * 32, g);
-                        tc_ld32(tl + (mh * 2 + 1) * kNR + cb * 32, u);
-                        uint32_t hw[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const __half2 h2 =
-                                __floats2half2_rn(silu(g[2 * i]) * u[2 * i], silu(g[2 * i + 1]) * u[2 * i + 1]);
-                            hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
-                            bad = bad || (valid && !half2_finite(hw[i]));
-                        }
-                        if (valid) {
-                            uint4* o = reinterpret_cast<uint4*>(out + cb * 32);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                o[v] = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int c2 = 0; c2 < kNR / 64; ++c2) {
-                        const int j = sel * (kNR / 64) + c2;
-                        const int b = j / (kNR / 32), cb = j % (kNR / 32);
-                        float* out = static_cast<float*>(p.out) + grow * p.ldo + n0 + b * kNR + cb * 32;
-                        float v[32];
-                        tc_ld32(tl + (mh * 2 + b) * kNR + cb * 32, v);
-                        if (valid) {
-                            float4* o = reinterpret_cast<float4*>(out);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                        }
-                    }
-                }
+        if (!kGrouped && ok && mine > 0) {
+            // one tile per CTA: the decoder warps read it out, four per
+            // lane quarter on alternate column blocks
+            bool bad = false;
+            if (warp_wait(smem_addr(&ctl.acc_full[0]), 0, p.timeout_ns, &ctl.abort)) {
+                tc_fence_after();
+                read_out(tile_at<kDown, MH, kGrouped>(p, blockIdx.x), 0, warp >> 2, 4, bad);
+            } else if (lane == 0) {
+                fail(ctl, p.status);
             }
             if (bad) record_status(p.status, FP9_ERR_RANGE);
         }
@@ -502,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     grid_launch_dependents();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, C::kTmemCols);
+    if (warp == 0) tc_dealloc(tmem, kAcc * kAccCols);
 }
 
 // ---------------------------------------------- gate/up, weights in TMEM ---
@@ -936,7 +1030,7 @@ fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const
     p.wrow0 = static_cast<int32_t>(wrow0);
     const int mh = choose_mh(m, ntiles, sms);
     p.mtiles = static_cast<int32_t>((m + kTileRows * mh - 1) / (kTileRows * mh));
-    const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles;
+    const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles;  // one CTA per tile
     if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
     void (*k)(const PrefillMaps, const PrefillArgs) =
         down ? (mh == 2 ? prefill_kernel<true, 2, false> : prefill_kernel<true, 1, false>)
@@ -971,7 +1065,6 @@ fp9_status check_prefill_bank(const fp9_ffn_bank* f, int64_t index) {
 fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* shared, const GroupTableDev& tab,
                               int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows,
                               int32_t* status, int sms, cudaStream_t stream) {
-    (void)sms;
     const int64_t H = routed.hidden, I = routed.inter;
     if (max_mtiles <= 0 || rows <= 0) return FP9_OK;
     fp9_status st = ensure_attrs();
@@ -1007,10 +1100,12 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         p.n_groups = tab.n_groups;
         p.n_routed = tab.n_routed;
         p.inter = static_cast<int32_t>(I);
-        const int64_t ctas = max_mtiles * ntiles;
+        int64_t ctas = max_mtiles * ntiles;  // an upper bound of the tiles
         if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
+        // down: a persistent grid of one CTA per SM walks the tiles
+        if (down && ctas > sms) ctas = sms;
         void (*k)(const PrefillMaps, const PrefillArgs) = down ? prefill_kernel<true, 1, true> : gateup_kernel<true>;
-        FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(down ? kThreads : kGuThreads),
+        FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(down ? kGroupedThreads : kGuThreads),
                                 down ? Cfg<1>::kSmem : kGuSmem, stream, maps, p));
     }
     return FP9_OK;
