@@ -95,6 +95,10 @@ _SIGS = {
                                             ctypes.c_int32, ctypes.c_void_p]),
     "fp9_status_str": (ctypes.c_char_p, [ctypes.c_int32]),
     "fp9_profile_events": (None, [ctypes.c_void_p, ctypes.c_void_p]),
+    "fp9_moe_forward_host": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int32,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                            ctypes.c_void_p]),
+    "fp9_moe_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(MoELayerC), ctypes.c_int32]),
     "fp9_moe_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int32,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p]),
@@ -191,6 +195,10 @@ def moe_workspace_bytes(layer, bsz: int) -> int:
     return int(load().fp9_moe_workspace_bytes(ctypes.byref(layer.c_struct()), bsz))
 
 
+def moe_host_workspace_bytes(layer, bsz: int) -> int:
+    return int(load().fp9_moe_host_workspace_bytes(ctypes.byref(layer.c_struct()), bsz))
+
+
 def dense_workspace_bytes(ffn, bsz: int) -> int:
     return int(load().fp9_dense_workspace_bytes(ctypes.byref(ffn.c_struct()), bsz))
 
@@ -209,6 +217,18 @@ def fp9_moe_forward(layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
                                   _ptr(ids), _ptr(weights), _ptr(ws),
                                   ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
            "fp9_moe_forward")
+
+
+def fp9_moe_forward_host(layer, x_host: torch.Tensor, y_host: torch.Tensor, ws: torch.Tensor,
+                         status: torch.Tensor | None = None, stream=None) -> None:
+    """fp9_moe_forward with x and y in host memory (pinned CPU tensors for
+    asynchronous copies): queues the copy in, the forward and the copy out;
+    y_host holds the result once the stream is synchronised."""
+    if x_host.device.type != "cpu" or y_host.device.type != "cpu":
+        raise ValueError("fp9_moe_forward_host takes host (CPU) tensors for x and y")
+    _check(load().fp9_moe_forward_host(ctypes.byref(layer.c_struct()), _ptr(x_host), x_host.shape[0],
+                                       _ptr(y_host), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                       _stream(stream)), "fp9_moe_forward_host")
 
 
 def fp9_dense_ffn(ffn, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,

@@ -110,6 +110,13 @@ class Workspace:
         return cls(n, device)
 
     @classmethod
+    def for_moe_host(cls, layer: MoELayer, bsz: int, device="cuda"):
+        n = binding.moe_host_workspace_bytes(layer, bsz)
+        if n == 0:
+            raise binding.Fp9Error(binding.FP9_ERR_INVALID_ARG, "moe_host_workspace_bytes")
+        return cls(n, device)
+
+    @classmethod
     def for_dense(cls, ffn: FFNBank, bsz: int, device="cuda"):
         n = binding.dense_workspace_bytes(ffn, bsz)
         if n == 0:

@@ -201,6 +201,27 @@ fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x,
                            void* stream);
 
 /*
+ * fp9_moe_forward_host: fp9_moe_forward with x and y in host memory, for a
+ * caller that holds its activations on the host (one call per layer step
+ * instead of a copy, the forward and a copy). This is an interface of this
+ * library only; the pages have no counterpart.
+ *   x_host, y_host: host fp32 [bsz, hidden] (page-locked memory lets the
+ *   copies run asynchronously; pageable memory works but the copy of x
+ *   then finishes before the call returns). Queued on `stream`: the copy
+ *   of x into the workspace, the forward, the copy of y back. y_host holds
+ *   the result once the stream has reached that point (synchronise the
+ *   stream, or wait on an event recorded after the call).
+ *   ws: device, >= fp9_moe_host_workspace_bytes(layer, bsz), 256-byte
+ *   aligned: fp9_moe_forward's workspace followed by two staging rows.
+ *   Errors: as fp9_moe_forward; FP9_ERR_CUDA if a copy cannot be queued.
+ */
+fp9_status fp9_moe_forward_host(const fp9_moe_layer* layer,
+                                const float* x_host, int32_t bsz,
+                                float* y_host, void* ws, size_t ws_bytes,
+                                int32_t* d_status, void* stream);
+size_t fp9_moe_host_workspace_bytes(const fp9_moe_layer* layer, int32_t bsz);
+
+/*
  * fp9_dense_ffn: y = FFN(x) for a dense fp9 SwiGLU FFN (ffn->n == 1), as in
  * the model's first layers. x, y device fp32 [bsz, hidden].
  */

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
               "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
               "fp9_selftest_timeout", "fp9_status_str", "fp9_from_fp8", "fp9_ffn_prefill",
               "fp9_prefill_workspace_bytes", "fp9_moe_prefill", "fp9_moe_prefill_workspace_bytes",
-              "fp9_prefill_selftest_timeout"]:
+              "fp9_prefill_selftest_timeout", "fp9_moe_forward_host", "fp9_moe_host_workspace_bytes"]:
         assert n in names, n
 
 
@@ -95,6 +95,28 @@ def test_moe_forward_argument_checks(lib):
     assert _fwd(lib, _layer(), y=P) == binding.FP9_ERR_INVALID_ARG       # y aliases x
     assert _fwd(lib, _layer(), ws=P + 16) == binding.FP9_ERR_ALIGN
     assert lib.fp9_moe_workspace_bytes(ctypes.byref(_layer(topk=17)), 1) == 0
+
+
+def test_moe_forward_host_argument_checks(lib):
+    # the host buffers are only dereferenced by the queued copies, which an
+    # argument error never reaches
+    xh = ctypes.create_string_buffer(4096)
+    yh = ctypes.create_string_buffer(4096)
+    L = _layer()
+
+    def call(layer=L, x=xh, bsz=1, y=yh, ws=P, ws_bytes=1 << 30):
+        return lib.fp9_moe_forward_host(ctypes.byref(layer) if layer is not None else None, x, bsz, y, ws,
+                                        ws_bytes, None, None)
+    assert call(layer=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(bsz=0) == binding.FP9_ERR_INVALID_ARG
+    assert call(bsz=9) == binding.FP9_ERR_INVALID_ARG
+    assert call(x=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(y=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(y=xh) == binding.FP9_ERR_INVALID_ARG          # y aliases x
+    assert call(ws=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(ws=P + 16) == binding.FP9_ERR_ALIGN
+    assert call(layer=_layer(topk=17)) == binding.FP9_ERR_SHAPE
+    assert lib.fp9_moe_host_workspace_bytes(ctypes.byref(_layer(topk=17)), 1) == 0
 
 
 def test_dense_and_norm_argument_checks(lib):
