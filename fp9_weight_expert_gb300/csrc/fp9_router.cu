@@ -387,6 +387,41 @@ extern "C" size_t fp9_moe_workspace_bytes(const fp9_moe_layer* layer, int32_t bs
     return moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true)).total;
 }
 
+// fp9_moe_forward with host buffers: x and y go through two staging rows
+// at the end of the workspace, copied in and out on the call's stream.
+static size_t host_stage_bytes(int32_t bsz, int64_t hidden) {
+    return align_up(sizeof(float) * static_cast<size_t>(bsz) * static_cast<size_t>(hidden));
+}
+
+extern "C" size_t fp9_moe_host_workspace_bytes(const fp9_moe_layer* layer, int32_t bsz) {
+    const size_t base = fp9_moe_workspace_bytes(layer, bsz);
+    if (base == 0) return 0;
+    return align_up(base) + 2 * host_stage_bytes(bsz, layer->hidden);
+}
+
+extern "C" fp9_status fp9_moe_forward_host(const fp9_moe_layer* layer, const float* x_host, int32_t bsz,
+                                           float* y_host, void* ws, size_t ws_bytes, int32_t* d_status,
+                                           void* stream) {
+    fp9_status st = check_layer(layer, bsz);
+    if (st != FP9_OK) return st;
+    FP9_CHECK_ARG(x_host != nullptr && y_host != nullptr && ws != nullptr && x_host != y_host, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
+    const size_t base = fp9_moe_workspace_bytes(layer, bsz);
+    FP9_CHECK_ARG(base > 0, FP9_ERR_CUDA);
+    const size_t stage = host_stage_bytes(bsz, layer->hidden);
+    FP9_CHECK_ARG(ws_bytes >= align_up(base) + 2 * stage, FP9_ERR_WORKSPACE);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* xd = reinterpret_cast<float*>(w + align_up(base));
+    float* yd = reinterpret_cast<float*>(w + align_up(base) + stage);
+    const size_t bytes = sizeof(float) * static_cast<size_t>(bsz) * static_cast<size_t>(layer->hidden);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FP9_CUDA_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+    st = fp9_moe_forward(layer, xd, bsz, yd, nullptr, nullptr, ws, base, d_status, stream);
+    if (st != FP9_OK) return st;
+    FP9_CUDA_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    return FP9_OK;
+}
+
 extern "C" fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int32_t bsz, int32_t* ids,
                                  float* weights, void* ws, size_t ws_bytes, void* stream) {
     fp9_status st = check_layer(layer, bsz);
