@@ -41,77 +41,85 @@ namespace {
 
 // ------------------------------------------------------------- logits ---
 
-constexpr int kLogitTile = 64, kLogitK = 32, kLogitThreads = 256;
+constexpr int kLogitM = 128, kLogitN = 64, kLogitK = 16, kLogitThreads = 256;
 
-// Partial logits over K split `blockIdx.z` of `splits` equal parts:
-// part[z][t, e] = sum over k of that part of x[t, k] W_g[e, k], fp32, each
-// thread summing its 4 x 4 outputs in k order. The selection adds the parts
-// in split order. (H / splits) % 32 == 0.
-__global__ void __launch_bounds__(kLogitThreads) logits_kernel(const float* __restrict__ x,
-                                                               const float* __restrict__ wr,
-                                                               float* __restrict__ part, int32_t m, int32_t E,
-                                                               int32_t H, int32_t splits) {
-    __shared__ __align__(16) float xs[2][kLogitK][kLogitTile + 4];
-    __shared__ __align__(16) float ws[2][kLogitK][kLogitTile + 4];
+// Partial logits over K part `blockIdx.z` of `splits`: part[z][t, e] = the
+// sum over that part's k of x[t, k] W_g[e, k], fp32, each thread summing its
+// outputs in k order; the selection adds the parts in split order. A CTA
+// computes 128 tokens x 64 experts, a thread 8 x 4 of them (tokens
+// 4 ty + [0, 4) and 64 + 4 ty + [0, 4), experts 4 tx + [0, 4)), reading 3
+// float4 of shared memory per 32 multiply-adds. K runs in steps of 16,
+// double-buffered; part z covers steps [z S / splits, (z + 1) S / splits)
+// of the S = H / 16 steps. H % 16 == 0.
+__global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* __restrict__ x,
+                                                                  const float* __restrict__ wr,
+                                                                  float* __restrict__ part, int32_t m, int32_t E,
+                                                                  int32_t H, int32_t splits) {
+    __shared__ __align__(16) float xs[2][kLogitK][kLogitM + 4];
+    __shared__ __align__(16) float ws[2][kLogitK][kLogitN + 4];
     grid_dependency_wait();
     grid_launch_dependents();
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int t0 = blockIdx.x * kLogitTile, e0 = blockIdx.y * kLogitTile;
-    const int klen = H / splits, kbeg = blockIdx.z * klen;
-    // loads: element (row = i mod 64, k quad = i / 64) for i = tid + 256 j:
-    // a warp stores 32 consecutive rows of one k (no bank conflicts)
-    float4 rx[2], rw[2];
+    const int t0 = blockIdx.x * kLogitM, e0 = blockIdx.y * kLogitN;
+    const int nst = H / kLogitK;
+    const int s0 = static_cast<int>(static_cast<int64_t>(blockIdx.z) * nst / splits);
+    const int s1 = static_cast<int>(static_cast<int64_t>(blockIdx.z + 1) * nst / splits);
+    // loads: four consecutive threads read the 64 bytes of one row's k step
+    // (x: rows (tid + 256 j) / 4 for j = 0, 1; W_g: row tid / 4)
+    const int kq = tid & 3, r0 = tid >> 2;
+    float4 rx[2], rw;
     auto load = [&](int k0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int i = tid + kLogitThreads * j, row = i & 63, kq = i >> 6;
+            const int row = r0 + 64 * j;
             rx[j] = (t0 + row < m)
                         ? __ldg(reinterpret_cast<const float4*>(x + static_cast<int64_t>(t0 + row) * H + k0) + kq)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
-            rw[j] = (e0 + row < E)
-                        ? __ldg(reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e0 + row) * H + k0) + kq)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        rw = (e0 + r0 < E) ? __ldg(reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e0 + r0) * H + k0) + kq)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     auto store = [&](int buf) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int i = tid + kLogitThreads * j, row = i & 63, kq = i >> 6;
+            const int row = r0 + 64 * j;
             xs[buf][4 * kq + 0][row] = rx[j].x;
             xs[buf][4 * kq + 1][row] = rx[j].y;
             xs[buf][4 * kq + 2][row] = rx[j].z;
             xs[buf][4 * kq + 3][row] = rx[j].w;
-            ws[buf][4 * kq + 0][row] = rw[j].x;
-            ws[buf][4 * kq + 1][row] = rw[j].y;
-            ws[buf][4 * kq + 2][row] = rw[j].z;
-            ws[buf][4 * kq + 3][row] = rw[j].w;
         }
+        ws[buf][4 * kq + 0][r0] = rw.x;
+        ws[buf][4 * kq + 1][r0] = rw.y;
+        ws[buf][4 * kq + 2][r0] = rw.z;
+        ws[buf][4 * kq + 3][r0] = rw.w;
     };
-    float acc[4][4] = {};
-    load(kbeg);
-    store(0);
+    float acc[8][4] = {};
+    if (s0 < s1) {
+        load(s0 * kLogitK);
+        store(0);
+    }
     __syncthreads();
-    const int nk = klen / kLogitK;
-    for (int kt = 0; kt < nk; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < nk) load(kbeg + (kt + 1) * kLogitK);
-#pragma unroll 8
-        for (int k = 0; k < kLogitK; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
-            const float4 b = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    for (int st = s0; st < s1; ++st) {
+        const int buf = (st - s0) & 1;
+        if (st + 1 < s1) load((st + 1) * kLogitK);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int k = 0; k < kLogitK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][k][64 + ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        if (kt + 1 < nk) store(buf ^ 1);
+        if (st + 1 < s1) store(buf ^ 1);
         __syncthreads();
     }
     float* out = part + static_cast<int64_t>(blockIdx.z) * m * E;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
         if (t >= m) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -426,15 +434,26 @@ __global__ void __launch_bounds__(kRowThreads) moe_combine_kernel(const CombineA
 
 // -------------------------------------------------------------- host ---
 
-constexpr int kMaxLogitSplits = 8;
+// K parts of the logits GEMM: about three CTAs per SM (the kernel's
+// register budget), and never more parts than the workspace holds.
+int64_t logit_tiles(int64_t m, int64_t E) {
+    return ((m + kLogitM - 1) / kLogitM) * ((E + kLogitN - 1) / kLogitN);
+}
 
-// K splits of the logits GEMM: about four CTAs per SM (eight warps each, so
-// that the shared-memory latency of the FFMA loop is hidden), at most 8.
+// Parts the workspace holds: at most 32 and 1024 CTAs' worth, so that the
+// partial planes take at most about 1024 / tiles x m x E floats.
+int logit_split_cap(int64_t m, int64_t E, int64_t H) {
+    int64_t cap = 1024 / logit_tiles(m, E);
+    if (cap > 32) cap = 32;
+    if (cap > H / kLogitK) cap = H / kLogitK;
+    return cap < 1 ? 1 : static_cast<int>(cap);
+}
+
 int logit_splits(int64_t m, int32_t E, int64_t H, int sms) {
-    const int64_t tiles = ((m + kLogitTile - 1) / kLogitTile) * ((E + kLogitTile - 1) / kLogitTile);
-    int s = 1;
-    while (s < kMaxLogitSplits && tiles * s < 4 * static_cast<int64_t>(sms) && (H / (2 * s)) % kLogitK == 0) s *= 2;
-    return s;
+    int64_t s = 3 * static_cast<int64_t>(sms) / logit_tiles(m, E);
+    const int cap = logit_split_cap(m, E, H);
+    if (s > cap) s = cap;
+    return s < 1 ? 1 : static_cast<int>(s);
 }
 
 struct MoePrefillLayout {
@@ -451,7 +470,7 @@ MoePrefillLayout moe_prefill_layout(const fp9_moe_layer* L, int64_t m) {
     W.max_mtiles = (m * K + kPrefillTileRows - 1) / kPrefillTileRows + E + S * ((m + kPrefillTileRows - 1) / kPrefillTileRows);
     size_t off = align_up(sizeof(uint32_t));
     W.off_logits = off;
-    off = align_up(off + sizeof(float) * kMaxLogitSplits * m * E);
+    off = align_up(off + sizeof(float) * logit_split_cap(m, E, H) * m * E);
     W.off_ids = off;
     off = align_up(off + sizeof(int32_t) * m * K);
     W.off_wts = off;
@@ -525,8 +544,8 @@ extern "C" fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x
 
     const int splits = logit_splits(m, E, H, sms);
     FP9_CUDA_TRY(launch_pdl(logits_kernel,
-                            dim3(static_cast<unsigned>((m + kLogitTile - 1) / kLogitTile),
-                                 static_cast<unsigned>((E + kLogitTile - 1) / kLogitTile), static_cast<unsigned>(splits)),
+                            dim3(static_cast<unsigned>((m + kLogitM - 1) / kLogitM),
+                                 static_cast<unsigned>((E + kLogitN - 1) / kLogitN), static_cast<unsigned>(splits)),
                             dim3(kLogitThreads), 0, s, x, layer->w_router, logits, mi, E, H, splits));
 
     SelectArgs sa{logits, splits, mi, E, layer->n_groups, layer->topk_groups, K, layer->route_scale, ids_ws, wts_ws, ids,
