@@ -142,6 +142,10 @@ struct PrefillArgs {
     const int32_t* g_mtile;
     int32_t n_groups, n_routed;
     int32_t inter;           // weight rows per FFN
+    // dense down: K split into ksplit parts (whole 128-column raw chunks),
+    // part s written to out + s * part_stride (the caller adds the parts)
+    int32_t ksplit;
+    int64_t part_stride;
 };
 
 // CTA order: groups of kGroupM token tiles walk the output tiles together,
@@ -254,6 +258,7 @@ __device__ __forceinline__ void fail(Ctl& ctl, int32_t* status) {
 // of its FFN from wrow0 in the routed or the shared planes.
 struct Tile {
     int arow0, nvalid, n0, wrow0;
+    int part, c0, nc;  // K part, its first 64-column chunk and its chunks
     bool shared_bank;
 };
 
@@ -261,6 +266,9 @@ template <bool kDown, int MH, bool kGrouped>
 __device__ __forceinline__ Tile tile_at(const PrefillArgs& p, int L) {
     Tile t;
     t.shared_bank = false;
+    t.part = 0;
+    t.c0 = 0;
+    t.nc = p.nk;
     if (kGrouped) {
         const int q = L / p.ntiles, nt = L - q * p.ntiles;
         int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
@@ -276,6 +284,13 @@ __device__ __forceinline__ Tile tile_at(const PrefillArgs& p, int L) {
         t.wrow0 = (t.shared_bank ? lo - p.n_routed : lo) * p.inter;
         t.n0 = nt * (kDown ? 2 * kNR : kNR);
     } else {
+        // K part s of the tile: raw chunks [s R / S, (s + 1) R / S) of R
+        const int per_part = p.mtiles * p.ntiles;
+        t.part = L / per_part;
+        L -= t.part * per_part;
+        const int nraw = p.nk / 2;
+        t.c0 = 2 * (t.part * nraw / p.ksplit);
+        t.nc = 2 * ((t.part + 1) * nraw / p.ksplit) - t.c0;
         int mt, nt;
         tile_of(L, p.mtiles, p.ntiles, mt, nt);
         t.arow0 = mt * kTileRows * MH;
@@ -308,9 +323,8 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
         grid_dependency_wait();  // the group table comes from the previous launches
         total = __ldg(p.g_mtile + p.n_groups) * p.ntiles;
     } else {
-        total = p.mtiles * p.ntiles;
+        total = p.mtiles * p.ntiles * p.ksplit;
     }
-    const int mine = static_cast<int>(blockIdx.x) < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw0 = smem_addr(smem_raw);
     const uint32_t base = (raw0 + 1023u) & ~1023u;
@@ -359,8 +373,6 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
 
-    const int nk = p.nk;
-
     // Reads tile t's accumulator `acc` out (TMEM lanes 32 (warp mod 4) +
     // [0, 32): the rows of this warp's lane quarter) for the column blocks
     // first, first + step, ...: gate/up 8 blocks of 16 intermediate columns
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
             const int64_t grow = static_cast<int64_t>(t.arow0) + r;
             const bool valid = r < t.nvalid;
             if (!kDown) {
-                __half* out = static_cast<__half*>(p.out) + grow * p.ldo + t.n0;
+                __half* out = static_cast<__half*>(p.out) + t.part * p.part_stride + grow * p.ldo + t.n0;
 #pragma unroll 1
                 for (int cb = first; cb < kNR / 16; cb += step) {
                     float g[16], u[16];
@@ -398,7 +410,8 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
 #pragma unroll 1
                 for (int jb = first; jb < 2 * kNR / 32; jb += step) {
                     const int b = jb / (kNR / 32), cb = jb % (kNR / 32);
-                    float* out = static_cast<float*>(p.out) + grow * p.ldo + t.n0 + b * kNR + cb * 32;
+                    float* out =
+                        static_cast<float*>(p.out) + t.part * p.part_stride + grow * p.ldo + t.n0 + b * kNR + cb * 32;
                     float v[32];
                     tc_ld32(tl + (mh * 2 + b) * kNR + cb * 32, v);
                     if (valid) {
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
                 const Tile t = tile_at<kDown, MH, kGrouped>(p, L);
-                for (int kc = 0; kc < nk; ++kc) {
+                for (int kc = 0; kc < t.nc; ++kc) {
                     const int s = ka % C::kASlots;
                     if (ka >= C::kASlots && !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((ka / C::kASlots) + 1) & 1,
                                                                p.timeout_ns, &ctl.abort)) {
@@ -432,8 +445,8 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
                     mbar_arrive_expect_tx(bar, C::kASlotBytes);
 #pragma unroll
                     for (int mh = 0; mh < MH; ++mh)
-                        tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act, kc * kChunkK,
-                                    t.arow0 + mh * kTileRows, bar);
+                        tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act,
+                                    (t.c0 + kc) * kChunkK, t.arow0 + mh * kTileRows, bar);
                     ++ka;
                 }
             }
@@ -446,14 +459,13 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
     } else if (warp == kRawWarp) {
         // ------------------------------------------------ weight loads ---
         if (lane == 0) {
-            const int nw = nk / 2;  // raw chunks of 128 K per tile (K is a multiple of 128)
-            int kw = 0;             // raw chunks issued, over all tiles
+            int kw = 0;  // raw chunks of 128 K issued, over all tiles
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
                 const Tile t = tile_at<kDown, MH, kGrouped>(p, L);
                 const CUtensorMap* bmap = t.shared_bank ? maps.body_sh : maps.body;
                 const CUtensorMap* smap = t.shared_bank ? maps.sign_sh : maps.sign;
-                for (int kr = 0; kr < nw; ++kr) {
+                for (int kr = t.c0 / 2; kr < (t.c0 + t.nc) / 2; ++kr) {
                     const int s = kw % C::kRawSlots;
                     if (kw >= C::kRawSlots &&
                         !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / C::kRawSlots) + 1) & 1, p.timeout_ns,
@@ -494,7 +506,9 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
             const uint32_t idesc = tc_idesc_f16(kTileRows, 2 * kNR) | (kDown ? (1u << 16) : 0u);
             int kg = 0;  // chunks consumed, over all tiles
             bool ok = true;
-            for (int j = 0; j < mine && ok; ++j) {
+            int j = 0;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++j) {
+                const int nc = tile_at<kDown, MH, kGrouped>(p, L).nc;
                 const int acc = j % kAcc;
                 // the accumulator's previous tile has been read out
                 if (j >= kAcc && !mbar_wait_bounded(smem_addr(&ctl.acc_empty[acc]), ((j / kAcc) - 1) & 1,
@@ -504,7 +518,7 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + acc * kAccCols;
-                for (int kc = 0; kc < nk; ++kc, ++kg) {
+                for (int kc = 0; kc < nc; ++kc, ++kg) {
                     const int sa = kg % C::kASlots, sb = kg % C::kBSlots;
                     if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kg / C::kASlots) & 1, p.timeout_ns,
                                            &ctl.abort) ||
@@ -562,7 +576,8 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
         // ----------------------------------------------------- decoders ---
         const int t = threadIdx.x;
         bool ok = true;
-        const int nchunks = mine * nk;  // over all of this CTA's tiles
+        int nchunks = 0;  // over all of this CTA's tiles
+        for (int L = blockIdx.x; L < total; L += gridDim.x) nchunks += tile_at<kDown, MH, kGrouped>(p, L).nc;
         for (int kg = 0; kg < nchunks && ok; ++kg) {
             const int kw = kg >> 1, h = kg & 1;  // every tile has an even number of chunks
             const int sw = kw % C::kRawSlots, sb = kg % C::kBSlots;
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
             }
         }
         if (!ok && lane == 0) fail(ctl, p.status);
-        if (!kGrouped && ok && mine > 0) {
+        if (!kGrouped && ok && static_cast<int>(blockIdx.x) < total) {
             // one tile per CTA: the decoder warps read it out, four per
             // lane quarter on alternate column blocks
             bool bad = false;
@@ -1010,16 +1025,77 @@ PrefillArgs base_args(int64_t m, int64_t K, int32_t ntiles, void* out, int64_t l
     p.ldo = ldo;
     p.status = status;
     p.timeout_ns = kTimeoutNs;
+    p.ksplit = 1;
+    p.part_stride = 0;
     return p;
+}
+
+// Token-tile height (MH) and K parts of the dense down GEMM: the fewest
+// rounds of CTAs times one tile's time, plus the pass that adds the parts.
+// A 256-token tile of 256 columns and K takes about 2 K 256^2 / 9.2e12 s on
+// one SM (the measured ~1.4 PFLOP/s over 152 SMs), a 128-token tile about
+// 1 / 1.8 of that, and every CTA spends about 5 us outside its main loop
+// (start and epilogue, timed per CTA); adding S parts reads S planes and
+// writes one at about 6.5 TB/s. A plan replaces the one before it only when
+// it is 3 % cheaper.
+// Without a device (sms <= 0): one part, MH from choose_mh.
+constexpr int kMaxDownSplits = 4;
+
+struct DownPlan {
+    int mh, splits;
+};
+
+DownPlan plan_down(int64_t m, int64_t H, int64_t I, int sms) {
+    const int64_t ntiles = H / (2 * kNR);
+    if (sms <= 0) return DownPlan{choose_mh(m, ntiles, 1), 1};
+    DownPlan best{1, 1};
+    double best_cost = 1e300;
+    for (int mh = 1; mh <= 2; ++mh) {
+        const int64_t mt = (m + kTileRows * mh - 1) / (kTileRows * mh);
+        for (int sp = 1; sp <= kMaxDownSplits && sp <= I / kRawK; ++sp) {
+            const int64_t ctas = mt * ntiles * sp;
+            const double rounds = static_cast<double>((ctas + sms - 1) / sms);
+            const double tile = 2.0 * static_cast<double>(I) / sp * 65536.0 / 9.2e12 / (mh == 2 ? 1.0 : 1.8);
+            const double sum = sp > 1 ? (sp + 1.0) * static_cast<double>(m) * static_cast<double>(H) * 4.0 / 6.5e12 : 0.0;
+            const double cost = rounds * (tile + 5e-6) + sum;
+            if (cost < 0.97 * best_cost) {
+                best_cost = cost;
+                best = DownPlan{mh, sp};
+            }
+        }
+    }
+    return best;
+}
+
+// y = the K parts of the dense down GEMM added in part order (fp32):
+// parts [nparts][n4] float4, y [n4] float4.
+__global__ void __launch_bounds__(256) sum_parts_kernel(const float4* __restrict__ parts, int64_t n4, int32_t nparts,
+                                                        float4* __restrict__ y) {
+    grid_dependency_wait();  // every part is written
+    grid_launch_dependents();
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 a = __ldcs(parts + i);
+        for (int sp = 1; sp < nparts; ++sp) {
+            const float4 b = __ldcs(parts + sp * n4 + i);
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        y[i] = a;
+    }
 }
 
 // One GEMM launch: activations act [m, K] fp16; weight rows [wrow0, ...)
 // of planes with plane_rows rows of `hidden` columns (gate/up: body/sign
 // [0..1] = W_gate, W_up, `ncols` = inter output columns; down:
-// body/sign[0] = down_t, `ncols` = hidden).
+// body/sign[0] = down_t, `ncols` = hidden). A down GEMM whose plan splits K
+// writes its parts to `parts` ([splits, m, ncols] fp32) and adds them into
+// out (ldo == ncols) with a second launch.
 fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const uint8_t* const body[2],
                        const uint8_t* const sign[2], int64_t plane_rows, int64_t hidden, int64_t wrow0, int64_t ncols,
-                       void* out, int64_t ldo, int32_t* status, int sms, cudaStream_t stream) {
+                       void* out, int64_t ldo, float* parts, int32_t* status, int sms, cudaStream_t stream) {
     const int32_t ntiles = static_cast<int32_t>(ncols / (down ? 2 * kNR : kNR));
     PrefillMaps maps;
     if (!make_act_map(&maps.act, act, m, K) || !make_weight_maps(down, body, sign, plane_rows, hidden, maps.body, maps.sign))
@@ -1028,27 +1104,46 @@ fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const
     maps.sign_sh[0] = maps.sign_sh[1] = maps.sign[0];
     PrefillArgs p = base_args(m, K, ntiles, out, ldo, status);
     p.wrow0 = static_cast<int32_t>(wrow0);
-    const int mh = choose_mh(m, ntiles, sms);
+    const DownPlan plan = down ? plan_down(m, ncols, K, sms) : DownPlan{choose_mh(m, ntiles, sms), 1};
+    const int mh = plan.mh;
+    if (plan.splits > 1) {
+        if (parts == nullptr || ldo != ncols) return FP9_ERR_WORKSPACE;
+        p.out = parts;
+        p.ksplit = plan.splits;
+        p.part_stride = m * ncols;
+    }
     p.mtiles = static_cast<int32_t>((m + kTileRows * mh - 1) / (kTileRows * mh));
-    const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles;  // one CTA per tile
+    const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles * p.ksplit;  // one CTA per tile and K part
     if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
     void (*k)(const PrefillMaps, const PrefillArgs) =
         down ? (mh == 2 ? prefill_kernel<true, 2, false> : prefill_kernel<true, 1, false>)
              : (mh == 2 ? prefill_kernel<false, 2, false> : prefill_kernel<false, 1, false>);
     const int smem = mh == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem;
     FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, maps, p));
+    if (plan.splits > 1) {
+        const int64_t n4 = m * ncols / 4;
+        const int64_t blocks = (n4 + 255) / 256 < static_cast<int64_t>(sms) * 8 ? (n4 + 255) / 256 : sms * 8;
+        FP9_CUDA_TRY(launch_pdl(sum_parts_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                                reinterpret_cast<const float4*>(parts), n4, plan.splits, static_cast<float4*>(out)));
+    }
     return FP9_OK;
 }
 
 struct PrefillLayout {
-    size_t off_x16 = 0, off_h = 0, total = 0;
+    size_t off_x16 = 0, off_h = 0, off_parts = 0, total = 0;
 };
 
-PrefillLayout prefill_layout(int64_t m, int64_t hidden, int64_t inter) {
+// x and h as fp16, then the K parts of the down GEMM when its plan splits
+// K (sms: the device's SMs; <= 0: no split).
+PrefillLayout prefill_layout(int64_t m, int64_t hidden, int64_t inter, int sms) {
     PrefillLayout L;
     L.off_x16 = 0;
     L.off_h = align_up(sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(hidden));
-    L.total = L.off_h + align_up(sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(inter));
+    L.off_parts = L.off_h + align_up(sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(inter));
+    const DownPlan plan = plan_down(m, hidden, inter, sms);
+    L.total = L.off_parts + (plan.splits > 1 ? align_up(sizeof(float) * static_cast<size_t>(plan.splits) *
+                                                         static_cast<size_t>(m) * static_cast<size_t>(hidden))
+                                             : 0);
     return L;
 }
 
@@ -1117,7 +1212,7 @@ using namespace fp9;
 
 extern "C" size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m) {
     if (check_prefill_bank(ffn, 0) != FP9_OK || m < 0 || m > FP9_MAX_PREFILL_TOKENS) return 0;
-    return prefill_layout(m, ffn->hidden, ffn->inter).total;
+    return prefill_layout(m, ffn->hidden, ffn->inter, device_sm_count()).total;
 }
 
 extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, const float* x, int64_t m,
@@ -1129,9 +1224,9 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
     FP9_CHECK_ARG(x != nullptr && y != nullptr && ws != nullptr, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(x, 16) && aligned(y, 16) && aligned(ws, 256), FP9_ERR_ALIGN);
     const int64_t H = ffn->hidden, I = ffn->inter;
-    const PrefillLayout lay = prefill_layout(m, H, I);
-    FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     const int sms = device_sm_count();
+    const PrefillLayout lay = prefill_layout(m, H, I, sms);
+    FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     if (sms <= 0) return FP9_ERR_CUDA;
     st = ensure_attrs();
     if (st != FP9_OK) return st;
@@ -1139,6 +1234,7 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
     uint8_t* w = static_cast<uint8_t*>(ws);
     __half* x16 = reinterpret_cast<__half*>(w + lay.off_x16);
     __half* h = reinterpret_cast<__half*>(w + lay.off_h);
+    float* parts = lay.total > lay.off_parts ? reinterpret_cast<float*>(w + lay.off_parts) : nullptr;
 
     const int64_t n4 = m * H / 4;
     const int64_t blocks = (n4 + 255) / 256 < static_cast<int64_t>(sms) * 8 ? (n4 + 255) / 256 : sms * 8;
@@ -1149,11 +1245,11 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
     const size_t wg = static_cast<size_t>(index) * static_cast<size_t>(I) * static_cast<size_t>(H);
     const uint8_t* gu_body[2] = {ffn->gate_body + wg, ffn->up_body + wg};
     const uint8_t* gu_sign[2] = {ffn->gate_sign + wg / 8, ffn->up_sign + wg / 8};
-    st = launch_gemm(false, x16, m, H, gu_body, gu_sign, I, H, 0, I, h, I, d_status, sms, s);
+    st = launch_gemm(false, x16, m, H, gu_body, gu_sign, I, H, 0, I, h, I, nullptr, d_status, sms, s);
     if (st != FP9_OK) return st;
     const uint8_t* d_body[2] = {ffn->down_body + wg, ffn->down_body + wg};
     const uint8_t* d_sign[2] = {ffn->down_sign + wg / 8, ffn->down_sign + wg / 8};
-    return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, H, y, H, d_status, sms, s);
+    return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, H, y, H, parts, d_status, sms, s);
 }
 
 extern "C" fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status, int32_t timeout_us,
