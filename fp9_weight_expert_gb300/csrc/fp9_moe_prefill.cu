@@ -289,20 +289,22 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(const RankArgs a) {
     __shared__ int s_last;
     grid_dependency_wait();
     grid_launch_dependents();
-    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const int e = blockIdx.x, tid = threadIdx.x;
+    // thread t takes the (token, slot) pairs [t L, (t + 1) L) in order: it
+    // counts its matches, one block scan gives each run's first rank, and a
+    // second pass over the run writes the ranks
     const int64_t P = static_cast<int64_t>(a.m) * a.topk;
+    const int64_t L = (P + kRankThreads - 1) / kRankThreads;
+    const int64_t i0 = tid * L, i1 = i0 + L < P ? i0 + L : P;
+    int32_t mine = 0;
+    for (int64_t i = i0; i < i1; ++i) mine += __ldg(a.ids + i) == e ? 1 : 0;
     int32_t base = 0;
-    for (int64_t c0 = 0; c0 < P; c0 += kRankThreads) {
-        const int64_t idx = c0 + tid;
-        const bool match = idx < P && __ldg(a.ids + idx) == e;
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, match);
-        const int32_t before_in_warp = __popc(bal & ((1u << lane) - 1u));
-        int32_t total = 0;
-        const int32_t warp_off = block_scan_excl(lane == 0 ? __popc(bal) : 0, total);
-        const int32_t off = __shfl_sync(0xFFFFFFFFu, warp_off, 0);
-        if (match) a.rank[idx] = base + off + before_in_warp;
-        base += total;
-    }
+    int32_t r = block_scan_excl(mine, base);
+    for (int64_t i = i0; i < i1 && mine > 0; ++i)
+        if (__ldg(a.ids + i) == e) {
+            a.rank[i] = r++;
+            --mine;
+        }
     if (tid == 0) {
         a.cnt[e] = base;
         __threadfence();
