@@ -244,7 +244,10 @@ fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
  *   Shape: hidden % 256 == 0 (256 <= hidden <= FP9_MAX_PREFILL_HIDDEN),
  *          inter % 128 == 0 (inter <= FP9_MAX_INTER), else FP9_ERR_SHAPE.
  *   ws     device, >= fp9_prefill_workspace_bytes(ffn, m), 256-byte aligned
- *          (holds x and h = SiLU(W_gate x) * (W_up x) as fp16).
+ *          (holds x and h = SiLU(W_gate x) * (W_up x) as fp16, and for
+ *          small m the down GEMM's partial outputs: it then splits K into
+ *          up to 4 parts and adds them in part order, so y is still
+ *          deterministic).
  *   Arithmetic: the fp9 weights are exact in fp16 (body << 7 | sign << 15
  *   is their fp16, [MEMOIR-FP9]); x and h are rounded to fp16 (round to
  *   nearest even), the MMA operand type, and products are accumulated in
@@ -258,8 +261,10 @@ fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t k, const float* x,
                            int64_t m, float* y, void* ws, size_t ws_bytes,
                            int32_t* d_status, void* stream);
 
-/* Workspace bytes of fp9_ffn_prefill for m tokens (0 if the arguments are
- * invalid). */
+/* Workspace bytes of fp9_ffn_prefill for m tokens on the current device
+ * (0 if the arguments are invalid): x and h as fp16, plus fp32 partial
+ * outputs when the down GEMM splits K for this m on this device's SM count
+ * (small m), so query it on the device that will run the call. */
 size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m);
 
 /*
