@@ -121,3 +121,21 @@ def test_prefill_matches_decode_path_within_tolerance():
     torch.cuda.synchronize()
     fro, row = support.prefill_errors(y.cpu().numpy(), yd.cpu().numpy())
     assert fro <= support.PREFILL_FRO and row <= support.PREFILL_ROW
+
+
+def test_prefill_workspace_holds_the_down_parts_for_small_m():
+    # small m splits the down GEMM's K: the workspace then also holds fp32
+    # partial outputs, and one with room for x and h only is rejected before
+    # anything runs; large m needs x and h only
+    f = FFNBank(1, 1280, 768)
+    xh = 2 * (768 + 1280)  # bytes per token of x and h as fp16
+    small = binding.prefill_workspace_bytes(f, 517)
+    assert small >= 517 * xh + 2 * 517 * 768 * 4
+    big = binding.prefill_workspace_bytes(f, 65536)
+    assert big < 65536 * xh + 1024
+    x = torch.zeros((517, 768), dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    short = torch.zeros(517 * xh + 1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.Fp9Error) as e:
+        binding.fp9_ffn_prefill(f, x, y, short, 0)
+    assert e.value.code == binding.FP9_ERR_WORKSPACE
