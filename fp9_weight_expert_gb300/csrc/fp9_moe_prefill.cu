@@ -41,17 +41,17 @@ namespace {
 
 // ------------------------------------------------------------- logits ---
 
-constexpr int kLogitM = 128, kLogitN = 64, kLogitK = 16, kLogitThreads = 256;
+constexpr int kLogitM = 128, kLogitN = 128, kLogitK = 16, kLogitThreads = 256;
 
 // Partial logits over K part `blockIdx.z` of `splits`: part[z][t, e] = the
 // sum over that part's k of x[t, k] W_g[e, k], fp32, each thread summing its
 // outputs in k order; the selection adds the parts in split order. A CTA
-// computes 128 tokens x 64 experts, a thread 8 x 4 of them (tokens
-// 4 ty + [0, 4) and 64 + 4 ty + [0, 4), experts 4 tx + [0, 4)), reading 3
-// float4 of shared memory per 32 multiply-adds. K runs in steps of 16,
+// computes 128 tokens x 128 experts, a thread 8 x 8 of them (tokens and
+// experts 4 ty / 4 tx + [0, 4) and 64 + the same), reading 4 float4 of
+// shared memory per 64 multiply-adds. K runs in steps of 16,
 // double-buffered; part z covers steps [z S / splits, (z + 1) S / splits)
 // of the S = H / 16 steps. H % 16 == 0.
-__global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* __restrict__ x,
+__global__ void __launch_bounds__(kLogitThreads, 2) logits_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ wr,
                                                                   float* __restrict__ part, int32_t m, int32_t E,
                                                                   int32_t H, int32_t splits) {
@@ -65,9 +65,9 @@ __global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* _
     const int s0 = static_cast<int>(static_cast<int64_t>(blockIdx.z) * nst / splits);
     const int s1 = static_cast<int>(static_cast<int64_t>(blockIdx.z + 1) * nst / splits);
     // loads: four consecutive threads read the 64 bytes of one row's k step
-    // (x: rows (tid + 256 j) / 4 for j = 0, 1; W_g: row tid / 4)
+    // (rows tid / 4 and 64 + tid / 4 of x and of W_g)
     const int kq = tid & 3, r0 = tid >> 2;
-    float4 rx[2], rw;
+    float4 rx[2], rw[2];
     auto load = [&](int k0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -76,8 +76,13 @@ __global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* _
                         ? __ldg(reinterpret_cast<const float4*>(x + static_cast<int64_t>(t0 + row) * H + k0) + kq)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        rw = (e0 + r0 < E) ? __ldg(reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e0 + r0) * H + k0) + kq)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int row = r0 + 64 * j;
+            rw[j] = (e0 + row < E)
+                        ? __ldg(reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e0 + row) * H + k0) + kq)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     };
     auto store = [&](int buf) {
 #pragma unroll
@@ -88,12 +93,16 @@ __global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* _
             xs[buf][4 * kq + 2][row] = rx[j].z;
             xs[buf][4 * kq + 3][row] = rx[j].w;
         }
-        ws[buf][4 * kq + 0][r0] = rw.x;
-        ws[buf][4 * kq + 1][r0] = rw.y;
-        ws[buf][4 * kq + 2][r0] = rw.z;
-        ws[buf][4 * kq + 3][r0] = rw.w;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int row = r0 + 64 * j;
+            ws[buf][4 * kq + 0][row] = rw[j].x;
+            ws[buf][4 * kq + 1][row] = rw[j].y;
+            ws[buf][4 * kq + 2][row] = rw[j].z;
+            ws[buf][4 * kq + 3][row] = rw[j].w;
+        }
     };
-    float acc[8][4] = {};
+    float acc[8][8] = {};
     if (s0 < s1) {
         load(s0 * kLogitK);
         store(0);
@@ -106,12 +115,14 @@ __global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* _
         for (int k = 0; k < kLogitK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
             const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][k][64 + ty * 4]);
-            const float4 b = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            const float4 b0 = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&ws[buf][k][64 + tx * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
         if (st + 1 < s1) store(buf ^ 1);
         __syncthreads();
@@ -122,8 +133,8 @@ __global__ void __launch_bounds__(kLogitThreads, 3) logits_kernel(const float* _
         const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
         if (t >= m) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
+        for (int j = 0; j < 8; ++j) {
+            const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
             if (e < E) out[static_cast<int64_t>(t) * E + e] = acc[i][j];
         }
     }
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(kRowThreads) moe_combine_kernel(const CombineA
 
 // -------------------------------------------------------------- host ---
 
-// K parts of the logits GEMM: about three CTAs per SM (the kernel's
+// K parts of the logits GEMM: about two CTAs per SM (the kernel's
 // register budget), and never more parts than the workspace holds.
 int64_t logit_tiles(int64_t m, int64_t E) {
     return ((m + kLogitM - 1) / kLogitM) * ((E + kLogitN - 1) / kLogitN);
@@ -452,7 +463,7 @@ int logit_split_cap(int64_t m, int64_t E, int64_t H) {
 }
 
 int logit_splits(int64_t m, int32_t E, int64_t H, int sms) {
-    int64_t s = 3 * static_cast<int64_t>(sms) / logit_tiles(m, E);
+    int64_t s = 2 * static_cast<int64_t>(sms) / logit_tiles(m, E);
     const int cap = logit_split_cap(m, E, H);
     if (s > cap) s = cap;
     return s < 1 ? 1 : static_cast<int>(s);
