@@ -33,8 +33,9 @@
 // issues the activation loads, warp 17 the raw weight loads (so the HBM
 // weight stream runs ahead of the MMAs by up to the raw ring's depth), warp
 // 18 one thread issues the MMAs and commits each A and B slot back through
-// an mbarrier. The grouped (MoE) launch is persistent and has 4 more warps,
-// 19-22, that run the epilogue of one tile while the next one's MMAs run. gate/up weight rows
+// an mbarrier. The grouped (MoE) launches are persistent (one CTA per SM
+// walking the tiles); the grouped down GEMM has 4 more warps, 19-22, that
+// run the epilogue of one tile while the next one's MMAs run. gate/up weight rows
 // are K-major; down_t tiles are MN-major (K = inter runs across rows), read
 // through the transposed-B bit. Every wait is bounded: a timeout records
 // FP9_ERR_TIMEOUT, raises an abort flag, and the kernel still waits for its
@@ -662,40 +663,46 @@ __device__ __forceinline__ void decode_row32(uint32_t raw, uint32_t b, uint32_t 
     for (int i = 0; i < 8; ++i) fp9_to_half4(w[i], spread_sign_nibble((s32 >> (4 * i)) & 0xFu), r[2 * i], r[2 * i + 1]);
 }
 
+// A grouped gate/up tile: rows [arow0, arow0 + nvalid) of act (tokens of
+// one FFN), intermediate rows n0 + [0, 128) of that FFN's W_gate and W_up
+// (weight rows from wrow0 in the routed or the shared planes), and the MMA's
+// N: the valid tokens rounded up to 16.
+struct GuTile {
+    int arow0, nvalid, n0, wrow0;
+    uint32_t n_mma;
+    bool shared_bank;
+};
+
+__device__ __forceinline__ GuTile gu_tile_at(const PrefillArgs& p, int L) {
+    GuTile t;
+    const int q = L / p.ntiles, nt = L - q * p.ntiles;
+    int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.g_mtile + mid) <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    const int mt = q - __ldg(p.g_mtile + lo);
+    t.arow0 = __ldg(p.g_row + lo) + mt * kGuTokens;
+    t.nvalid = __ldg(p.g_cnt + lo) - mt * kGuTokens;
+    t.shared_bank = lo >= p.n_routed;
+    t.wrow0 = (t.shared_bank ? lo - p.n_routed : lo) * p.inter;
+    t.n0 = nt * kNR;
+    t.n_mma = static_cast<uint32_t>((min(t.nvalid, kGuTokens) + 15) / 16 * 16);
+    return t;
+}
+
+// Persistent over the group table's tiles (CTA b: tiles b, b + gridDim.x,
+// ...): the rings run on across tiles, so the next tile's activation and
+// weight loads land while the current tile's MMAs and epilogue run. D (both
+// accumulators) is read out by the decoder warps after the tile's last
+// MMA; the next tile's MMAs wait until it has been (acc_empty).
 template <bool kGrouped>
 __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_constant__ PrefillMaps maps,
                                                              const PrefillArgs p) {
-    int arow0, nvalid, n0, wrow0;
-    bool shared_bank = false;
-    if (kGrouped) {
-        grid_dependency_wait();  // the group table comes from the previous launches
-        const int total = p.g_mtile[p.n_groups] * p.ntiles;
-        if (static_cast<int>(blockIdx.x) >= total) return;  // the grid is an upper bound
-        const int q = blockIdx.x / p.ntiles, nt = blockIdx.x - q * p.ntiles;
-        int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.g_mtile + mid) <= q) lo = mid;
-            else hi = mid - 1;
-        }
-        const int mt = q - __ldg(p.g_mtile + lo);
-        arow0 = __ldg(p.g_row + lo) + mt * kGuTokens;
-        nvalid = __ldg(p.g_cnt + lo) - mt * kGuTokens;
-        shared_bank = lo >= p.n_routed;
-        wrow0 = (shared_bank ? lo - p.n_routed : lo) * p.inter;
-        n0 = nt * kNR;
-    } else {
-        int mt, nt;
-        tile_of(blockIdx.x, p.mtiles, p.ntiles, mt, nt);
-        arow0 = mt * kGuTokens;
-        nvalid = p.m - arow0;
-        wrow0 = p.wrow0;
-        n0 = nt * kNR;
-    }
-    // the MMA's N: the tile's valid tokens rounded up to 16
-    const uint32_t n_mma = static_cast<uint32_t>((min(nvalid, kGuTokens) + 15) / 16 * 16);
-    const CUtensorMap* bmap = shared_bank ? maps.body_sh : maps.body;
-    const CUtensorMap* smap = shared_bank ? maps.sign_sh : maps.sign;
+    static_assert(kGrouped, "the gate/up kernel with weights in TMEM serves the grouped launch");
+    grid_dependency_wait();  // the group table comes from the previous launches
+    const int total = __ldg(p.g_mtile + p.n_groups) * p.ntiles;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw0 = smem_addr(smem_raw);
     const uint32_t base = (raw0 + 1023u) & ~1023u;
@@ -717,6 +724,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
             mbar_init(smem_addr(&ctl.b_full[s]), kDecoderWarps);
             mbar_init(smem_addr(&ctl.b_empty[s]), 2);
         }
+        mbar_init(smem_addr(&ctl.acc_full[0]), 2);                 // both MMA warps' commits of a tile
+        mbar_init(smem_addr(&ctl.acc_empty[0]), kDecoderWarps);    // D read out
         mbar_init(smem_addr(&ctl.done), 2);
         ctl.abort = 0;
         ctl.never = 0;
@@ -724,10 +733,12 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
     }
     if (warp == kActWarp && lane == 0) prefetch_map(&maps.act);
     if (warp == kRawWarp && lane == 0) {
-        prefetch_map(&bmap[0]);
-        prefetch_map(&smap[0]);
-        prefetch_map(&bmap[1]);
-        prefetch_map(&smap[1]);
+        for (int b = 0; b < 2; ++b) {
+            prefetch_map(&maps.body[b]);
+            prefetch_map(&maps.sign[b]);
+            prefetch_map(&maps.body_sh[b]);
+            prefetch_map(&maps.sign_sh[b]);
+        }
     }
     if (warp == 0) tc_alloc(smem_addr(&ctl.tmem), 512);
     tc_fence_before();
@@ -739,22 +750,26 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
     if (warp == kActWarp) {
         // -------------------------------------------- activation loads ---
         if (lane == 0) {
-            grid_dependency_wait();  // the activations come from the previous launch
-            int issued = 0;
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % kGuActSlots;
-                if (kc >= kGuActSlots &&
-                    !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((kc / kGuActSlots) + 1) & 1, p.timeout_ns,
-                                       &ctl.abort)) {
-                    fail(ctl, p.status);
-                    break;
+            int ka = 0;  // chunks issued, over all tiles
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const GuTile t = gu_tile_at(p, L);
+                for (int kc = 0; kc < nk; ++kc) {
+                    const int s = ka % kGuActSlots;
+                    if (ka >= kGuActSlots &&
+                        !mbar_wait_bounded(smem_addr(&ctl.a_empty[s]), ((ka / kGuActSlots) + 1) & 1, p.timeout_ns,
+                                           &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_addr(&ctl.a_full[s]);
+                    mbar_arrive_expect_tx(bar, kGuActSlot);
+                    tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * kChunkK, t.arow0, bar);
+                    ++ka;
                 }
-                const uint32_t bar = smem_addr(&ctl.a_full[s]);
-                mbar_arrive_expect_tx(bar, kGuActSlot);
-                tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * kChunkK, arow0, bar);
-                issued = kc + 1;
             }
-            for (int j = issued > kGuActSlots ? issued - kGuActSlots : 0; j < issued; ++j)
+            for (int j = ka > kGuActSlots ? ka - kGuActSlots : 0; j < ka; ++j)
                 (void)mbar_wait_bounded(smem_addr(&ctl.a_full[j % kGuActSlots]), (j / kGuActSlots) & 1, p.timeout_ns,
                                         &ctl.never);
         }
@@ -762,28 +777,34 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
     } else if (warp == kRawWarp) {
         // ------------------------------------------------ weight loads ---
         if (lane == 0) {
-            const int nw = nk / 2;
-            int issued = 0;
-            for (int kw = 0; kw < nw; ++kw) {
-                const int s = kw % kGuRawSlots;
-                if (kw >= kGuRawSlots &&
-                    !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / kGuRawSlots) + 1) & 1, p.timeout_ns,
-                                       &ctl.abort)) {
-                    fail(ctl, p.status);
-                    break;
-                }
-                const uint32_t bar = smem_addr(&ctl.w_full[s]);
-                const uint32_t slot = ringW + s * kRawSlot;
-                mbar_arrive_expect_tx(bar, kRawSlot);
-                const int row = wrow0 + n0;
+            int kw = 0;  // raw chunks issued, over all tiles
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const GuTile t = gu_tile_at(p, L);
+                const CUtensorMap* bmap = t.shared_bank ? maps.body_sh : maps.body;
+                const CUtensorMap* smap = t.shared_bank ? maps.sign_sh : maps.sign;
+                for (int kr = 0; kr < nk / 2; ++kr) {
+                    const int s = kw % kGuRawSlots;
+                    if (kw >= kGuRawSlots &&
+                        !mbar_wait_bounded(smem_addr(&ctl.w_empty[s]), ((kw / kGuRawSlots) + 1) & 1, p.timeout_ns,
+                                           &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_addr(&ctl.w_full[s]);
+                    const uint32_t slot = ringW + s * kRawSlot;
+                    mbar_arrive_expect_tx(bar, kRawSlot);
+                    const int row = t.wrow0 + t.n0;
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kw * kRawK, row, bar);
-                    tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kw * (kRawK / 8), row, bar);
+                    for (int b = 0; b < 2; ++b) {
+                        tma_load_2d(slot + b * (kNR * kRawK), &bmap[b], kr * kRawK, row, bar);
+                        tma_load_2d(slot + kRawBody + b * (kNR * 16), &smap[b], kr * (kRawK / 8), row, bar);
+                    }
+                    ++kw;
                 }
-                issued = kw + 1;
             }
-            for (int j = issued > kGuRawSlots ? issued - kGuRawSlots : 0; j < issued; ++j)
+            for (int j = kw > kGuRawSlots ? kw - kGuRawSlots : 0; j < kw; ++j)
                 (void)mbar_wait_bounded(smem_addr(&ctl.w_full[j % kGuRawSlots]), (j / kGuRawSlots) & 1, p.timeout_ns,
                                         &ctl.never);
         }
@@ -792,27 +813,41 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
         // ---------------------------------------------------------- MMA ---
         // warp kMmaWarp issues the gate MMAs, the next warp the up MMAs (one
         // issuing thread is part of the per-instruction cost); each commits
-        // its own, so every slot and `done` take two arrivals
+        // its own, so every slot, acc_full and `done` take two arrivals
         const uint32_t ob = static_cast<uint32_t>(warp - kMmaWarp);
         if (lane == 0) {
-            const uint32_t idesc = tc_idesc_f16(kTileRows, n_mma);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int sa = kc % kGuActSlots, sw = kc % kGuWSlots;
-                if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kc / kGuActSlots) & 1, p.timeout_ns, &ctl.abort) ||
-                    !mbar_wait_bounded(smem_addr(&ctl.b_full[sw]), (kc / kGuWSlots) & 1, p.timeout_ns, &ctl.abort)) {
+            int kg = 0, j = 0;  // chunks and tiles consumed
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++j) {
+                const uint32_t idesc = tc_idesc_f16(kTileRows, gu_tile_at(p, L).n_mma);
+                // the previous tile's D has been read out
+                if (j > 0 && !mbar_wait_bounded(smem_addr(&ctl.acc_empty[0]), (j - 1) & 1, p.timeout_ns, &ctl.abort)) {
                     fail(ctl, p.status);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sA = ringA + sa * kGuActSlot;
-                const uint32_t wcol = tmem + kGuWCol0 + sw * 64u;
+                for (int kc = 0; kc < nk; ++kc, ++kg) {
+                    const int sa = kg % kGuActSlots, sw = kg % kGuWSlots;
+                    if (!mbar_wait_bounded(smem_addr(&ctl.a_full[sa]), (kg / kGuActSlots) & 1, p.timeout_ns,
+                                           &ctl.abort) ||
+                        !mbar_wait_bounded(smem_addr(&ctl.b_full[sw]), (kg / kGuWSlots) & 1, p.timeout_ns,
+                                           &ctl.abort)) {
+                        fail(ctl, p.status);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = ringA + sa * kGuActSlot;
+                    const uint32_t wcol = tmem + kGuWCol0 + sw * 64u;
 #pragma unroll
-                for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
-                    const uint64_t bd = tc_desc_sw128(sA + 32u * k16);
-                    tc_mma_f16_tmem_a(tmem + ob * kNR, wcol + ob * 32u + 8u * k16, bd, idesc, kc > 0 || k16 > 0);
+                    for (int k16 = 0; k16 < kChunkK / 16; ++k16) {
+                        const uint64_t bd = tc_desc_sw128(sA + 32u * k16);
+                        tc_mma_f16_tmem_a(tmem + ob * kNR, wcol + ob * 32u + 8u * k16, bd, idesc, kc > 0 || k16 > 0);
+                    }
+                    tc_commit(smem_addr(&ctl.a_empty[sa]));
+                    tc_commit(smem_addr(&ctl.b_empty[sw]));
                 }
-                tc_commit(smem_addr(&ctl.a_empty[sa]));
-                tc_commit(smem_addr(&ctl.b_empty[sw]));
+                if (ok) tc_commit(smem_addr(&ctl.acc_full[0]));
             }
             tc_commit(smem_addr(&ctl.done));
             if (!mbar_wait_bounded(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.never))
@@ -827,58 +862,66 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
         const uint32_t q = warp & 3, sel = warp >> 2, b = sel >> 1, kh = sel & 1;
         const uint32_t row = 32u * q + lane;
         const uint32_t tlane = tmem + ((32u * q) << 16);
-        // Both 64-wide chunks of a raw slot per iteration: two TMEM stores,
-        // then one wait for their completion.
-        bool ok = true;
-        for (int kw = 0; kw < nk / 2 && ok; ++kw) {
-            const int sr = kw % kGuRawSlots;
-            const int kc0 = 2 * kw, sw0 = kc0 % kGuWSlots, sw1 = (kc0 + 1) % kGuWSlots;
-            ok = warp_wait(smem_addr(&ctl.w_full[sr]), (kw / kGuRawSlots) & 1, p.timeout_ns, &ctl.abort);
-            if (ok && kc0 >= kGuWSlots)
-                ok = warp_wait(smem_addr(&ctl.b_empty[sw0]), ((kc0 / kGuWSlots) + 1) & 1, p.timeout_ns, &ctl.abort);
-            if (ok && kc0 + 1 >= kGuWSlots)
-                ok = warp_wait(smem_addr(&ctl.b_empty[sw1]), (((kc0 + 1) / kGuWSlots) + 1) & 1, p.timeout_ns,
-                               &ctl.abort);
-            if (!ok) break;
-            const uint32_t raw = ringW + sr * kRawSlot;
-            uint32_t r[16];
-            decode_row32(raw, b, row, 0, kh, r);
-            tc_st16(tlane + kGuWCol0 + sw0 * 64u + b * 32u + kh * 16u, r);
-            decode_row32(raw, b, row, 1, kh, r);
-            tc_st16(tlane + kGuWCol0 + sw1 * 64u + b * 32u + kh * 16u, r);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_addr(&ctl.b_full[sw0]));
-                mbar_arrive(smem_addr(&ctl.b_full[sw1]));
-                mbar_arrive(smem_addr(&ctl.w_empty[sr]));
+        bool ok = true, bad = false;
+        int kw = 0, j = 0;  // raw chunks and tiles, over all tiles
+        for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++j) {
+            // both 64-wide chunks of a raw slot per iteration: two TMEM
+            // stores, then one wait for their completion
+            for (int kr = 0; kr < nk / 2 && ok; ++kr, ++kw) {
+                const int sr = kw % kGuRawSlots;
+                const int kc0 = 2 * kw, sw0 = kc0 % kGuWSlots, sw1 = (kc0 + 1) % kGuWSlots;
+                ok = warp_wait(smem_addr(&ctl.w_full[sr]), (kw / kGuRawSlots) & 1, p.timeout_ns, &ctl.abort);
+                if (ok && kc0 >= kGuWSlots)
+                    ok = warp_wait(smem_addr(&ctl.b_empty[sw0]), ((kc0 / kGuWSlots) + 1) & 1, p.timeout_ns,
+                                   &ctl.abort);
+                if (ok && kc0 + 1 >= kGuWSlots)
+                    ok = warp_wait(smem_addr(&ctl.b_empty[sw1]), (((kc0 + 1) / kGuWSlots) + 1) & 1, p.timeout_ns,
+                                   &ctl.abort);
+                if (!ok) break;
+                const uint32_t raw = ringW + sr * kRawSlot;
+                uint32_t r[16];
+                decode_row32(raw, b, row, 0, kh, r);
+                tc_st16(tlane + kGuWCol0 + sw0 * 64u + b * 32u + kh * 16u, r);
+                decode_row32(raw, b, row, 1, kh, r);
+                tc_st16(tlane + kGuWCol0 + sw1 * 64u + b * 32u + kh * 16u, r);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_addr(&ctl.b_full[sw0]));
+                    mbar_arrive(smem_addr(&ctl.b_full[sw1]));
+                    mbar_arrive(smem_addr(&ctl.w_empty[sr]));
+                }
             }
-        }
-        if (!ok && lane == 0) fail(ctl, p.status);
-        // ----------------------------------------------------- epilogue ---
-        // warp w: weight rows 32 (w mod 4) + [0, 32), tokens 32 (w / 4) +
-        // [0, 32); h[token, n0 + row] = SiLU(gate) * up, 32 lanes writing 32
-        // consecutive intermediate columns of a token row
-        if (warp_wait(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.abort)) {
+            if (!ok) break;
+            // ------------------------------------------------- epilogue ---
+            // warp w: weight rows 32 (w mod 4) + [0, 32), tokens 32 (w / 4)
+            // + [0, 32); h[token, n0 + row] = SiLU(gate) * up, 32 lanes
+            // writing 32 consecutive intermediate columns of a token row
+            ok = warp_wait(smem_addr(&ctl.acc_full[0]), j & 1, p.timeout_ns, &ctl.abort);
+            if (!ok) break;
             tc_fence_after();
+            const GuTile t = gu_tile_at(p, L);
             const int cb = static_cast<int>(sel);
             float g[32], u[32];
             tc_ld32(tlane + cb * 32, g);
             tc_ld32(tlane + kNR + cb * 32, u);
-            __half* out = static_cast<__half*>(p.out) + n0 + row;
-            bool bad = false;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[0]));  // D may be overwritten now
+            __half* out = static_cast<__half*>(p.out) + t.n0 + row;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = cb * 32 + j;
-                if (t < nvalid) {
-                    const __half hv = __float2half_rn(silu(g[j]) * u[j]);
+            for (int i = 0; i < 32; ++i) {
+                const int tk = cb * 32 + i;
+                if (tk < t.nvalid) {
+                    const __half hv = __float2half_rn(silu(g[i]) * u[i]);
                     bad = bad || __hisinf(hv) || __hisnan(hv);
-                    out[(static_cast<int64_t>(arow0) + t) * p.ldo] = hv;
+                    out[(static_cast<int64_t>(t.arow0) + tk) * p.ldo] = hv;
                 }
             }
-            if (bad) record_status(p.status, FP9_ERR_RANGE);
         }
+        if (!ok && lane == 0) fail(ctl, p.status);
+        if (bad) record_status(p.status, FP9_ERR_RANGE);
     }
 
     grid_launch_dependents();
@@ -1197,8 +1240,8 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         p.inter = static_cast<int32_t>(I);
         int64_t ctas = max_mtiles * ntiles;  // an upper bound of the tiles
         if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
-        // down: a persistent grid of one CTA per SM walks the tiles
-        if (down && ctas > sms) ctas = sms;
+        // a persistent grid of one CTA per SM walks the tiles
+        if (ctas > sms) ctas = sms;
         void (*k)(const PrefillMaps, const PrefillArgs) = down ? prefill_kernel<true, 1, true> : gateup_kernel<true>;
         FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(down ? kGroupedThreads : kGuThreads),
                                 down ? Cfg<1>::kSmem : kGuSmem, stream, maps, p));
