@@ -15,8 +15,8 @@
 // in registers and writes it once per job it touches, and a second kernel
 // adds those partials in a fixed order.
 //
-// CTA layout (one per SM): NW = H / 512 consumer warps (14 for H = 7168)
-// and one producer warp. The producer's lane 0 streams each chunk of
+// CTA layout (one per SM): NW = H / 512 consumer warps (14 for H = 7168;
+// the one-token kernel rounds them up to 16) and one producer warp. The producer's lane 0 streams each chunk of
 // R = NW / 2 rows as three stages, one per ring slot: slot 0 the gate rows,
 // slot 1 the up rows, slot 2 the down rows (bodies, then signs; bulk copies
 // completing on mbarriers).
@@ -53,6 +53,10 @@ constexpr int kSlots = 3;                                       // gate, up, dow
 constexpr int kDownCols = 16;                                   // down columns per thread
 constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / kDownCols / 32;  // 14
 constexpr int kMaxThreads = kMaxConsumerWarps * 32 + 32;        // 480
+// One-token kernels round the consumer warps up to a multiple of 4, so that
+// each of the SM's four schedulers holds as many (16 for H = 7168).
+constexpr int kMaxConsumerWarps1 = (kMaxConsumerWarps + 3) / 4 * 4;
+constexpr int kMaxThreads1 = kMaxConsumerWarps1 * 32 + 32;      // 544
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;           // 1 s
 constexpr int kGate = 0, kUp = 1, kDown = 2;
 
@@ -343,12 +347,14 @@ __device__ __forceinline__ void down_row(const uint8_t* st, int H, int R, int rr
     }
 }
 
-// The down rows of a chunk. RC > 0: a full chunk of RC rows with every lane
-// active is unrolled (no guards).
+// The down rows of a chunk. RC > 0: a full chunk of RC rows is unrolled
+// (no guards) when every lane of the warp owns columns; a warp with lanes
+// past the last column (the one-token kernel's extra warps) takes the
+// guarded loop, whose inactive lanes only join the shuffles.
 template <int T, int MT, int RC>
 __device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int rows, int cc, bool active, float hv,
                                            Cols<MT>& y) {
-    if (RC > 0 && rows == RC) {
+    if (RC > 0 && rows == RC && __all_sync(0xFFFFFFFFu, active)) {
 #pragma unroll
         for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, cc, hv, y);
         return;
@@ -424,13 +430,16 @@ __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float
 }
 
 // The fixed shape of a specialised kernel: hidden size HC (0: any), its
-// consumer warps (16 down columns per thread), the 16-column chunks per
-// lane of a gate/up row, and its rows per chunk (one gate/up row per
-// consumer warp, at least 4).
-template <int HC>
+// consumer warps (16 down columns per thread; a one-token kernel rounds
+// them up to a multiple of 4, one group per scheduler, and the extra warps
+// own no down columns), the 16-column chunks per lane of a half row, and its
+// rows per chunk (two half rows per row: one per consumer warp, at least
+// 4). For H = 7168: 14 warps and 7 rows, or 16 and 8 with one token.
+template <int MT, int HC>
 struct Shape {
     static constexpr int kNch = HC / 16;
-    static constexpr int kNW = (HC / kDownCols + 31) / 32;
+    static constexpr int kNW0 = (HC / kDownCols + 31) / 32;
+    static constexpr int kNW = MT == 1 ? (kNW0 + 3) / 4 * 4 : kNW0;
     static constexpr int kNC = (HC > 0 && kNch % 64 == 0) ? kNch / 64 : 0;  // chunks per lane of a half row
     static constexpr int kRows = HC > 0 ? (kNW / 2 > 4 ? kNW / 2 : 4) : 0;
 };
@@ -438,7 +447,7 @@ struct Shape {
 template <int MT, int HC>
 __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const uint8_t* ring, int NW, int warp,
                          int lane) {
-    using S = Shape<HC>;
+    using S = Shape<MT, HC>;
     const int H = HC > 0 ? HC : a.H;
     const int R = S::kRows > 0 ? S::kRows : a.rows;
     if (S::kNW > 0) NW = S::kNW;
@@ -542,7 +551,7 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
 // MT: most tokens a job can hold (1 when bsz == 1). HC: the hidden size
 // the kernel is specialised for (0: any).
 template <int MT, int HC>
-__global__ void __launch_bounds__(kMaxThreads, 1) expert_kernel(const ExpertArgs a) {
+__global__ void __launch_bounds__(MT == 1 ? kMaxThreads1 : kMaxThreads, 1) expert_kernel(const ExpertArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem);
     float4* xs = reinterpret_cast<float4*>(smem + kCtlBytes);
@@ -665,12 +674,16 @@ struct LaunchShape {
 
 constexpr int kDsv3Hidden = 7168;
 
-// Consumer warps: one thread per 16 hidden columns. Rows per chunk: half
-// the consumer warps (so that the 2R gate/up rows of a chunk give every
-// warp one; 7 for hidden 7168), at least 4, and as many as fit in shared
-// memory next to x.
+// Consumer warps: one thread per 16 hidden columns, rounded up to a
+// multiple of 4 in the one-token kernel (16 for hidden 7168: each of the
+// four schedulers then runs four warps' half rows per phase, where 14 warps
+// left two schedulers with four and two with three). Rows per chunk: half
+// the consumer warps (the 2R half rows of a stage give every warp one: 7,
+// or 8 with one token, for hidden 7168), at least 4, and as many as fit in
+// shared memory next to x.
 static fp9_status expert_shape(int32_t H, int MT, LaunchShape& s) {
-    const int nw = (H / kDownCols + 31) / 32;
+    int nw = (H / kDownCols + 31) / 32;
+    if (MT == 1) nw = (nw + 3) / 4 * 4;  // as many consumer warps per scheduler
     s.threads = nw * 32 + 32;
     const int32_t optin = device_max_smem_optin();
     if (optin <= 0) return FP9_ERR_CUDA;
@@ -752,7 +765,8 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_start, stream));
     // the DeepSeek-V3 hidden size has its own kernel with every loop bound fixed
-    const bool special = H == kDsv3Hidden && shp.rows == Shape<kDsv3Hidden>::kRows;
+    const bool special = H == kDsv3Hidden && shp.rows == (MT == 1 ? Shape<1, kDsv3Hidden>::kRows
+                                                                   : Shape<2, kDsv3Hidden>::kRows);
     void (*kern)(const ExpertArgs) = special ? (MT == 1 ? expert_kernel<1, kDsv3Hidden> : expert_kernel<2, kDsv3Hidden>)
                                              : (MT == 1 ? expert_kernel<1, 0> : expert_kernel<2, 0>);
     FP9_CUDA_TRY(launch_pdl(kern, dim3(lay.grid), dim3(shp.threads), shp.smem, stream, a));
