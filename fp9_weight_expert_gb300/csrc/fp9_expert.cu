@@ -16,8 +16,9 @@
 // adds those partials in a fixed order.
 //
 // CTA layout (one per SM): NW = H / 512 consumer warps (14 for H = 7168;
-// the one-token kernel rounds them up to 16) and one producer warp. The producer's lane 0 streams each chunk of
-// R = NW / 2 rows as three stages, one per ring slot: slot 0 the gate rows,
+// the one-token kernel rounds them up to 16) and one producer warp. The
+// producer's lane 0 streams each chunk of R = NW / 2 rows as three stages,
+// one per ring slot: slot 0 the gate rows,
 // slot 1 the up rows, slot 2 the down rows (bodies, then signs; bulk copies
 // completing on mbarriers).
 //   gate/up: the R rows of the gate stage are cut into 2R half rows, one
