@@ -18,9 +18,8 @@
 // CTA layout (one per SM): NW = H / 512 consumer warps (14 for H = 7168;
 // the one-token kernel rounds them up to 16) and one producer warp. The
 // producer's lane 0 streams each chunk of R = NW / 2 rows as three stages,
-// one per ring slot: slot 0 the gate rows,
-// slot 1 the up rows, slot 2 the down rows (bodies, then signs; bulk copies
-// completing on mbarriers).
+// one per ring slot: slot 0 the gate rows, slot 1 the up rows, slot 2 the
+// down rows (bodies, then signs; bulk copies completing on mbarriers).
 //   gate/up: the R rows of the gate stage are cut into 2R half rows, one
 //     per warp; a warp computes its half row against x (staged in shared
 //     memory), so the only reduction is a 5-step warp sum; lane 0
