@@ -10,8 +10,8 @@ than the 129 MB L2).
   python bench.py --leg fp8_to_fp9|prefill|moe_prefill   (one side measurement alone)
 
 Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on
-the host cores instead (one token through one expert FFN per step, scaled
-to MoE-layer tokens/s). Multi-GPU runs are independent replicas (the path
+the host cores instead (one token through one whole MoE layer per step, its
+expert FFNs on one worker process each). Multi-GPU runs are independent replicas (the path
 has no exchange step), launched one rank per GPU by torchrun.
 """
 
@@ -237,18 +237,19 @@ def _native(args):
     def step(i, ids_out=None):
         binding.fp9_moe_forward(Ls[i % len(Ls)], xs[i % n_tok], y, ws.tensor, status, ids_out)
 
+    # The clock sampler starts before the warm-up, so that the GPU stays busy
+    # from the warm-up into the timed region (an idle GPU takes a while to
+    # come back to full speed, which a short region would measure).
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
     for i in range(W):
         step(i)
-    torch.cuda.synchronize()
-
+    if world > 1:
+        torch.cuda.synchronize()
+        dist.barrier()
     # Timed region: K back-to-back steps with nothing queued between the
     # launches (an event recorded between two launches would stop the next
     # kernel from starting while the previous one finishes).
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
     t_region0 = time.time()
     start.record(stream)
@@ -313,6 +314,8 @@ def _native(args):
     extra = {}
     if not args.no_extra and world == 1:
         extra = _side_runs(Ls, ws, status, dev, shape)
+        extra["tiny"] = _tiny_run(dev)
+        extra["dense_decode"] = _dense_decode_run(dev, _peaks()[0])
         extra["fp8_to_fp9"] = _convert_run(dev, _peaks()[0])
         extra["stack12"] = _stack_run(dev, shape)
         extra["prefill"] = _prefill_run(dev, _tensor_peak())
@@ -379,14 +382,27 @@ def _native(args):
     return out
 
 
+def _streamed_units(ids_step, n_shared: int, bsz: int) -> int:
+    """Expert FFNs the fused kernel streams for one step: each routed expert
+    once per group of up to two of its tokens, each shared expert once per
+    pair of tokens."""
+    from collections import Counter
+    per_expert = Counter(ids_step)
+    return sum((n + 1) // 2 for n in per_expert.values()) + n_shared * ((bsz + 1) // 2)
+
+
 def _side_runs(Ls, ws, status, dev, shape):
-    """bsz 2 on the same layers (weight-stream GB/s of the union of experts)."""
+    """The same layers at bsz 2, 5 and 8 (the pair and verify row counts):
+    weight-stream GB/s of the union of touched experts, and the bytes the
+    kernel actually streams (experts with three or more tokens, and the
+    shared expert, are streamed once per pair of tokens)."""
     import torch
 
     from fp9_weight_expert_gb300 import Workspace, binding, synth
     res = {}
-    for bsz in (2,):
-        K = 400
+    unit = 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT
+    for bsz in (2, 5, 8):
+        K = 400 if bsz == 2 else 200
         xs = synth.tokens(64 * bsz, shape.hidden, synth.seed_for(3000, bsz, synth.TOKENS), dev).view(64, bsz, -1)
         y = torch.empty((bsz, shape.hidden), device=dev)
         ids = torch.empty((K, bsz, shape.topk), dtype=torch.int32, device=dev)
@@ -403,13 +419,93 @@ def _side_runs(Ls, ws, status, dev, shape):
         ms = a.elapsed_time(b)
         idc = ids.cpu()
         units = sum(len(set(idc[i].flatten().tolist())) + shape.n_shared for i in range(K))
-        gbs = units * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT / (ms / 1e3) / 1e9
+        streamed = sum(_streamed_units(idc[i].flatten().tolist(), shape.n_shared, bsz) for i in range(K))
+        gbs = units * unit / (ms / 1e3) / 1e9
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
-                            "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2)}
+                            "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2),
+                            "streamed_experts": round(streamed / K, 2),
+                            "streamed_gbs": round(streamed * unit / (ms / 1e3) / 1e9, 1), "steps": K}
+        del w2
     res.update(_moe_prefill_run(Ls, status, dev, shape, (1481, 4096)))
     if int(status.item()) != 0:
         raise RuntimeError("side runs status: " + binding.status_str(int(status.item())))
     return res
+
+
+def _tiny_run(dev, K=2000):
+    """The tiny layer (hidden 256, 8 experts top-2, 1 shared; 1 MB of fp9,
+    L2-resident, so no roofline claim): tokens/s and us per layer at bsz 1."""
+    import torch
+
+    from fp9_weight_expert_gb300 import Workspace, binding, layers, synth
+    shape = synth.TINY
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    L = layers.MoELayer(shape.hidden, shape.inter, shape.n_experts, shape.n_groups, shape.topk_groups, shape.topk,
+                        shape.n_shared, shape.route_scale, dev)
+    kinds = (synth.ROUTED, synth.SHARED)
+    L.fill(lambda b, k, m: synth.ffn_weight(shape, shape.inter, shape.hidden, synth.seed_for(8100, 0, kinds[b], k, m),
+                                            dev),
+           synth.normal((shape.n_experts, shape.hidden), shape.router_std, synth.seed_for(8100, 0, synth.ROUTER), dev),
+           status)
+    xs = synth.tokens(64, shape.hidden, synth.seed_for(8200, 0, synth.TOKENS), dev).view(64, 1, -1)
+    y = torch.empty((1, shape.hidden), device=dev)
+    ws = Workspace.for_moe(L, 1, dev)
+    for i in range(20):
+        binding.fp9_moe_forward(L, xs[i % 64], y, ws.tensor, status)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        binding.fp9_moe_forward(L, xs[i % 64], y, ws.tensor, status)
+    b.record()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("tiny status: " + binding.status_str(int(status.item())))
+    ms = a.elapsed_time(b) / K
+    return {"tok_s": round(1.0 / (ms / 1e3), 1), "us_per_layer": round(ms * 1e3, 2), "steps": K,
+            "note": "995 KB of fp9: L2-resident, launch-latency bound"}
+
+
+def _dense_decode_run(dev, peak, K=400):
+    """The dense FFN of the model's first layers (hidden 7168, intermediate
+    18432; 445.9 MB of fp9) decoded at bsz 1 and 2 with fp9_dense_ffn; two
+    FFNs alternate, so every call streams its weights from HBM."""
+    import torch
+
+    from fp9_weight_expert_gb300 import FFNBank, Workspace, binding, synth
+    H, I = synth.DENSE_HIDDEN, synth.DENSE_INTER
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fs = []
+    for n in range(2):
+        f = FFNBank(1, I, H, dev)
+        for m in range(3):
+            f.pack(0, m, synth.ffn_weight(None, I, H, synth.seed_for(8300, n, synth.DENSE, 0, m), dev), status)
+        fs.append(f)
+    wbytes = 3 * I * H * FP9_BYTES_PER_WEIGHT
+    out = {"weight_bytes": int(wbytes)}
+    for bsz in (1, 2):
+        xs = synth.tokens(64 * bsz, H, synth.seed_for(8400, bsz, synth.TOKENS), dev).view(64, bsz, -1)
+        y = torch.empty((bsz, H), device=dev)
+        ws = Workspace.for_dense(fs[0], bsz, dev)
+        for i in range(10):
+            binding.fp9_dense_ffn(fs[i % 2], xs[i % 64], y, ws.tensor, status)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(K):
+            binding.fp9_dense_ffn(fs[i % 2], xs[i % 64], y, ws.tensor, status)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / K
+        gbs = wbytes / (ms / 1e3) / 1e9
+        out[f"bsz{bsz}"] = {"tok_s": round(bsz / (ms / 1e3), 1), "us_per_call": round(ms * 1e3, 2),
+                            "weight_stream_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                            "steps": K}
+    if int(status.item()) != 0:
+        raise RuntimeError("dense status: " + binding.status_str(int(status.item())))
+    del fs
+    torch.cuda.empty_cache()
+    return out
 
 
 def _moe_prefill_run(Ls, status, dev, shape, lengths):
@@ -446,11 +542,12 @@ def _moe_prefill_run(Ls, status, dev, shape, lengths):
     return res
 
 
-def _stack_run(dev, shape, n_layers=12, K=40):
+def _stack_run(dev, shape, n_layers=12, K=1000):
     """The 12-layer stack of the workload (config 5): 12 distinct resident
     DeepSeek-V3 MoE layers (153 GB) with the residual + RMSNorm glue between
     them, h <- h + MoE_l(RMSNorm(h)); the whole stack step is captured once
-    in a CUDA graph and replayed. Tokens/s through all 12 layers."""
+    in a CUDA graph and replayed K = 1000 times (the workload's steady
+    state over 1000 steps). Tokens/s through all 12 layers."""
     import torch
 
     from fp9_weight_expert_gb300 import Workspace, binding, layers, synth
@@ -512,7 +609,7 @@ def _stack_run(dev, shape, n_layers=12, K=40):
         out[f"bsz{bsz}"] = {"tok_s": round(bsz / (ms / 1e3), 1), "us_per_stack_step": round(ms * 1e3, 1),
                             "us_per_layer": round(ms * 1e3 / n_layers, 2),
                             "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
-                            "experts_streamed": experts}
+                            "experts_streamed": experts, "steps": K}
     del Ls
     torch.cuda.empty_cache()
     return out
@@ -609,10 +706,16 @@ def _prefill_run(dev, peaks):
 
 
 # ------------------------------------------------------------- CPU oracle
+#
+# The oracle (oracle/, float64 numpy) timed on the host cores as a reported
+# baseline. Each process runs numpy with one BLAS thread; "all cores" runs
+# one worker process per expert FFN of the layer (the oracle's own
+# dense_ffn on that expert's planes), so the FFNs of a layer run side by
+# side, as many at once as there are workers.
 
 def _cpu_baseline(mode: str, steps: int = 0, warmup: int = 0):
-    """Runs the oracle in a fresh single-threaded process (no CUDA) and
-    returns its timing record."""
+    """Runs the oracle timing in a fresh process (no CUDA, one BLAS thread
+    per process) and returns its record."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[v] = "1"
@@ -624,10 +727,119 @@ def _cpu_baseline(mode: str, steps: int = 0, warmup: int = 0):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def _expert_planes(kind: int, k: int):
+    """The oracle's packed planes of one DeepSeek-V3 expert FFN, from the
+    seeded fp32 draws."""
+    import oracle as O
+    from fp9_weight_expert_gb300 import synth
+    shape = synth.DSV3
+    out = []
+    for m in range(3):
+        body, sign, _ = O.fp9_pack(synth.ffn_weight(shape, shape.inter, shape.hidden,
+                                                    synth.seed_for(5000, 0, kind, k, m)).numpy())
+        out += [body, sign]
+    return tuple(out)
+
+
+def _expert_worker(conn, kind: int, k: int):
+    """Child process: packs one expert once (not timed), then answers each
+    token block x with the oracle's dense_ffn(x, planes), or ("parts", x)
+    with the seconds of its two steps (decode the planes, run the FFN on
+    x), until it gets None."""
+    import oracle as O
+    planes = _expert_planes(kind, k)
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        if isinstance(msg, tuple):
+            t0 = time.perf_counter()
+            dec = tuple(O.fp9_decode(planes[2 * i], planes[2 * i + 1]) for i in range(3))
+            t1 = time.perf_counter()
+            O.ffn(msg[1], *dec)
+            conn.send((t1 - t0, time.perf_counter() - t1))
+        else:
+            conn.send(O.dense_ffn(msg, planes))
+    conn.close()
+
+
+class _ExpertPool:
+    """One worker process per expert FFN (spawned: no state is shared)."""
+
+    def __init__(self, experts):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for kind, k in experts:
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_expert_worker, args=(b, kind, k), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def run(self, x):
+        """Every worker's FFN of x, all at once."""
+        for c in self.conns:
+            c.send(x)
+        return [c.recv() for c in self.conns]
+
+    def run_one_at_a_time(self, x):
+        """The same FFNs, one worker at a time (one core busy)."""
+        out = []
+        for c in self.conns:
+            c.send(x)
+            out.append(c.recv())
+        return out
+
+    def parts(self, x):
+        """(decode seconds, FFN seconds) of worker 0 alone."""
+        self.conns[0].send(("parts", x))
+        return self.conns[0].recv()
+
+    def close(self):
+        for c in self.conns:
+            c.send(None)
+        for p in self.procs:
+            p.join(timeout=30)
+
+
+def _oracle_layer_setup():
+    """Config 2 (one DeepSeek-V3 MoE layer, bsz 1): the router weight, one
+    token, its routing (oracle) and the experts it needs."""
+    import oracle as O
+    from fp9_weight_expert_gb300 import synth
+    shape = synth.DSV3
+    wr = synth.normal((shape.n_experts, shape.hidden), shape.router_std, synth.seed_for(5000, 0, synth.ROUTER)).numpy()
+    x = synth.tokens(1, shape.hidden, synth.seed_for(5000, 0, synth.TOKENS)).numpy()
+    ids, w = O.route(x, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
+    experts = [(synth.ROUTED, int(e)) for e in ids[0]] + [(synth.SHARED, 0)]
+    return shape, wr, x, ids, w, experts
+
+
+def _layer_all_cores(pool, x, wr, shape, w, one_core=False):
+    """One layer step on the pool: the oracle's routing, then the routed and
+    shared expert FFNs side by side (or one at a time), added as the
+    oracle's moe() adds them."""
+    import oracle as O
+    O.route(x, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
+    ys = pool.run_one_at_a_time(x) if one_core else pool.run(x)
+    y = sum(float(wk) * yk for wk, yk in zip(w[0], ys[:-1])) + ys[-1]
+    return y
+
+
 def _cpu_sample_worker(spec: str):
-    """Oracle timing, CPU only. mode 'layer': one token through one full
-    DeepSeek-V3 MoE layer (router + 8 routed + 1 shared expert FFN).
-    mode 'expert': per step one token through one of its 9 expert FFNs."""
+    """Oracle timing, CPU only (see _cpu_baseline).
+
+    mode 'layer' (the bench's cpu_baseline): config 2 on one core (the
+    oracle's moe() on one token, two passes) and on all cores (the layer's 9
+    expert FFNs on 9 worker processes); then configs 1, 3 and 4 from the
+    measured per-expert times, scaled to each config's expert count.
+    mode 'ref' (the reference arm): `steps` timed layer steps of config 2 on
+    all cores after `warmup` untimed ones.
+    """
     import numpy as np
 
     import oracle as O
@@ -635,61 +847,108 @@ def _cpu_sample_worker(spec: str):
 
     mode, steps, warmup = spec.split(":")
     steps, warmup = int(steps), int(warmup)
-    shape = synth.DSV3
-    H, I = shape.hidden, shape.inter
-    wr = synth.normal((shape.n_experts, H), shape.router_std, synth.seed_for(5000, 0, synth.ROUTER)).numpy()
-    x = synth.tokens(1, H, synth.seed_for(5000, 0, synth.TOKENS)).numpy()
+    ncores = len(os.sched_getaffinity(0))
+    shape, wr, x, ids, w, experts = _oracle_layer_setup()
     t0 = time.perf_counter()
-    ids, w = O.route(x, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
-    t_router = time.perf_counter() - t0
+    pool = _ExpertPool(experts)
+    setup_s = time.perf_counter() - t0
+    workers = len(experts)
+    used = min(workers, ncores)
+    try:
+        if mode == "ref":
+            for _ in range(warmup):
+                _layer_all_cores(pool, x, wr, shape, w)
+            t0 = time.perf_counter()
+            for _ in range(max(steps, 1)):
+                y = _layer_all_cores(pool, x, wr, shape, w)
+            dt = (time.perf_counter() - t0) / max(steps, 1)
+            assert np.isfinite(y).all()
+            print(json.dumps({
+                "value": round(1.0 / dt, 5), "unit": "tok/s", "cores": used, "host_cores": ncores,
+                "kind": "oracle", "seconds_per_step": round(dt, 4), "setup_s": round(setup_s, 1),
+                "sample": f"per step one token through one DeepSeek-V3 MoE layer: the oracle's routing, then its "
+                          f"8 routed + 1 shared expert FFNs (fp64 numpy, one BLAS thread each) on {workers} worker "
+                          f"processes side by side ({used} of {ncores} host cores busy), added as moe() adds them"}))
+            return
+        # all cores: config 2, two timed passes after one untimed
+        _layer_all_cores(pool, x, wr, shape, w)
+        t0 = time.perf_counter()
+        for _ in range(2):
+            y_all = _layer_all_cores(pool, x, wr, shape, w)
+        t_all = (time.perf_counter() - t0) / 2
+        # one core: the same layer with its FFNs one after the other
+        t0 = time.perf_counter()
+        y_one = _layer_all_cores(pool, x, wr, shape, w, one_core=True)
+        t_one = time.perf_counter() - t0
+        assert np.array_equal(y_one, y_all)
+        t_dec, t_tok = pool.parts(x)
+    finally:
+        pool.close()
+    xs8 = synth.tokens(8, shape.hidden, synth.seed_for(5000, 1, synth.TOKENS)).numpy()
+    t0 = time.perf_counter()
+    ids8, _ = O.route(xs8, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
+    t_route8 = time.perf_counter() - t0
+    configs = {}
+    # config 1: the tiny layer, measured directly (L2-sized, one core)
+    tiny = synth.TINY
 
-    def planes(kind, k):
+    def tiny_planes(kind, k):
         out = []
         for m in range(3):
-            body, sign, _ = O.fp9_pack(synth.ffn_weight(shape, I, H, synth.seed_for(5000, 0, kind, k, m)).numpy())
-            out += [body, sign]
+            b, sg, _ = O.fp9_pack(synth.ffn_weight(tiny, tiny.inter, tiny.hidden,
+                                                   synth.seed_for(5100, 0, kind, k, m)).numpy())
+            out += [b, sg]
         return tuple(out)
-
-    experts = [(synth.ROUTED, int(e), float(wt)) for e, wt in zip(ids[0], w[0])] + [(synth.SHARED, 0, 1.0)]
-    if mode == "layer":
-        cache = {k: planes(kind, k) for kind, k, _ in experts if kind == synth.ROUTED}
-        shared = [planes(synth.SHARED, 0)]
-        reps = 4  # about 10 s of CPU work
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            y = O.moe(x, wr, lambda e: cache[e], shared, shape.n_groups, shape.topk_groups, shape.topk,
-                      shape.route_scale)
-        dt = (time.perf_counter() - t0) / reps
-        assert np.isfinite(y).all()
-        print(json.dumps({"value": round(1.0 / dt, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
-                          "seconds": round(dt * reps, 3),
-                          "sample": f"{reps} passes of one token through one DeepSeek-V3 MoE layer (router over "
-                                    "256 experts, 8 routed + 1 shared expert FFN, fp64 numpy oracle, 1 thread)"}))
-        return
-    n = min(len(experts), steps + warmup)
-    cache = [planes(kind, k) for kind, k, _ in experts[:n]]
-    times = []
-    for i in range(warmup + steps):
-        kind, k, wt = experts[i % n]
-        t0 = time.perf_counter()
-        yk = wt * O.dense_ffn(x, cache[i % n])
-        times.append(time.perf_counter() - t0)
-        assert np.isfinite(yk).all()
-    t_exp = statistics.mean(times[warmup:]) if steps else statistics.mean(times)
-    per_layer = t_router + len(experts) * t_exp
-    print(json.dumps({"value": round(1.0 / per_layer, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
-                      "seconds_per_expert": round(t_exp, 4), "router_seconds": round(t_router, 4),
-                      "seconds_per_step": round(t_exp, 4),
-                      "sample": "per step one token through one of its 9 expert FFNs of a DeepSeek-V3 MoE "
-                                "layer (fp64 numpy oracle, 1 thread); MoE-layer tok/s = "
-                                "1 / (router + 9 x mean expert time)"}))
+    tcache = {k: tiny_planes(synth.ROUTED, k) for k in range(tiny.n_experts)}
+    tsh = [tiny_planes(synth.SHARED, 0)]
+    twr = synth.normal((tiny.n_experts, tiny.hidden), tiny.router_std, synth.seed_for(5100, 0, synth.ROUTER)).numpy()
+    tx = synth.tokens(1, tiny.hidden, synth.seed_for(5100, 0, synth.TOKENS)).numpy()
+    t0 = time.perf_counter()
+    n_tiny = 50
+    for _ in range(n_tiny):
+        O.moe(tx, twr, lambda e: tcache[e], tsh, tiny.n_groups, tiny.topk_groups, tiny.topk, tiny.route_scale)
+    t_tiny = (time.perf_counter() - t0) / n_tiny
+    configs["tiny_bsz1"] = {"tok_s_1core": round(1.0 / t_tiny, 2), "measured": "directly (moe(), 50 passes)"}
+    configs["dsv3_bsz1"] = {"tok_s_1core": round(1.0 / t_one, 5), "tok_s_all_cores": round(1.0 / t_all, 5),
+                            "measured": "directly"}
+    # config 3: bsz 2, 5, 8 tokens drawn independently; the oracle decodes
+    # each distinct expert once and runs one FFN per (token, expert) pair
+    for bsz in (2, 5, 8):
+        U = len(set(ids8[:bsz].flatten().tolist())) + shape.n_shared
+        pairs = bsz * shape.topk + bsz
+        t1 = t_route8 * bsz / 8 + U * t_dec + pairs * t_tok
+        rounds = -(-U // ncores)
+        ta = t_route8 * bsz / 8 + rounds * t_all
+        configs[f"dsv3_bsz{bsz}"] = {"experts": U, "tok_s_1core": round(bsz / t1, 5),
+                                     "tok_s_all_cores": round(bsz / ta, 5),
+                                     "measured": "scaled from the per-expert times (decode once per expert, one "
+                                                 "FFN per token and expert; all cores: one expert per core, "
+                                                 "rounds of the measured all-core layer time)"}
+    # config 4: the dense FFN (18432 = 9 x 2048 rows) costs 9 expert FFNs
+    for bsz in (1, 2):
+        t1 = 9 * t_dec + 9 * bsz * t_tok
+        configs[f"dense_bsz{bsz}"] = {"tok_s_1core": round(bsz / t1, 5),
+                                      "tok_s_all_cores": round(bsz / (t_all + (bsz - 1) * t_tok), 5),
+                                      "measured": "scaled: 9 x one expert's decode + FFN (one core); all cores: "
+                                                  "its 9 row blocks of 2048 side by side, as the 9 expert FFNs "
+                                                  "of config 2, plus one more token's FFN per extra token"}
+    print(json.dumps({
+        "value": round(1.0 / t_all, 5), "unit": "tok/s", "cores": used, "host_cores": ncores, "kind": "oracle",
+        "seconds_all_cores": round(t_all, 4), "one_core": {"value": round(1.0 / t_one, 5), "cores": 1,
+                                                           "seconds": round(t_one, 4)},
+        "per_expert_s": {"decode": round(t_dec, 4), "ffn_one_token": round(t_tok, 4)},
+        "configs": configs,
+        "sample": f"one token through one DeepSeek-V3 MoE layer (oracle routing over 256 experts, 8 routed + 1 "
+                  f"shared expert FFN, fp64 numpy, one BLAS thread per process): all cores = the 9 expert FFNs "
+                  f"on {workers} worker processes side by side ({used} of {ncores} host cores busy, two passes); "
+                  f"one core = the same FFNs one at a time (one pass)"}))
 
 
 def _reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    rec = _cpu_baseline(mode="expert", steps=args.steps, warmup=args.warmup)
+    rec = _cpu_baseline(mode="ref", steps=args.steps, warmup=args.warmup)
     if "error" in rec:
         return {"impl": "reference", "unavailable": "oracle run failed: " + rec["error"][-200:]}
     v = rec["value"]
@@ -707,8 +966,7 @@ def _reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "one DeepSeek-V3 MoE layer, bsz 1 (CPU oracle, sampled per expert)",
-                   "bsz": 1},
+        "config": {"workload": "one DeepSeek-V3 MoE layer, bsz 1 (CPU oracle on the host cores)", "bsz": 1},
         "cpu_baseline": rec,
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

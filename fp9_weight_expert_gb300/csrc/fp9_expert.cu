@@ -35,7 +35,9 @@
 //
 // Every wait is bounded (a timeout sets FP9_ERR_TIMEOUT in the status word
 // and the CTA drains its copies in flight and returns).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <cstdlib>
@@ -703,20 +705,16 @@ static cudaError_t set_smem(int optin) {
 }
 
 static fp9_status ensure_smem_attr() {
-    static bool configured[64] = {false};
-    int dev = 0;
-    FP9_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
-    if (!configured[dev]) {
+    static DeviceOnce attr;
+    return attr.run([] {
         const int32_t optin = device_max_smem_optin();
         if (optin <= 0) return FP9_ERR_CUDA;
         FP9_CUDA_TRY((set_smem<1, 0>(optin)));
         FP9_CUDA_TRY((set_smem<2, 0>(optin)));
         FP9_CUDA_TRY((set_smem<1, kDsv3Hidden>(optin)));
         FP9_CUDA_TRY((set_smem<2, kDsv3Hidden>(optin)));
-        configured[dev] = true;
-    }
-    return FP9_OK;
+        return FP9_OK;
+    });
 }
 
 // Optional events bracketing each fused-kernel launch (fp9_profile_events).
@@ -901,8 +899,9 @@ extern "C" void fp9_profile_events(void* start, void* stop) {
 // The array is a file-scope __device__ object: every GPU that loads this
 // library holds kNoAllocScratchBytes for it until the process exits. Host
 // code may not use the array's name as a device address, so the address is
-// looked up once per device with cudaGetSymbolAddress (with that device
-// current) on the first call made on that device; make that first call
+// looked up with cudaGetSymbolAddress (with that device current) on the
+// first call made on each device, and again on the first call after the
+// device's context was replaced (cudaDeviceReset); make that first call
 // before any stream capture. All calls share the array and it keeps the
 // last call's contents: the control block (the router's ticket and
 // counts) is cleared by every call, and calls that overlap on the GPU
@@ -914,18 +913,48 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The current context (driver entry point looked up once; nullptr if it
+// cannot be had). After cudaDeviceReset a device's primary context is a new
+// one, this library's module is loaded into it again and the array gets a
+// new address, so a saved address is used only in the context it was looked
+// up in.
+static CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        else
+            (void)cudaGetLastError();
+    }
+    CUcontext ctx = nullptr;
+    if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
+// Device address of the scratch array on device `dev` (current), looked up
+// with cudaGetSymbolAddress on the first call in each context of the device
+// and kept; nullptr if the lookup fails.
 static void* noalloc_scratch_ptr(int dev) {
     static std::mutex mu;
     static void* ptrs[64] = {nullptr};
+    static CUcontext ctxs[64] = {nullptr};
     if (dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (ptrs[dev] == nullptr) {
+    const CUcontext ctx = current_context();
+    if (ptrs[dev] == nullptr || ctx == nullptr || ctx != ctxs[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             (void)cudaGetLastError();
+            ptrs[dev] = nullptr;
             return nullptr;
         }
         ptrs[dev] = p;
+        ctxs[dev] = ctx;
     }
     return ptrs[dev];
 }

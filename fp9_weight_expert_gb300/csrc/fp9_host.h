@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <utility>
 
 #include <cuda_runtime.h>
@@ -61,6 +62,32 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// One-time set-up per device (kernel attributes): `run` calls `setup` the
+// first time it is called with a given device current, under a mutex, so
+// first calls from several host threads at once are safe. A set-up that
+// fails is tried again on the next call.
+struct DeviceOnce {
+    std::mutex mu;
+    bool done[64] = {};
+
+    template <typename F>
+    fp9_status run(F&& setup) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FP9_ERR_CUDA;
+        }
+        if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            const fp9_status st = setup();
+            if (st != FP9_OK) return st;
+            done[dev] = true;
+        }
+        return FP9_OK;
+    }
+};
 
 // Number of SMs of the current device (-1 if it cannot be queried).
 int32_t device_sm_count();

@@ -564,14 +564,13 @@ extern "C" fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x
     SelectArgs sa{logits, splits, mi, E, layer->n_groups, layer->topk_groups, K, layer->route_scale, ids_ws, wts_ws, ids,
                   weights};
     const size_t sel_smem = sizeof(float) * kSelectWarps * E;
-    static bool configured[64] = {false};
-    int dev = 0;
-    FP9_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    static DeviceOnce attr;
+    const fp9_status ast = attr.run([] {
         FP9_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(sizeof(float) * kSelectWarps * FP9_MAX_EXPERTS)));
-        configured[dev] = true;
-    }
+        return FP9_OK;
+    });
+    if (ast != FP9_OK) return ast;
     FP9_CUDA_TRY(launch_pdl(select_kernel, dim3(static_cast<unsigned>((m + kSelectWarps - 1) / kSelectWarps)),
                             dim3(kSelectWarps * 32), sel_smem, s, sa));
 

@@ -998,11 +998,8 @@ cudaError_t set_smem_attr() {
 }
 
 fp9_status ensure_attrs() {
-    static bool configured[64] = {false};
-    int dev = 0;
-    FP9_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return FP9_ERR_CUDA;
-    if (!configured[dev]) {
+    static DeviceOnce attr;
+    return attr.run([] {
         const int optin = device_max_smem_optin();
         if (optin < Cfg<1>::kSmem || optin < Cfg<2>::kSmem) return FP9_ERR_CUDA;
         FP9_CUDA_TRY((set_smem_attr<false, 1, false>()));
@@ -1011,9 +1008,8 @@ fp9_status ensure_attrs() {
         FP9_CUDA_TRY((set_smem_attr<true, 2, false>()));
         FP9_CUDA_TRY((set_smem_attr<true, 1, true>()));
         FP9_CUDA_TRY(cudaFuncSetAttribute(gateup_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGuSmem));
-        configured[dev] = true;
-    }
-    return FP9_OK;
+        return FP9_OK;
+    });
 }
 
 // Tensor maps of one weight bank for a GEMM: gate/up read the bodies in

@@ -364,14 +364,13 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.I = L->inter;
     a.grid = lay.grid;
     const size_t smem = sizeof(float) * bsz * L->n_experts;  // <= 32 KB
-    static bool configured[64] = {false};
-    int dev = 0;
-    FP9_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    static DeviceOnce attr;
+    const fp9_status ast = attr.run([] {
         FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
-        configured[dev] = true;
-    }
+        return FP9_OK;
+    });
+    if (ast != FP9_OK) return ast;
     FP9_CUDA_TRY(launch_pdl(router_kernel, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
     return FP9_OK;
 }

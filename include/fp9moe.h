@@ -29,8 +29,11 @@
  * Conventions for every entry point:
  *   - Pointers named as device pointers must point to memory of the current
  *     CUDA device; the caller owns all memory. The library allocates no
- *     memory and never synchronises: work is queued on `stream` (a
- *     cudaStream_t; NULL means the legacy default stream).
+ *     memory (the one exception is the fixed array that
+ *     fp9_moe_forward_noalloc uses, a static device object of the library)
+ *     and does not synchronise (the one exception is a host-buffer call
+ *     with pageable memory, see fp9_moe_forward_host): work is queued on
+ *     `stream` (a cudaStream_t; NULL means the legacy default stream).
  *   - Argument checks run on the host before anything is queued and are
  *     returned synchronously. A failed launch returns FP9_ERR_CUDA.
  *   - Conditions found on the device (a value out of fp9 range, a bounded
@@ -205,9 +208,11 @@ fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x,
  * caller that holds its activations on the host (one call per layer step
  * instead of a copy, the forward and a copy). This is an interface of this
  * library only; the pages have no counterpart.
- *   x_host, y_host: host fp32 [bsz, hidden] (page-locked memory lets the
- *   copies run asynchronously; pageable memory works but the copy of x
- *   then finishes before the call returns). Queued on `stream`: the copy
+ *   x_host, y_host: host fp32 [bsz, hidden]. With page-locked memory both
+ *   copies are asynchronous and the call returns at once. With a pageable
+ *   y_host the call is synchronous: the copy of y back to pageable memory
+ *   returns only once it is done, i.e. after the whole forward (a pageable
+ *   x_host only makes the copy of x finish before the call returns). Queued on `stream`: the copy
  *   of x into the workspace, the forward, the copy of y back. y_host holds
  *   the result once the stream has reached that point (synchronise the
  *   stream, or wait on an event recorded after the call).
@@ -223,7 +228,20 @@ size_t fp9_moe_host_workspace_bytes(const fp9_moe_layer* layer, int32_t bsz);
 
 /*
  * fp9_dense_ffn: y = FFN(x) for a dense fp9 SwiGLU FFN (ffn->n == 1), as in
- * the model's first layers. x, y device fp32 [bsz, hidden].
+ * the model's first layers: the page of [MEMOIR-FP9], section "在只有 AVX2 的
+ * N100 上，我先做出了单核 MLP fp9", where the fp9 MLP first ran as one dense
+ * SwiGLU MLP on a single core (gate, up, SiLU(gate) * up, down).
+ *   x, y   device fp32 [bsz, hidden], 16-byte aligned, y may not alias x;
+ *          1 <= bsz <= FP9_MAX_BSZ.
+ *   ffn    host struct (device planes), n == 1; hidden % 128 == 0 and
+ *          hidden <= FP9_MAX_HIDDEN, 1 <= inter <= FP9_MAX_INTER
+ *          (FP9_ERR_SHAPE otherwise).
+ *   ws     device, >= fp9_dense_workspace_bytes(ffn, bsz), 256-byte aligned.
+ *   The weights are streamed once per call for each pair of tokens; the
+ *   arithmetic is the decode step's (fp32 products and sums, partials over
+ *   intermediate slices added in a fixed order: deterministic for a device).
+ *   Errors: argument checks as above (synchronous); FP9_ERR_TIMEOUT in
+ *   *d_status if a bounded wait runs out.
  */
 fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
                          float* y, void* ws, size_t ws_bytes, int32_t* d_status,
@@ -300,7 +318,14 @@ size_t fp9_moe_prefill_workspace_bytes(const fp9_moe_layer* layer, int64_t m);
  * fp9_residual_rmsnorm: stack glue between layers, per token t:
  *   h[t] += y[t] (skipped when y is NULL);
  *   x_out[t] = h[t] / sqrt(mean(h[t]^2) + eps)   (unit gain).
- *   h, y, x_out device fp32 [bsz, hidden], 16-byte aligned, hidden % 4 == 0.
+ * The pages keep the layernorm and the residual add on the GPU side of each
+ * decode layer ("第 9 章 MTP1 dual-lane overlap", section 9.5: stage 0 of a
+ * layer holds them); between two MoE layers of a stack the step is
+ * h <- h + MoE(RMSNorm(h)).
+ *   h, y, x_out device fp32 [bsz, hidden], 16-byte aligned, hidden % 4 == 0;
+ *   h is updated in place; x_out may not alias h or y. 1 <= bsz <=
+ *   FP9_MAX_BSZ, eps >= 0. The sum of squares is added in a fixed order.
+ *   Errors: FP9_ERR_INVALID_ARG / FP9_ERR_SHAPE / FP9_ERR_ALIGN (synchronous).
  */
 fp9_status fp9_residual_rmsnorm(float* h, const float* y, float* x_out,
                                 int32_t bsz, int64_t hidden, float eps,
@@ -344,7 +369,9 @@ fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes,
  *   A call whose workspace would not fit returns FP9_ERR_WORKSPACE (the
  *   DeepSeek-V3 layer fits up to bsz 3 on a 152-SM GPU).
  *   The first call on a device looks up the array's device address on
- *   that device (cudaGetSymbolAddress): make it before any stream capture.
+ *   that device (cudaGetSymbolAddress), and so does the first call after
+ *   the device's context was replaced (cudaDeviceReset): make that call
+ *   before any stream capture.
  *   Every call clears the control block it needs zeroed. All calls share
  *   the one array, so calls that overlap on the GPU (other streams, other
  *   host threads) race: serialise them.

@@ -2,10 +2,11 @@
 memory (a runtime that owns and caps device memory, a plugin handed only
 its buffers, a path that must not risk an allocation's synchronisation).
 
-It runs the same kernels as fp9_moe_forward with the library's fixed
-scratch array as the workspace; its output must match the workspace
-version on two calls in a row (the second call reuses the array as the
-first left it). Collected last, so a failure here stops a run only after
+It runs the same kernels, plan and grid as fp9_moe_forward with the
+library's fixed scratch array as the workspace, and both add their partial
+sums in the same fixed order; so its routing and its output must equal the
+workspace version's bit for bit, on two calls in a row (the second call
+reuses the array as the first left it). Collected last, so a failure here stops a run only after
 every other test has run."""
 
 import numpy as np
@@ -29,13 +30,18 @@ def test_noalloc_forward_matches_workspace_forward_twice(shape, bsz):
         x = support.safe_tokens(shape, wr, bsz, 910 + 10 * call + bsz, device="cuda")
         y_ref = torch.empty_like(x)
         ids_ref = torch.empty((bsz, shape.topk), dtype=torch.int32, device="cuda")
-        binding.fp9_moe_forward(L, x, y_ref, ws.tensor, status, ids_ref)
+        w_ref = torch.empty((bsz, shape.topk), dtype=torch.float32, device="cuda")
+        binding.fp9_moe_forward(L, x, y_ref, ws.tensor, status, ids_ref, w_ref)
         y = torch.full_like(x, float("nan"))
         ids = torch.empty_like(ids_ref)
-        binding.fp9_moe_forward_noalloc(L, x, y, status, ids)
+        w = torch.full_like(w_ref, float("nan"))
+        binding.fp9_moe_forward_noalloc(L, x, y, status, ids, w)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, binding.status_str(int(status.item()))
         assert torch.equal(ids, ids_ref)
+        assert torch.equal(w, w_ref)
+        assert torch.equal(y, y_ref)
+        # and the oracle's tolerance, as for the workspace call
         assert support.max_rel_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= support.TOL
     del L
     torch.cuda.empty_cache()
