@@ -521,20 +521,24 @@ def _moe_prefill_run(Ls, status, dev, shape, lengths):
         x = synth.tokens(m, shape.hidden, synth.seed_for(3100, m, synth.TOKENS), dev)
         y = torch.empty_like(x)
         wp = Workspace.for_moe_prefill(Ls[0], m, dev)
-        for i in range(2):
-            binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status)
-        torch.cuda.synchronize()
-        K = 8
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for i in range(K):
-            binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status)
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / K
-        wbytes = (shape.n_experts + shape.n_shared) * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT
-        res[f"moe_prefill_m{m}"] = {"us_per_layer": round(ms * 1e3, 1), "tok_s": round(m / (ms / 1e3)),
-                                    "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1)}
+        for name, prec in (("split", binding.FP9_PREFILL_SPLIT), ("fp16", binding.FP9_PREFILL_FP16)):
+            for i in range(2):
+                binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status, precision=prec)
+            torch.cuda.synchronize()
+            K = 8
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(K):
+                binding.fp9_moe_prefill(Ls[i % len(Ls)], x, y, wp.tensor, status, precision=prec)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / K
+            wbytes = (shape.n_experts + shape.n_shared) * 3 * shape.inter * shape.hidden * FP9_BYTES_PER_WEIGHT
+            key = f"moe_prefill_m{m}" + ("" if name == "split" else "_fp16")
+            res[key] = {"us_per_layer": round(ms * 1e3, 1), "tok_s": round(m / (ms / 1e3)),
+                        "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+                        "precision": "activations as two fp16 terms (hi + lo; the default)" if name == "split"
+                        else "activations as one fp16 term (opt-in)"}
         del wp
         torch.cuda.empty_cache()
     if int(status.item()) != 0:
@@ -683,23 +687,30 @@ def _prefill_run(dev, peaks):
             y = torch.empty_like(x)
             ws = Workspace.for_prefill(f, m, dev).tensor
             status = torch.zeros(1, dtype=torch.int32, device=dev)
-            for i in range(3):
-                binding.fp9_ffn_prefill(f, x, y, ws, i % n, status)
-            torch.cuda.synchronize()
-            K = 20
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            for i in range(K):
-                binding.fp9_ffn_prefill(f, x, y, ws, i % n, status)
-            b.record()
-            torch.cuda.synchronize()
-            if int(status.item()) != 0:
-                raise RuntimeError("fp9_ffn_prefill status: " + binding.status_str(int(status.item())))
-            us = a.elapsed_time(b) / K * 1e3
-            tf = 2.0 * m * 3 * H * I / (us * 1e-6) / 1e12
-            out[f"{name}_m{m}"] = {"us_per_call": round(us, 1), "tflops": round(tf, 1),
-                                   "tok_per_s": round(m / (us * 1e-6)), "peak_tflops": peak,
-                                   "frac": round(tf / peak, 4), "bound": "tensor", "dtype": "fp16 x fp9->fp16"}
+            for pname, prec in (("split", binding.FP9_PREFILL_SPLIT), ("fp16", binding.FP9_PREFILL_FP16)):
+                for i in range(3):
+                    binding.fp9_ffn_prefill(f, x, y, ws, i % n, status, precision=prec)
+                torch.cuda.synchronize()
+                K = 20
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for i in range(K):
+                    binding.fp9_ffn_prefill(f, x, y, ws, i % n, status, precision=prec)
+                b.record()
+                torch.cuda.synchronize()
+                if int(status.item()) != 0:
+                    raise RuntimeError("fp9_ffn_prefill status: " + binding.status_str(int(status.item())))
+                us = a.elapsed_time(b) / K * 1e3
+                # useful flops of the FFN; the default precision issues twice
+                # the MMAs (each weight meets the hi and the lo term)
+                tf = 2.0 * m * 3 * H * I / (us * 1e-6) / 1e12
+                key = f"{name}_m{m}" + ("" if pname == "split" else "_fp16")
+                out[key] = {"us_per_call": round(us, 1), "tflops": round(tf, 1),
+                            "tok_per_s": round(m / (us * 1e-6)), "peak_tflops": peak,
+                            "frac": round(tf / peak, 4), "bound": "tensor",
+                            "mma_tflops": round(tf * (2 if pname == "split" else 1), 1),
+                            "dtype": "fp16 x fp9->fp16, activations as hi + lo fp16 terms" if pname == "split"
+                            else "fp16 x fp9->fp16, one fp16 term per activation"}
         del f
         torch.cuda.empty_cache()
     return out

@@ -25,6 +25,9 @@ FP9_ERR_RANGE = 5
 FP9_ERR_CUDA = 6
 FP9_ERR_TIMEOUT = 7
 
+FP9_PREFILL_SPLIT = 0   # prefill activations as two fp16 terms (hi + lo): the default
+FP9_PREFILL_FP16 = 1    # one fp16 term per activation: faster, looser
+
 FP9_MAX_BSZ = 8
 FP9_MAX_HIDDEN = 7168
 FP9_MAX_PREFILL_TOKENS = 1048576
@@ -104,12 +107,12 @@ _SIGS = {
                                                ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "fp9_ffn_prefill": (ctypes.c_int, [ctypes.POINTER(FFNBankC), ctypes.c_int64, ctypes.c_void_p,
-                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
-                                       ctypes.c_void_p, ctypes.c_void_p]),
+                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(FFNBankC), ctypes.c_int64]),
     "fp9_moe_prefill": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_int64,
-                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                       ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_moe_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(MoELayerC), ctypes.c_int64]),
     "fp9_prefill_selftest_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                     ctypes.c_int32, ctypes.c_void_p]),
@@ -280,11 +283,12 @@ def prefill_workspace_bytes(ffn, m: int) -> int:
 
 
 def fp9_ffn_prefill(ffn, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, k: int = 0,
-                    status: torch.Tensor | None = None, stream=None) -> None:
+                    status: torch.Tensor | None = None, stream=None, precision: int = FP9_PREFILL_SPLIT) -> None:
     """y [m, hidden] = FFN k of the bank ``ffn`` applied to x [m, hidden]
-    (fp32), on the tensor cores (x and h rounded to fp16, fp32 accumulation)."""
-    _check(load().fp9_ffn_prefill(ctypes.byref(ffn.c_struct()), k, _ptr(x), x.shape[0], _ptr(y), _ptr(ws),
-                                  ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+    (fp32), on the tensor cores (x and h as two fp16 terms each by default,
+    or one with FP9_PREFILL_FP16; fp32 accumulation)."""
+    _check(load().fp9_ffn_prefill(ctypes.byref(ffn.c_struct()), k, _ptr(x), x.shape[0], _ptr(y), precision,
+                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
            "fp9_ffn_prefill")
 
 
@@ -294,11 +298,12 @@ def moe_prefill_workspace_bytes(layer, m: int) -> int:
 
 def fp9_moe_prefill(layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
                     status: torch.Tensor | None = None, ids: torch.Tensor | None = None,
-                    weights: torch.Tensor | None = None, stream=None) -> None:
+                    weights: torch.Tensor | None = None, stream=None, precision: int = FP9_PREFILL_SPLIT) -> None:
     """y [m, hidden] = the MoE layer applied to m tokens x (fp32) at once,
-    expert FFNs on the tensor cores (fp16 operands, fp32 accumulation)."""
+    expert FFNs on the tensor cores (activations as two fp16 terms by
+    default, or one with FP9_PREFILL_FP16; fp32 accumulation)."""
     _check(load().fp9_moe_prefill(ctypes.byref(layer.c_struct()), _ptr(x), x.shape[0], _ptr(y), _ptr(ids),
-                                  _ptr(weights), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                  _ptr(weights), precision, _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
                                   _stream(stream)), "fp9_moe_prefill")
 
 

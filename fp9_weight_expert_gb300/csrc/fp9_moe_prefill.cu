@@ -359,13 +359,17 @@ struct PermuteArgs {
     const int32_t* rank;     // [m, topk]
     const int32_t* row;      // [E + n_shared]
     int32_t m, H, topk, E, n_shared;
-    __half* x16;             // [rows, H]
+    __half* x16;             // [rows, H], or [rows, 2H] in the split layout
     int32_t* pos;            // [m, topk] the slot's row
     int32_t* status;
+    int32_t split;           // 1: two fp16 terms per value (hi, lo)
 };
 
 // Token t's fp16 row goes to the row of each of its slots and to row t of
 // each shared group. A value whose fp16 is not finite is a range error.
+// In the split layout each value is written as hi = fp16(v) and lo =
+// fp16(v - hi): 64-column chunk c of a row holds its hi terms in columns
+// [128 c, 128 c + 64) and its lo terms in the next 64.
 __global__ void __launch_bounds__(kRowThreads) permute_kernel(const PermuteArgs a) {
     __shared__ int32_t s_rows[FP9_MAX_TOPK + FP9_MAX_SHARED];
     grid_dependency_wait();
@@ -392,7 +396,22 @@ __global__ void __launch_bounds__(kRowThreads) permute_kernel(const PermuteArgs 
         o.y = *reinterpret_cast<const uint32_t*>(&h1);
         finite = finite && ((o.x & 0x7C00u) != 0x7C00u) && ((o.x & 0x7C000000u) != 0x7C000000u) &&
                  ((o.y & 0x7C00u) != 0x7C00u) && ((o.y & 0x7C000000u) != 0x7C000000u);
-        for (int r = 0; r < nr; ++r) reinterpret_cast<uint2*>(a.x16 + static_cast<int64_t>(s_rows[r]) * a.H)[c] = o;
+        if (a.split) {
+            const __half2 l0 = __floats2half2_rn(v.x - __low2float(h0), v.y - __high2float(h0));
+            const __half2 l1 = __floats2half2_rn(v.z - __low2float(h1), v.w - __high2float(h1));
+            uint2 l;
+            l.x = *reinterpret_cast<const uint32_t*>(&l0);
+            l.y = *reinterpret_cast<const uint32_t*>(&l1);
+            const int64_t col = 4 * static_cast<int64_t>(c);  // four columns inside one 64-column chunk
+            const int64_t sc = ((col >> 6) << 7) + (col & 63);
+            for (int r = 0; r < nr; ++r) {
+                __half* dst = a.x16 + static_cast<int64_t>(s_rows[r]) * 2 * a.H + sc;
+                *reinterpret_cast<uint2*>(dst) = o;
+                *reinterpret_cast<uint2*>(dst + 64) = l;
+            }
+        } else {
+            for (int r = 0; r < nr; ++r) reinterpret_cast<uint2*>(a.x16 + static_cast<int64_t>(s_rows[r]) * a.H)[c] = o;
+        }
     }
     if (!finite) record_status(a.status, FP9_ERR_RANGE);
 }
@@ -498,10 +517,12 @@ MoePrefillLayout moe_prefill_layout(const fp9_moe_layer* L, int64_t m) {
     off = align_up(off + sizeof(int32_t) * G);
     W.off_mtile = off;
     off = align_up(off + sizeof(int32_t) * (G + 1));
+    // x and h in the split layout (two fp16 terms per value; the one-term
+    // mode uses the first half of each)
     W.off_x16 = off;
-    off = align_up(off + sizeof(__half) * W.rows * H);
+    off = align_up(off + 2 * sizeof(__half) * W.rows * H);
     W.off_h = off;
-    off = align_up(off + sizeof(__half) * W.rows * I);
+    off = align_up(off + 2 * sizeof(__half) * W.rows * I);
     W.off_y = off;
     off = align_up(off + sizeof(float) * W.rows * H);
     W.total = off;
@@ -528,10 +549,12 @@ extern "C" size_t fp9_moe_prefill_workspace_bytes(const fp9_moe_layer* layer, in
 }
 
 extern "C" fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x, int64_t m, float* y,
-                                      int32_t* ids, float* weights, void* ws, size_t ws_bytes, int32_t* d_status,
-                                      void* stream) {
+                                      int32_t* ids, float* weights, int32_t precision, void* ws, size_t ws_bytes,
+                                      int32_t* d_status, void* stream) {
     fp9_status st = check_moe_prefill(layer, m);
     if (st != FP9_OK) return st;
+    FP9_CHECK_ARG(precision == FP9_PREFILL_SPLIT || precision == FP9_PREFILL_FP16, FP9_ERR_INVALID_ARG);
+    const bool split = precision == FP9_PREFILL_SPLIT;
     if (m == 0) return FP9_OK;
     FP9_CHECK_ARG(x != nullptr && y != nullptr && ws != nullptr, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(x, 16) && aligned(y, 16) && aligned(ws, kAlign), FP9_ERR_ALIGN);
@@ -577,12 +600,12 @@ extern "C" fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x
     RankArgs ra{ids_ws, mi, K, E, S, rank, cnt, row, mtile, reinterpret_cast<uint32_t*>(w + W.off_ticket)};
     FP9_CUDA_TRY(launch_pdl(rank_kernel, dim3(E), dim3(kRankThreads), 0, s, ra));
 
-    PermuteArgs pa{x, ids_ws, rank, row, mi, H, K, E, S, x16, pos, d_status};
+    PermuteArgs pa{x, ids_ws, rank, row, mi, H, K, E, S, x16, pos, d_status, split ? 1 : 0};
     FP9_CUDA_TRY(launch_pdl(permute_kernel, dim3(mi), dim3(kRowThreads), 0, s, pa));
 
     GroupTableDev tab{row, cnt, mtile, E + S, E};
     st = launch_grouped_ffn(layer->routed, S > 0 ? &layer->shared : nullptr, tab, W.max_mtiles, x16, h, yrows, W.rows,
-                            d_status, sms, s);
+                            split, d_status, sms, s);
     if (st != FP9_OK) return st;
 
     CombineArgs ca{yrows, pos, wts_ws, row, mi, H, K, E, S, y};

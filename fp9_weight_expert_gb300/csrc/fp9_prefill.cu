@@ -96,15 +96,27 @@ constexpr uint32_t kMnGroupStride = 4096;
 // Ring depths. 128-token tiles: three activation slots, two decoded slots,
 // three raw slots (two in flight while one is decoded: four 64-wide chunks
 // of weights). 256-token tiles (twice the MMA time per chunk): two of each.
-template <int MH>
+// Split activations (kSplit: each activation is carried as two fp16 terms,
+// hi + lo, and every weight chunk meets both, so a chunk has twice the MMA
+// work): 128-token tiles whose activation slot holds the hi and the lo
+// tile, two slots of each ring.
+template <int MH, bool kSplit = false>
 struct Cfg {
-    static constexpr int kASlotBytes = MH * kTileBytes;
-    static constexpr int kASlots = MH == 1 ? 3 : 2;
+    static_assert(!kSplit || MH == 1, "split activations use 128-token tiles");
+    static constexpr int kASlotBytes = (kSplit ? 2 : 1) * MH * kTileBytes;
+    static constexpr int kASlots = (MH == 1 && !kSplit) ? 3 : 2;
     static constexpr int kBSlots = 2;
-    static constexpr int kRawSlots = MH == 1 ? 3 : 2;
+    static constexpr int kRawSlots = (MH == 1 && !kSplit) ? 3 : 2;
     static constexpr int kSmem = 1024 + kCtlBytes + kASlots * kASlotBytes + kBSlots * kBSlot + kRawSlots * kRawSlot;
     static_assert(kSmem <= kSmemMax, "shared memory");
 };
+
+// Split layout of an fp16 activation matrix with K columns: [rows, 2K],
+// each 64-column chunk c of K stored as 128 columns, its hi terms in
+// [128 c, 128 c + 64) and its lo terms in [128 c + 64, 128 c + 128), where
+// hi = fp16(v) and lo = fp16(v - hi) (both round to nearest even). Column
+// j's hi term:
+__host__ __device__ __forceinline__ int64_t split_col(int64_t j) { return ((j >> 6) << 7) + (j & 63); }
 
 struct Ctl {
     uint64_t a_full[8], a_empty[8];   // activation ring: TMA bytes / MMA commit
@@ -312,10 +324,10 @@ __device__ __forceinline__ Tile tile_at(const PrefillArgs& p, int L) {
 // and the epilogue warps read tile j's while the MMAs of tile j + 1 fill the
 // other. Timed per CTA, a one-tile grouped CTA spent 3.7 us before its
 // first MMA, 2.4 us in its epilogue and 1 us between CTAs out of 25.9.
-template <bool kDown, int MH, bool kGrouped>
+template <bool kDown, int MH, bool kGrouped, bool kSplit>
 __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillArgs p) {
-    using C = Cfg<MH>;
+    using C = Cfg<MH, kSplit>;
     static_assert(!kGrouped || MH == 1, "grouped tiles are 128 rows");
     constexpr int kAcc = kGrouped ? 2 : 1;                // accumulators
     constexpr uint32_t kAccCols = MH * 2 * kNR;           // TMEM columns of one
@@ -387,24 +399,34 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
             const int64_t grow = static_cast<int64_t>(t.arow0) + r;
             const bool valid = r < t.nvalid;
             if (!kDown) {
-                __half* out = static_cast<__half*>(p.out) + t.part * p.part_stride + grow * p.ldo + t.n0;
+                __half* out = static_cast<__half*>(p.out) + t.part * p.part_stride + grow * p.ldo;
 #pragma unroll 1
                 for (int cb = first; cb < kNR / 16; cb += step) {
                     float g[16], u[16];
                     tc_ld16(tl + (mh * 2 + 0) * kNR + cb * 16, g);
                     tc_ld16(tl + (mh * 2 + 1) * kNR + cb * 16, u);
-                    uint32_t hw[8];
+                    uint32_t hw[8], lw[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const __half2 h2 =
-                            __floats2half2_rn(silu(g[2 * i]) * u[2 * i], silu(g[2 * i + 1]) * u[2 * i + 1]);
+                        const float h0 = silu(g[2 * i]) * u[2 * i], h1 = silu(g[2 * i + 1]) * u[2 * i + 1];
+                        const __half2 h2 = __floats2half2_rn(h0, h1);
                         hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
                         bad = bad || (valid && !half2_finite(hw[i]));
+                        if (kSplit) {
+                            const __half2 l2 = __floats2half2_rn(h0 - __low2float(h2), h1 - __high2float(h2));
+                            lw[i] = *reinterpret_cast<const uint32_t*>(&l2);
+                        }
                     }
                     if (valid) {
-                        uint4* o = reinterpret_cast<uint4*>(out + cb * 16);
+                        const int64_t col = t.n0 + cb * 16;  // 16 columns inside one 64-column chunk
+                        uint4* o = reinterpret_cast<uint4*>(out + (kSplit ? split_col(col) : col));
                         o[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                         o[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                        if (kSplit) {
+                            uint4* ol = reinterpret_cast<uint4*>(out + split_col(col) + 64);
+                            ol[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                            ol[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                        }
                     }
                 }
             } else {
@@ -444,10 +466,16 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
                     }
                     const uint32_t bar = smem_addr(&ctl.a_full[s]);
                     mbar_arrive_expect_tx(bar, C::kASlotBytes);
+                    if (kSplit) {  // the chunk's hi tile, then its lo tile
+                        tma_load_2d(ringA + s * C::kASlotBytes, &maps.act, (t.c0 + kc) * 2 * kChunkK, t.arow0, bar);
+                        tma_load_2d(ringA + s * C::kASlotBytes + kTileBytes, &maps.act,
+                                    (t.c0 + kc) * 2 * kChunkK + kChunkK, t.arow0, bar);
+                    } else {
 #pragma unroll
-                    for (int mh = 0; mh < MH; ++mh)
-                        tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act,
-                                    (t.c0 + kc) * kChunkK, t.arow0 + mh * kTileRows, bar);
+                        for (int mh = 0; mh < MH; ++mh)
+                            tma_load_2d(ringA + s * C::kASlotBytes + mh * kTileBytes, &maps.act,
+                                        (t.c0 + kc) * kChunkK, t.arow0 + mh * kTileRows, bar);
+                    }
                     ++ka;
                 }
             }
@@ -537,10 +565,15 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
                         const uint64_t bd = kDown ? tc_desc_sw128_mn(sB + 2u * kMnGroupStride * k16, kMnAtomStride,
                                                                      kMnGroupStride)
                                                   : tc_desc_sw128(sB + 32u * k16);
+                        if (kSplit) {  // the hi and the lo terms into the same accumulator
+                            tc_mma_f16(d, tc_desc_sw128(sA + 32u * k16), bd, idesc, kc > 0 || k16 > 0);
+                            tc_mma_f16(d, tc_desc_sw128(sA + kTileBytes + 32u * k16), bd, idesc, true);
+                        } else {
 #pragma unroll
-                        for (int mh = 0; mh < MH; ++mh) {
-                            const uint64_t ad = tc_desc_sw128(sA + mh * kTileBytes + 32u * k16);
-                            tc_mma_f16(d + mh * 2 * kNR, ad, bd, idesc, kc > 0 || k16 > 0);
+                            for (int mh = 0; mh < MH; ++mh) {
+                                const uint64_t ad = tc_desc_sw128(sA + mh * kTileBytes + 32u * k16);
+                                tc_mma_f16(d + mh * 2 * kNR, ad, bd, idesc, kc > 0 || k16 > 0);
+                            }
                         }
                     }
                     tc_commit(smem_addr(&ctl.a_empty[sa]));
@@ -630,7 +663,13 @@ __global__ void __launch_bounds__(kGrouped ? kGroupedThreads : kThreads, 1)
 // TMEM (512 columns): D_gate [0, 128), D_up [128, 256) (lane = weight row,
 // column = token), then 4 slots of decoded weights of 64 K columns: gate in
 // the first 32 columns, up in the next 32.
+// Split activations: up to 64 tokens per tile; an activation slot holds
+// the tile's hi rows (slot rows [0, 64)) and its lo rows (rows [64, 128)),
+// and one MMA of N = 64 + the valid tokens rounded up to 16 takes both, so
+// D column c < 64 is token c's hi part and column 64 + c its lo part
+// (added in the epilogue): the same MMA count as with one fp16 term.
 constexpr int kGuTokens = 128;
+constexpr int kGuTokensSplit = 64;
 constexpr int kGuActSlots = 4, kGuRawSlots = 4, kGuWSlots = 4;
 constexpr int kGuActSlot = kGuTokens * kChunkK * 2;  // 16 KiB
 constexpr int kGuSmem = 1024 + kCtlBytes + kGuActSlots * kGuActSlot + kGuRawSlots * kRawSlot;
@@ -673,9 +712,16 @@ struct GuTile {
     bool shared_bank;
 };
 
+// With split activations each 128-row m-tile of the group table is two
+// 64-token tiles (the second one empty, nvalid <= 0, when the m-tile holds
+// at most 64 tokens; every role skips empty tiles alike).
+template <bool kSplit>
 __device__ __forceinline__ GuTile gu_tile_at(const PrefillArgs& p, int L) {
+    constexpr int kT = kSplit ? kGuTokensSplit : kGuTokens;
+    constexpr int kPer = kPrefillTileRows / kT;
     GuTile t;
-    const int q = L / p.ntiles, nt = L - q * p.ntiles;
+    const int qq = L / p.ntiles, nt = L - qq * p.ntiles;
+    const int q = qq / kPer, half = qq - q * kPer;
     int lo = 0, hi = p.n_groups - 1;  // the last group whose first m-tile is <= q
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -683,12 +729,13 @@ __device__ __forceinline__ GuTile gu_tile_at(const PrefillArgs& p, int L) {
         else hi = mid - 1;
     }
     const int mt = q - __ldg(p.g_mtile + lo);
-    t.arow0 = __ldg(p.g_row + lo) + mt * kGuTokens;
-    t.nvalid = __ldg(p.g_cnt + lo) - mt * kGuTokens;
+    t.arow0 = __ldg(p.g_row + lo) + mt * kPrefillTileRows + half * kT;
+    t.nvalid = __ldg(p.g_cnt + lo) - mt * kPrefillTileRows - half * kT;
     t.shared_bank = lo >= p.n_routed;
     t.wrow0 = (t.shared_bank ? lo - p.n_routed : lo) * p.inter;
     t.n0 = nt * kNR;
-    t.n_mma = static_cast<uint32_t>((min(t.nvalid, kGuTokens) + 15) / 16 * 16);
+    const uint32_t n16 = static_cast<uint32_t>((max(min(t.nvalid, kT), 0) + 15) / 16 * 16);
+    t.n_mma = kSplit ? kT + n16 : n16;
     return t;
 }
 
@@ -697,12 +744,12 @@ __device__ __forceinline__ GuTile gu_tile_at(const PrefillArgs& p, int L) {
 // weight loads land while the current tile's MMAs and epilogue run. D (both
 // accumulators) is read out by the decoder warps after the tile's last
 // MMA; the next tile's MMAs wait until it has been (acc_empty).
-template <bool kGrouped>
+template <bool kGrouped, bool kSplit>
 __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_constant__ PrefillMaps maps,
                                                              const PrefillArgs p) {
     static_assert(kGrouped, "the gate/up kernel with weights in TMEM serves the grouped launch");
     grid_dependency_wait();  // the group table comes from the previous launches
-    const int total = __ldg(p.g_mtile + p.n_groups) * p.ntiles;
+    const int total = __ldg(p.g_mtile + p.n_groups) * p.ntiles * (kSplit ? kPrefillTileRows / kGuTokensSplit : 1);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw0 = smem_addr(smem_raw);
     const uint32_t base = (raw0 + 1023u) & ~1023u;
@@ -753,7 +800,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
             int ka = 0;  // chunks issued, over all tiles
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-                const GuTile t = gu_tile_at(p, L);
+                const GuTile t = gu_tile_at<kSplit>(p, L);
+                if (t.nvalid <= 0) continue;
                 for (int kc = 0; kc < nk; ++kc) {
                     const int s = ka % kGuActSlots;
                     if (ka >= kGuActSlots &&
@@ -765,7 +813,13 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
                     }
                     const uint32_t bar = smem_addr(&ctl.a_full[s]);
                     mbar_arrive_expect_tx(bar, kGuActSlot);
-                    tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * kChunkK, t.arow0, bar);
+                    if (kSplit) {  // 64 hi rows, then 64 lo rows (boxes of 64 rows)
+                        tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * 2 * kChunkK, t.arow0, bar);
+                        tma_load_2d(ringA + s * kGuActSlot + kGuTokensSplit * 128, &maps.act, kc * 2 * kChunkK + kChunkK,
+                                    t.arow0, bar);
+                    } else {
+                        tma_load_2d(ringA + s * kGuActSlot, &maps.act, kc * kChunkK, t.arow0, bar);
+                    }
                     ++ka;
                 }
             }
@@ -780,7 +834,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
             int kw = 0;  // raw chunks issued, over all tiles
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
-                const GuTile t = gu_tile_at(p, L);
+                const GuTile t = gu_tile_at<kSplit>(p, L);
+                if (t.nvalid <= 0) continue;
                 const CUtensorMap* bmap = t.shared_bank ? maps.body_sh : maps.body;
                 const CUtensorMap* smap = t.shared_bank ? maps.sign_sh : maps.sign;
                 for (int kr = 0; kr < nk / 2; ++kr) {
@@ -818,8 +873,10 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
         if (lane == 0) {
             int kg = 0, j = 0;  // chunks and tiles consumed
             bool ok = true;
-            for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++j) {
-                const uint32_t idesc = tc_idesc_f16(kTileRows, gu_tile_at(p, L).n_mma);
+            for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+                const GuTile t = gu_tile_at<kSplit>(p, L);
+                if (t.nvalid <= 0) continue;
+                const uint32_t idesc = tc_idesc_f16(kTileRows, t.n_mma);
                 // the previous tile's D has been read out
                 if (j > 0 && !mbar_wait_bounded(smem_addr(&ctl.acc_empty[0]), (j - 1) & 1, p.timeout_ns, &ctl.abort)) {
                     fail(ctl, p.status);
@@ -848,6 +905,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
                     tc_commit(smem_addr(&ctl.b_empty[sw]));
                 }
                 if (ok) tc_commit(smem_addr(&ctl.acc_full[0]));
+                ++j;
             }
             tc_commit(smem_addr(&ctl.done));
             if (!mbar_wait_bounded(smem_addr(&ctl.done), 0, p.timeout_ns, &ctl.never))
@@ -864,7 +922,9 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
         const uint32_t tlane = tmem + ((32u * q) << 16);
         bool ok = true, bad = false;
         int kw = 0, j = 0;  // raw chunks and tiles, over all tiles
-        for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++j) {
+        for (int L = blockIdx.x; L < total && ok; L += gridDim.x) {
+            const GuTile t = gu_tile_at<kSplit>(p, L);
+            if (t.nvalid <= 0) continue;
             // both 64-wide chunks of a raw slot per iteration: two TMEM
             // stores, then one wait for their completion
             for (int kr = 0; kr < nk / 2 && ok; ++kr, ++kw) {
@@ -899,24 +959,48 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(const __grid_cons
             // + [0, 32); h[token, n0 + row] = SiLU(gate) * up, 32 lanes
             // writing 32 consecutive intermediate columns of a token row
             ok = warp_wait(smem_addr(&ctl.acc_full[0]), j & 1, p.timeout_ns, &ctl.abort);
+            ++j;
             if (!ok) break;
             tc_fence_after();
-            const GuTile t = gu_tile_at(p, L);
             const int cb = static_cast<int>(sel);
             float g[32], u[32];
-            tc_ld32(tlane + cb * 32, g);
-            tc_ld32(tlane + kNR + cb * 32, u);
+            if (!kSplit) {
+                tc_ld32(tlane + cb * 32, g);
+                tc_ld32(tlane + kNR + cb * 32, u);
+            } else if (cb < 2) {  // tokens 32 cb + [0, 32): hi part + lo part
+                tc_ld32(tlane + cb * 32, g);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float a[16];
+                    tc_ld16(tlane + kGuTokensSplit + cb * 32 + hb * 16, a);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) g[hb * 16 + i] += a[i];
+                }
+                tc_ld32(tlane + kNR + cb * 32, u);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float a[16];
+                    tc_ld16(tlane + kNR + kGuTokensSplit + cb * 32 + hb * 16, a);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) u[hb * 16 + i] += a[i];
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[0]));  // D may be overwritten now
-            __half* out = static_cast<__half*>(p.out) + t.n0 + row;
+            if (kSplit && cb >= 2) continue;
+            const int64_t col = t.n0 + row;
+            __half* out = static_cast<__half*>(p.out) + (kSplit ? split_col(col) : col);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int tk = cb * 32 + i;
                 if (tk < t.nvalid) {
-                    const __half hv = __float2half_rn(silu(g[i]) * u[i]);
+                    const float hf = silu(g[i]) * u[i];
+                    const __half hv = __float2half_rn(hf);
                     bad = bad || __hisinf(hv) || __hisnan(hv);
-                    out[(static_cast<int64_t>(t.arow0) + tk) * p.ldo] = hv;
+                    __half* o = out + (static_cast<int64_t>(t.arow0) + tk) * p.ldo;
+                    o[0] = hv;
+                    if (kSplit) o[64] = __float2half_rn(hf - __half2float(hv));
                 }
             }
         }
@@ -945,6 +1029,35 @@ __global__ void to_half_kernel(const float4* __restrict__ x, uint2* __restrict__
         o.y = *reinterpret_cast<const uint32_t*>(&b);
         finite = finite && half2_finite(o.x) && half2_finite(o.y);
         h[i] = o;
+    }
+    if (!finite) record_status(status, FP9_ERR_RANGE);
+}
+
+// x fp32 [rows, H] -> the split layout [rows, 2H] (hi = fp16(v), lo =
+// fp16(v - hi), both round to nearest even); a value whose hi is not
+// finite is recorded as FP9_ERR_RANGE. H4 = H / 4; four consecutive
+// columns stay inside one 64-column chunk.
+__global__ void to_half_split_kernel(const float4* __restrict__ x, __half* __restrict__ h, int64_t n4, int64_t H4,
+                                     int32_t* status) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    bool finite = true;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 v = x[i];
+        const int64_t r = i / H4, c = 4 * (i - r * H4);
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        const __half2 la = __floats2half2_rn(v.x - __low2float(a), v.y - __high2float(a));
+        const __half2 lb = __floats2half2_rn(v.z - __low2float(b), v.w - __high2float(b));
+        uint2 o, l;
+        o.x = *reinterpret_cast<const uint32_t*>(&a);
+        o.y = *reinterpret_cast<const uint32_t*>(&b);
+        l.x = *reinterpret_cast<const uint32_t*>(&la);
+        l.y = *reinterpret_cast<const uint32_t*>(&lb);
+        finite = finite && half2_finite(o.x) && half2_finite(o.y);
+        __half* dst = h + r * 8 * H4 + split_col(c);
+        *reinterpret_cast<uint2*>(dst) = o;
+        *reinterpret_cast<uint2*>(dst + 64) = l;
     }
     if (!finite) record_status(status, FP9_ERR_RANGE);
 }
@@ -991,10 +1104,10 @@ int choose_mh(int64_t m, int64_t ntiles, int sms) {
     return waves(2) * 1.8 <= waves(1) ? 2 : 1;
 }
 
-template <bool kDown, int MH, bool kGrouped>
+template <bool kDown, int MH, bool kGrouped, bool kSplit>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(prefill_kernel<kDown, MH, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<MH>::kSmem);
+    return cudaFuncSetAttribute(prefill_kernel<kDown, MH, kGrouped, kSplit>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MH, kSplit>::kSmem);
 }
 
 fp9_status ensure_attrs() {
@@ -1002,12 +1115,19 @@ fp9_status ensure_attrs() {
     return attr.run([] {
         const int optin = device_max_smem_optin();
         if (optin < Cfg<1>::kSmem || optin < Cfg<2>::kSmem) return FP9_ERR_CUDA;
-        FP9_CUDA_TRY((set_smem_attr<false, 1, false>()));
-        FP9_CUDA_TRY((set_smem_attr<false, 2, false>()));
-        FP9_CUDA_TRY((set_smem_attr<true, 1, false>()));
-        FP9_CUDA_TRY((set_smem_attr<true, 2, false>()));
-        FP9_CUDA_TRY((set_smem_attr<true, 1, true>()));
-        FP9_CUDA_TRY(cudaFuncSetAttribute(gateup_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGuSmem));
+        if (optin < Cfg<1, true>::kSmem || optin < kGuSmem) return FP9_ERR_CUDA;
+        FP9_CUDA_TRY((set_smem_attr<false, 1, false, false>()));
+        FP9_CUDA_TRY((set_smem_attr<false, 2, false, false>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, false, false>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 2, false, false>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, true, false>()));
+        FP9_CUDA_TRY((set_smem_attr<false, 1, false, true>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, false, true>()));
+        FP9_CUDA_TRY((set_smem_attr<true, 1, true, true>()));
+        FP9_CUDA_TRY((cudaFuncSetAttribute(gateup_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kGuSmem)));
+        FP9_CUDA_TRY((cudaFuncSetAttribute(gateup_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kGuSmem)));
         return FP9_OK;
     });
 }
@@ -1050,9 +1170,11 @@ bool make_gateup_maps(const uint8_t* const body[2], const uint8_t* const sign[2]
     return true;
 }
 
-bool make_act_map(CUtensorMap* map, const __half* act, int64_t rows, int64_t K) {
-    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
-                    static_cast<uint64_t>(K) * 2, kChunkK, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+// Activations fp16 [rows, cols] (cols = K, or 2K in the split layout),
+// boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+bool make_act_map(CUtensorMap* map, const __half* act, int64_t rows, int64_t cols, uint32_t box_rows = kTileRows) {
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                    static_cast<uint64_t>(cols) * 2, kChunkK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 PrefillArgs base_args(int64_t m, int64_t K, int32_t ntiles, void* out, int64_t ldo, int32_t* status) {
@@ -1084,17 +1206,18 @@ struct DownPlan {
     int mh, splits;
 };
 
-DownPlan plan_down(int64_t m, int64_t H, int64_t I, int sms) {
+DownPlan plan_down(int64_t m, int64_t H, int64_t I, int sms, bool split) {
     const int64_t ntiles = H / (2 * kNR);
-    if (sms <= 0) return DownPlan{choose_mh(m, ntiles, 1), 1};
+    if (sms <= 0) return DownPlan{split ? 1 : choose_mh(m, ntiles, 1), 1};
     DownPlan best{1, 1};
     double best_cost = 1e300;
-    for (int mh = 1; mh <= 2; ++mh) {
+    for (int mh = 1; mh <= (split ? 1 : 2); ++mh) {
         const int64_t mt = (m + kTileRows * mh - 1) / (kTileRows * mh);
         for (int sp = 1; sp <= kMaxDownSplits && sp <= I / kRawK; ++sp) {
             const int64_t ctas = mt * ntiles * sp;
             const double rounds = static_cast<double>((ctas + sms - 1) / sms);
-            const double tile = 2.0 * static_cast<double>(I) / sp * 65536.0 / 9.2e12 / (mh == 2 ? 1.0 : 1.8);
+            const double tile =
+                (split ? 2.0 : 1.0) * 2.0 * static_cast<double>(I) / sp * 65536.0 / 9.2e12 / (mh == 2 ? 1.0 : 1.8);
             const double sum = sp > 1 ? (sp + 1.0) * static_cast<double>(m) * static_cast<double>(H) * 4.0 / 6.5e12 : 0.0;
             const double cost = rounds * (tile + 5e-6) + sum;
             if (cost < 0.97 * best_cost) {
@@ -1132,18 +1255,19 @@ __global__ void __launch_bounds__(256) sum_parts_kernel(const float4* __restrict
 // body/sign[0] = down_t, `ncols` = hidden). A down GEMM whose plan splits K
 // writes its parts to `parts` ([splits, m, ncols] fp32) and adds them into
 // out (ldo == ncols) with a second launch.
-fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const uint8_t* const body[2],
+fp9_status launch_gemm(bool down, bool split, const __half* act, int64_t m, int64_t K, const uint8_t* const body[2],
                        const uint8_t* const sign[2], int64_t plane_rows, int64_t hidden, int64_t wrow0, int64_t ncols,
                        void* out, int64_t ldo, float* parts, int32_t* status, int sms, cudaStream_t stream) {
     const int32_t ntiles = static_cast<int32_t>(ncols / (down ? 2 * kNR : kNR));
     PrefillMaps maps;
-    if (!make_act_map(&maps.act, act, m, K) || !make_weight_maps(down, body, sign, plane_rows, hidden, maps.body, maps.sign))
+    if (!make_act_map(&maps.act, act, m, split ? 2 * K : K) ||
+        !make_weight_maps(down, body, sign, plane_rows, hidden, maps.body, maps.sign))
         return FP9_ERR_CUDA;
     maps.body_sh[0] = maps.body_sh[1] = maps.body[0];
     maps.sign_sh[0] = maps.sign_sh[1] = maps.sign[0];
     PrefillArgs p = base_args(m, K, ntiles, out, ldo, status);
     p.wrow0 = static_cast<int32_t>(wrow0);
-    const DownPlan plan = down ? plan_down(m, ncols, K, sms) : DownPlan{choose_mh(m, ntiles, sms), 1};
+    const DownPlan plan = down ? plan_down(m, ncols, K, sms, split) : DownPlan{split ? 1 : choose_mh(m, ntiles, sms), 1};
     const int mh = plan.mh;
     if (plan.splits > 1) {
         if (parts == nullptr || ldo != ncols) return FP9_ERR_WORKSPACE;
@@ -1155,9 +1279,10 @@ fp9_status launch_gemm(bool down, const __half* act, int64_t m, int64_t K, const
     const int64_t ctas = static_cast<int64_t>(p.mtiles) * p.ntiles * p.ksplit;  // one CTA per tile and K part
     if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
     void (*k)(const PrefillMaps, const PrefillArgs) =
-        down ? (mh == 2 ? prefill_kernel<true, 2, false> : prefill_kernel<true, 1, false>)
-             : (mh == 2 ? prefill_kernel<false, 2, false> : prefill_kernel<false, 1, false>);
-    const int smem = mh == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem;
+        split ? (down ? prefill_kernel<true, 1, false, true> : prefill_kernel<false, 1, false, true>)
+        : down ? (mh == 2 ? prefill_kernel<true, 2, false, false> : prefill_kernel<true, 1, false, false>)
+               : (mh == 2 ? prefill_kernel<false, 2, false, false> : prefill_kernel<false, 1, false, false>);
+    const int smem = split ? Cfg<1, true>::kSmem : mh == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem;
     FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, maps, p));
     if (plan.splits > 1) {
         const int64_t n4 = m * ncols / 4;
@@ -1172,17 +1297,20 @@ struct PrefillLayout {
     size_t off_x16 = 0, off_h = 0, off_parts = 0, total = 0;
 };
 
-// x and h as fp16, then the K parts of the down GEMM when its plan splits
-// K (sms: the device's SMs; <= 0: no split).
+// x and h in the split layout (two fp16 terms per value; the one-term
+// mode uses the first half of each), then the K parts of the down GEMM
+// when either mode's plan splits K (sms: the device's SMs; <= 0: no split).
 PrefillLayout prefill_layout(int64_t m, int64_t hidden, int64_t inter, int sms) {
     PrefillLayout L;
     L.off_x16 = 0;
-    L.off_h = align_up(sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(hidden));
-    L.off_parts = L.off_h + align_up(sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(inter));
-    const DownPlan plan = plan_down(m, hidden, inter, sms);
-    L.total = L.off_parts + (plan.splits > 1 ? align_up(sizeof(float) * static_cast<size_t>(plan.splits) *
-                                                         static_cast<size_t>(m) * static_cast<size_t>(hidden))
-                                             : 0);
+    L.off_h = align_up(2 * sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(hidden));
+    L.off_parts = L.off_h + align_up(2 * sizeof(__half) * static_cast<size_t>(m) * static_cast<size_t>(inter));
+    int splits = plan_down(m, hidden, inter, sms, false).splits;
+    const int s2 = plan_down(m, hidden, inter, sms, true).splits;
+    if (s2 > splits) splits = s2;
+    L.total = L.off_parts + (splits > 1 ? align_up(sizeof(float) * static_cast<size_t>(splits) *
+                                                    static_cast<size_t>(m) * static_cast<size_t>(hidden))
+                                        : 0);
     return L;
 }
 
@@ -1197,7 +1325,7 @@ fp9_status check_prefill_bank(const fp9_ffn_bank* f, int64_t index) {
 }  // namespace
 
 fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* shared, const GroupTableDev& tab,
-                              int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows,
+                              int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows, bool split,
                               int32_t* status, int sms, cudaStream_t stream) {
     const int64_t H = routed.hidden, I = routed.inter;
     if (max_mtiles <= 0 || rows <= 0) return FP9_OK;
@@ -1212,7 +1340,10 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
                            CUtensorMap* sm) {
             return down ? make_weight_maps(true, bb, ss, rows_, H, bm, sm) : make_gateup_maps(bb, ss, rows_, H, bm, sm);
         };
-        if (!make_act_map(&maps.act, down ? h : x16, rows, down ? I : H) ||
+        const int64_t K = down ? I : H;
+        // split gate/up tiles load 64 hi rows and 64 lo rows
+        const uint32_t box_rows = (split && !down) ? kGuTokensSplit : kTileRows;
+        if (!make_act_map(&maps.act, down ? h : x16, rows, split ? 2 * K : K, box_rows) ||
             !maps_of(rb, rs, routed.n * I, maps.body, maps.sign))
             return FP9_ERR_CUDA;
         if (shared != nullptr && shared->n > 0) {
@@ -1227,7 +1358,7 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         }
         const int32_t ntiles = static_cast<int32_t>(down ? H / (2 * kNR) : I / kNR);
         PrefillArgs p = base_args(rows, down ? I : H, ntiles, down ? static_cast<void*>(y) : static_cast<void*>(h),
-                                  down ? H : I, status);
+                                  down ? H : (split ? 2 * I : I), status);
         p.g_row = tab.row;
         p.g_cnt = tab.cnt;
         p.g_mtile = tab.mtile;
@@ -1238,9 +1369,11 @@ fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* sh
         if (ctas > 0x7FFFFFFF) return FP9_ERR_SHAPE;
         // a persistent grid of one CTA per SM walks the tiles
         if (ctas > sms) ctas = sms;
-        void (*k)(const PrefillMaps, const PrefillArgs) = down ? prefill_kernel<true, 1, true> : gateup_kernel<true>;
+        void (*k)(const PrefillMaps, const PrefillArgs) =
+            down ? (split ? prefill_kernel<true, 1, true, true> : prefill_kernel<true, 1, true, false>)
+                 : (split ? gateup_kernel<true, true> : gateup_kernel<true, false>);
         FP9_CUDA_TRY(launch_pdl(k, dim3(static_cast<unsigned>(ctas)), dim3(down ? kGroupedThreads : kGuThreads),
-                                down ? Cfg<1>::kSmem : kGuSmem, stream, maps, p));
+                                down ? (split ? Cfg<1, true>::kSmem : Cfg<1>::kSmem) : kGuSmem, stream, maps, p));
     }
     return FP9_OK;
 }
@@ -1255,10 +1388,13 @@ extern "C" size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m
 }
 
 extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, const float* x, int64_t m,
-                                      float* y, void* ws, size_t ws_bytes, int32_t* d_status, void* stream) {
+                                      float* y, int32_t precision, void* ws, size_t ws_bytes, int32_t* d_status,
+                                      void* stream) {
     fp9_status st = check_prefill_bank(ffn, index);
     if (st != FP9_OK) return st;
     FP9_CHECK_ARG(m >= 0 && m <= FP9_MAX_PREFILL_TOKENS, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(precision == FP9_PREFILL_SPLIT || precision == FP9_PREFILL_FP16, FP9_ERR_INVALID_ARG);
+    const bool split = precision == FP9_PREFILL_SPLIT;
     if (m == 0) return FP9_OK;
     FP9_CHECK_ARG(x != nullptr && y != nullptr && ws != nullptr, FP9_ERR_INVALID_ARG);
     FP9_CHECK_ARG(aligned(x, 16) && aligned(y, 16) && aligned(ws, 256), FP9_ERR_ALIGN);
@@ -1277,18 +1413,23 @@ extern "C" fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t index, co
 
     const int64_t n4 = m * H / 4;
     const int64_t blocks = (n4 + 255) / 256 < static_cast<int64_t>(sms) * 8 ? (n4 + 255) / 256 : sms * 8;
-    FP9_CUDA_TRY(launch_pdl(to_half_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                            reinterpret_cast<const float4*>(x), reinterpret_cast<uint2*>(x16), n4, d_status));
+    if (split)
+        FP9_CUDA_TRY(launch_pdl(to_half_split_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                                reinterpret_cast<const float4*>(x), x16, n4, H / 4, d_status));
+    else
+        FP9_CUDA_TRY(launch_pdl(to_half_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                                reinterpret_cast<const float4*>(x), reinterpret_cast<uint2*>(x16), n4, d_status));
 
     // the maps cover FFN `index` only (rows [0, inter) of its planes)
     const size_t wg = static_cast<size_t>(index) * static_cast<size_t>(I) * static_cast<size_t>(H);
     const uint8_t* gu_body[2] = {ffn->gate_body + wg, ffn->up_body + wg};
     const uint8_t* gu_sign[2] = {ffn->gate_sign + wg / 8, ffn->up_sign + wg / 8};
-    st = launch_gemm(false, x16, m, H, gu_body, gu_sign, I, H, 0, I, h, I, nullptr, d_status, sms, s);
+    st = launch_gemm(false, split, x16, m, H, gu_body, gu_sign, I, H, 0, I, h, split ? 2 * I : I, nullptr, d_status,
+                     sms, s);
     if (st != FP9_OK) return st;
     const uint8_t* d_body[2] = {ffn->down_body + wg, ffn->down_body + wg};
     const uint8_t* d_sign[2] = {ffn->down_sign + wg / 8, ffn->down_sign + wg / 8};
-    return launch_gemm(true, h, m, I, d_body, d_sign, I, H, 0, H, y, H, parts, d_status, sms, s);
+    return launch_gemm(true, split, h, m, I, d_body, d_sign, I, H, 0, H, y, H, parts, d_status, sms, s);
 }
 
 extern "C" fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes, int32_t* d_status, int32_t timeout_us,
@@ -1318,7 +1459,7 @@ extern "C" fp9_status fp9_prefill_selftest_timeout(void* ws, size_t ws_bytes, in
     p.mtiles = 1;
     p.no_copy = 1;
     p.timeout_ns = static_cast<uint64_t>(timeout_us) * 1000ull;
-    FP9_CUDA_TRY(launch_pdl(prefill_kernel<false, 1, false>, dim3(1), dim3(kThreads), Cfg<1>::kSmem,
+    FP9_CUDA_TRY(launch_pdl(prefill_kernel<false, 1, false, false>, dim3(1), dim3(kThreads), Cfg<1>::kSmem,
                             static_cast<cudaStream_t>(stream), maps, p));
     return FP9_OK;
 }

@@ -29,11 +29,14 @@ struct GroupTableDev {
 };
 
 // Both GEMMs of the grouped FFN: x16 [rows, H] fp16 -> h [rows, I] fp16
-// (SwiGLU) -> y [rows, H] fp32 (unweighted per-row FFN outputs).
+// (SwiGLU) -> y [rows, H] fp32 (unweighted per-row FFN outputs). With
+// `split`, x16 and h hold two fp16 terms per value in the split layout
+// ([rows, 2H] and [rows, 2I]: each 64-column chunk c as its hi terms in
+// columns [128 c, 128 c + 64) and its lo terms in the next 64).
 // max_mtiles bounds mtile[n_groups] (the launch grids are sized by it;
 // CTAs past the real count exit at once).
 fp9_status launch_grouped_ffn(const fp9_ffn_bank& routed, const fp9_ffn_bank* shared, const GroupTableDev& tab,
-                              int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows,
+                              int64_t max_mtiles, const __half* x16, __half* h, float* y, int64_t rows, bool split,
                               int32_t* status, int sms, cudaStream_t stream);
 
 }  // namespace fp9

@@ -248,6 +248,24 @@ fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
                          void* stream);
 
 /*
+ * Precision of the prefill entry points (their `precision` argument). The
+ * fp9 weights are exact in fp16 (body << 7 | sign << 15 is their fp16,
+ * [MEMOIR-FP9]), so only the activations x and h = SiLU(W_gate x) *
+ * (W_up x) are rounded to the MMA's fp16 operand type:
+ *   FP9_PREFILL_SPLIT (0, the default): each activation is carried as two
+ *     fp16 terms, hi = fp16(v) and lo = fp16(v - hi) (22 significant bits),
+ *     and every weight meets both in fp32-accumulated MMAs; y agrees with
+ *     the exact FFN within 2e-4 * max|y| per token row, as the decode path
+ *     does. It takes about twice the MMA work of the dense kernels.
+ *   FP9_PREFILL_FP16 (1, opt-in): one fp16 term per activation; y differs
+ *     from the exact FFN by about the fp16 unit roundoff (2^-11) relative
+ *     to sum |terms|, which misses that rule (relative L2 error about
+ *     4e-4); faster.
+ */
+#define FP9_PREFILL_SPLIT 0
+#define FP9_PREFILL_FP16 1
+
+/*
  * fp9_ffn_prefill: y = FFN_k(x) for m tokens at once (prompt prefill), on
  * the tensor cores. The pages run the same fp9 FFN over every prompt token
  * and list their prefill kernel as far below the hardware's compute peak
@@ -261,28 +279,29 @@ fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz,
  *          (m = 0 is a no-op).
  *   Shape: hidden % 256 == 0 (256 <= hidden <= FP9_MAX_PREFILL_HIDDEN),
  *          inter % 128 == 0 (inter <= FP9_MAX_INTER), else FP9_ERR_SHAPE.
+ *   precision  FP9_PREFILL_SPLIT (default) or FP9_PREFILL_FP16, see above;
+ *          any other value is FP9_ERR_INVALID_ARG.
  *   ws     device, >= fp9_prefill_workspace_bytes(ffn, m), 256-byte aligned
- *          (holds x and h = SiLU(W_gate x) * (W_up x) as fp16, and for
- *          small m the down GEMM's partial outputs: it then splits K into
- *          up to 4 parts and adds them in part order, so y is still
+ *          (holds x and h = SiLU(W_gate x) * (W_up x) as fp16 terms, and
+ *          for small m the down GEMM's partial outputs: it then splits K
+ *          into up to 4 parts and adds them in part order, so y is still
  *          deterministic).
- *   Arithmetic: the fp9 weights are exact in fp16 (body << 7 | sign << 15
- *   is their fp16, [MEMOIR-FP9]); x and h are rounded to fp16 (round to
- *   nearest even), the MMA operand type, and products are accumulated in
- *   fp32, so y differs from the exact FFN by about the fp16 unit roundoff
- *   (2^-11) relative to sum |terms|. An x or h whose fp16 is not finite
- *   (|v| >= 65520, Inf, NaN) is recorded as FP9_ERR_RANGE in *d_status.
+ *   Arithmetic: products of the exact fp16 weights and the fp16 activation
+ *   terms are accumulated in fp32 (tensor memory). An x or h whose fp16 is
+ *   not finite (|v| >= 65520, Inf, NaN) is recorded as FP9_ERR_RANGE in
+ *   *d_status.
  */
 #define FP9_MAX_PREFILL_TOKENS 1048576
 #define FP9_MAX_PREFILL_HIDDEN 32768
 fp9_status fp9_ffn_prefill(const fp9_ffn_bank* ffn, int64_t k, const float* x,
-                           int64_t m, float* y, void* ws, size_t ws_bytes,
-                           int32_t* d_status, void* stream);
+                           int64_t m, float* y, int32_t precision, void* ws,
+                           size_t ws_bytes, int32_t* d_status, void* stream);
 
 /* Workspace bytes of fp9_ffn_prefill for m tokens on the current device
- * (0 if the arguments are invalid): x and h as fp16, plus fp32 partial
- * outputs when the down GEMM splits K for this m on this device's SM count
- * (small m), so query it on the device that will run the call. */
+ * (0 if the arguments are invalid), for either precision: x and h as two
+ * fp16 terms each, plus fp32 partial outputs when the down GEMM splits K
+ * for this m on this device's SM count (small m), so query it on the
+ * device that will run the call. */
 size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m);
 
 /*
@@ -290,26 +309,27 @@ size_t fp9_prefill_workspace_bytes(const fp9_ffn_bank* ffn, int64_t m);
  * layer of fp9_moe_forward, with the expert FFNs on the tensor cores. The
  * router is the decode step's (fp32 logits, then the same selection rules
  * and weight formula); each token's slots are grouped by expert, every
- * expert with tokens runs its FFN once over all of them as a GEMM (x and h
- * rounded to fp16, fp32 accumulation: the arithmetic of fp9_ffn_prefill),
- * and y[t] = sum_k w[t,k] FFN_{id[t,k]}(x[t]) + sum_s FFN_shared_s(x[t]) is
- * added in slot, then shared-expert order (deterministic for a device).
+ * expert with tokens runs its FFN once over all of them as a GEMM (the
+ * arithmetic of fp9_ffn_prefill, in the chosen `precision`), and y[t] =
+ * sum_k w[t,k] FFN_{id[t,k]}(x[t]) + sum_s FFN_shared_s(x[t]) is added in
+ * slot, then shared-expert order (deterministic for a device).
  *   layer  as for fp9_moe_forward, plus hidden % 256 == 0 and inter % 128
  *          == 0 (FP9_ERR_SHAPE).
  *   x, y   device fp32 [m, hidden], 16-byte aligned, y may not alias x;
  *          0 <= m <= FP9_MAX_PREFILL_TOKENS (0 is a no-op).
  *   ids, weights  optional device outputs [m, topk] (NULL to skip).
+ *   precision  FP9_PREFILL_SPLIT (default) or FP9_PREFILL_FP16.
  *   ws     device, >= fp9_moe_prefill_workspace_bytes(layer, m), 256-byte
  *          aligned, zeroed once after allocation (its counter resets
  *          itself). It holds the routing, and x, h and the per-expert
  *          outputs of every (token, expert) pair: about
- *          m * (topk + n_shared) * (6 * hidden + 2 * inter) bytes.
+ *          m * (topk + n_shared) * (8 * hidden + 4 * inter) bytes.
  *   A token value or h whose fp16 is not finite is FP9_ERR_RANGE.
  */
 fp9_status fp9_moe_prefill(const fp9_moe_layer* layer, const float* x,
                            int64_t m, float* y, int32_t* ids, float* weights,
-                           void* ws, size_t ws_bytes, int32_t* d_status,
-                           void* stream);
+                           int32_t precision, void* ws, size_t ws_bytes,
+                           int32_t* d_status, void* stream);
 
 /* Workspace bytes of fp9_moe_prefill for m tokens (0 if invalid). */
 size_t fp9_moe_prefill_workspace_bytes(const fp9_moe_layer* layer, int64_t m);

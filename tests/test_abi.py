@@ -137,12 +137,14 @@ def test_dense_and_norm_argument_checks(lib):
 def test_prefill_argument_checks(lib):
     b = _bank(2, 128, 512)
 
-    def call(bank=b, k=0, x=P, m=4, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 30):
-        return lib.fp9_ffn_prefill(ctypes.byref(bank) if bank is not None else None, k, x, m, y, ws, ws_bytes,
-                                   None, None)
+    def call(bank=b, k=0, x=P, m=4, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 30, precision=0):
+        return lib.fp9_ffn_prefill(ctypes.byref(bank) if bank is not None else None, k, x, m, y, precision, ws,
+                                   ws_bytes, None, None)
 
     need = lib.fp9_prefill_workspace_bytes(ctypes.byref(b), 4)
-    assert need == 4 * 512 * 2 + 1024            # x and h as fp16, each 256-byte aligned
+    assert need == 4 * 512 * 4 + 4 * 128 * 4     # x and h as two fp16 terms each, each 256-byte aligned
+    assert call(precision=2) == binding.FP9_ERR_INVALID_ARG
+    assert call(precision=-1) == binding.FP9_ERR_INVALID_ARG
     assert call(bank=None) == binding.FP9_ERR_INVALID_ARG
     assert call(k=2) == binding.FP9_ERR_INVALID_ARG
     assert call(k=-1) == binding.FP9_ERR_INVALID_ARG
@@ -163,13 +165,14 @@ def test_prefill_argument_checks(lib):
 
 
 def test_moe_prefill_argument_checks(lib):
-    def call(layer, m=16, x=P, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 40):
-        return lib.fp9_moe_prefill(ctypes.byref(layer), x, m, y, None, None, ws, ws_bytes, None, None)
+    def call(layer, m=16, x=P, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 40, precision=0):
+        return lib.fp9_moe_prefill(ctypes.byref(layer), x, m, y, None, None, precision, ws, ws_bytes, None, None)
 
     L = _layer()
     need = lib.fp9_moe_prefill_workspace_bytes(ctypes.byref(L), 16)
-    assert need > 16 * 3 * (6 * 256 + 2 * 128)
-    assert lib.fp9_moe_prefill(None, P, 4, P, None, None, P, 1, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert need > 16 * 3 * (8 * 256 + 4 * 128)
+    assert lib.fp9_moe_prefill(None, P, 4, P, None, None, 0, P, 1, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert call(L, precision=3) == binding.FP9_ERR_INVALID_ARG
     assert call(_layer(hidden=384, routed=_bank(8, 128, 384), shared=_bank(1, 128, 384))) == binding.FP9_ERR_SHAPE
     assert call(_layer(inter=64, routed=_bank(8, 64, 256), shared=_bank(1, 64, 256))) == binding.FP9_ERR_SHAPE
     assert call(_layer(topk=17)) == binding.FP9_ERR_SHAPE
