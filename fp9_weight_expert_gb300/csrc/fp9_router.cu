@@ -85,21 +85,20 @@ __device__ void select_all(const RouterArgs& a, const float* s, int tid, int32_t
     __shared__ uint32_t s_kept[FP9_MAX_BSZ];
     __shared__ float s_sel[kMaxEntries];
     const int E = a.E, G = a.n_groups, gsize = E / G;
-    // group scores: sum of the two largest members (the one member if gsize == 1)
+    // group scores: sum of the two largest members (the one member if
+    // gsize == 1). The members are read from a rotated start (the groups'
+    // threads then hit distinct banks), eight loads at a time.
     for (int i = tid; i < a.bsz * G; i += blockDim.x) {
         const int t = i / G, g = i % G;
         const float* grp = s + t * E + g * gsize;
+        const int r0 = g % gsize;
         float m1 = -INFINITY, m2 = -INFINITY;
-        int idx = g % gsize;  // rotated start: the groups' threads hit distinct banks
+#pragma unroll 8
         for (int m = 0; m < gsize; ++m) {
+            const int idx = m + r0 < gsize ? m + r0 : m + r0 - gsize;
             const float v = grp[idx];
-            idx = (idx + 1 == gsize) ? 0 : idx + 1;
-            if (v > m1) {
-                m2 = m1;
-                m1 = v;
-            } else if (v > m2) {
-                m2 = v;
-            }
+            m2 = fmaxf(m2, fminf(m1, v));
+            m1 = fmaxf(m1, v);
         }
         s_gs[t][g] = (gsize == 1) ? m1 : m1 + m2;
     }
@@ -124,6 +123,9 @@ __device__ void select_all(const RouterArgs& a, const float* s, int tid, int32_t
             if (!((kept >> g) & 1u)) continue;
             const float* grp = st + g * gsize;
             const int base = g * gsize;
+            // the threads of a warp read the same member (a broadcast); eight
+            // independent loads at a time
+#pragma unroll 8
             for (int m = 0; m < gsize; ++m) rank += better(grp[m], base + m, v, e) ? 1 : 0;
         }
         if (rank < a.topk) {
@@ -144,6 +146,91 @@ __device__ void select_all(const RouterArgs& a, const float* s, int tid, int32_t
             a.w_ws[t * a.topk + k] = w;
             if (a.ids_out) a.ids_out[t * a.topk + k] = id;
             if (a.w_out) a.w_out[t * a.topk + k] = w;
+        }
+    }
+    __syncthreads();
+}
+
+// Warp bitonic sort of 32 (score, expert) pairs, one per lane, into the
+// selection order: larger score first, equal scores by lower expert (lane 0
+// holds the best). Each step keeps the better of a lane pair in the lane
+// whose run and position call for it.
+__device__ __forceinline__ void warp_sort_best_first(float& v, int& i, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j >= 1; j >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, i, j);
+            const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
+            if (better(ov, oi, v, i) == keep_better) {
+                v = ov;
+                i = oi;
+            }
+        }
+    }
+}
+
+// Selection when every group has 32 experts and the candidates (the best
+// topk of each kept group) fit in a warp (topk_groups * topk <= 32), as in
+// the DeepSeek-V3 gate (8 groups of 32, top-4 groups, top-8):
+//  1. one warp per (token, group) sorts the group's 32 scores; the group
+//     score is the sum of its first two; the sorted scores and their experts
+//     go back to the group's slots of s / s_idx;
+//  2. the kept groups by rank, as in select_all;
+//  3. one warp per token sorts the first topk of each kept group; its first
+//     topk lanes are the chosen experts in selection order.
+// The chosen experts, their order and the weights (s_i / sum, summed in
+// selection order, times route_scale) are those of select_all.
+__device__ void select_g32(const RouterArgs& a, float* s, int* s_idx, int tid, int32_t* s_ids, float* s_wts) {
+    __shared__ float s_gs[FP9_MAX_BSZ][FP9_MAX_GROUPS];
+    __shared__ uint32_t s_kept[FP9_MAX_BSZ];
+    const int E = a.E, G = a.n_groups, K = a.topk, KG = a.topk_groups, bsz = a.bsz;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = kRouterThreads / 32;
+    for (int p = warp; p < bsz * G; p += nwarps) {
+        const int t = p / G, g = p - t * G;
+        float* grp = s + t * E + g * 32;
+        float v = grp[lane];
+        int i = g * 32 + lane;
+        warp_sort_best_first(v, i, lane);
+        const float v1 = __shfl_sync(0xFFFFFFFFu, v, 1);
+        grp[lane] = v;
+        s_idx[t * E + g * 32 + lane] = i;
+        if (lane == 0) s_gs[t][g] = v + v1;
+    }
+    if (tid < bsz) s_kept[tid] = 0u;
+    __syncthreads();
+    for (int i = tid; i < bsz * G; i += blockDim.x) {
+        const int t = i / G, g = i % G;
+        const float v = s_gs[t][g];
+        int rank = 0;
+        for (int o = 0; o < G; ++o) rank += better(s_gs[t][o], o, v, g) ? 1 : 0;
+        if (rank < KG) atomicOr(&s_kept[t], 1u << g);
+    }
+    __syncthreads();
+    for (int t = warp; t < bsz; t += nwarps) {
+        const uint32_t kept = s_kept[t];
+        const int q = lane / K, r = lane - q * K;
+        float v = -INFINITY;
+        int i = INT_MAX;
+        if (q < KG) {
+            uint32_t m = kept;  // the q-th kept group: clear the q lowest set bits
+            for (int k = 0; k < q; ++k) m &= m - 1u;
+            const int g = __ffs(static_cast<int>(m)) - 1;
+            v = s[t * E + g * 32 + r];
+            i = s_idx[t * E + g * 32 + r];
+        }
+        warp_sort_best_first(v, i, lane);
+        float sum = 0.0f;
+        for (int k = 0; k < K; ++k) sum += __shfl_sync(0xFFFFFFFFu, v, k);
+        if (lane < K) {
+            const float w = v / sum * a.scale;
+            s_ids[t * K + lane] = i;
+            s_wts[t * K + lane] = w;
+            a.ids_ws[t * K + lane] = i;
+            a.w_ws[t * K + lane] = w;
+            if (a.ids_out) a.ids_out[t * K + lane] = i;
+            if (a.w_out) a.w_out[t * K + lane] = w;
         }
     }
     __syncthreads();
@@ -239,7 +326,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
-    extern __shared__ float s_scores[];  // [bsz, E] in the last CTA
+    extern __shared__ float s_scores[];  // [bsz, E] scores, then [bsz, E] experts, in the last CTA
     __shared__ float s_red[kRouterThreads / 32][FP9_MAX_BSZ];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -249,14 +336,20 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     const float4* w4 = reinterpret_cast<const float4*>(a.wr) + static_cast<int64_t>(e) * H4;
 
     // Nothing is read before the wait: the caller may have written x, W_g
-    // or the workspace with the kernel just before this one.
+    // or the workspace with the kernel just before this one. W_g is read
+    // with the L2 evict-last hint: the router weights (7.3 MB a layer) stay
+    // in L2 from one step to the next while the expert weights stream
+    // through it evict-first. The first token's x is loaded with them.
     grid_dependency_wait();
     grid_launch_dependents();
-    float4 wv[kRouterVec];
+    const uint64_t keep = l2_evict_last_policy();
+    float4 wv[kRouterVec], x0[kRouterVec];
 #pragma unroll
     for (int i = 0; i < kRouterVec; ++i) {
         const int c = tid + i * kRouterThreads;
-        wv[i] = c < H4 ? __ldcs(w4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool in = c < H4;
+        wv[i] = in ? ld_global_hint(w4 + c, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x0[i] = in ? __ldg(x4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     float acc[FP9_MAX_BSZ];
@@ -264,11 +357,20 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     for (int t = 0; t < FP9_MAX_BSZ; ++t) acc[t] = 0.0f;
 #pragma unroll
     for (int i = 0; i < kRouterVec; ++i) {
-        const int c = tid + i * kRouterThreads;
-        if (c < H4) {
+        float v = acc[0];
+        v = fmaf(wv[i].x, x0[i].x, v);
+        v = fmaf(wv[i].y, x0[i].y, v);
+        v = fmaf(wv[i].z, x0[i].z, v);
+        v = fmaf(wv[i].w, x0[i].w, v);
+        acc[0] = v;
+    }
 #pragma unroll
-            for (int t = 0; t < FP9_MAX_BSZ; ++t) {
-                if (t < a.bsz) {
+    for (int t = 1; t < FP9_MAX_BSZ; ++t) {
+        if (t < a.bsz) {
+#pragma unroll
+            for (int i = 0; i < kRouterVec; ++i) {
+                const int c = tid + i * kRouterThreads;
+                if (c < H4) {
                     const float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
                     float v = acc[t];
                     v = fmaf(wv[i].x, xv.x, v);
@@ -310,7 +412,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     __syncthreads();
     __shared__ int32_t s_ids[kMaxEntries];
     __shared__ float s_wts[kMaxEntries];
-    select_all(a, s_scores, tid, s_ids, s_wts);
+    if (a.E == 32 * a.n_groups && a.topk <= 32 && a.topk_groups * a.topk <= 32)
+        select_g32(a, s_scores, reinterpret_cast<int*>(s_scores + a.bsz * a.E), tid, s_ids, s_wts);
+    else
+        select_all(a, s_scores, tid, s_ids, s_wts);
     if (a.jobs != nullptr) build_jobs(a, tid, s_ids, s_wts);
 }
 
@@ -363,11 +468,12 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.cta_row = reinterpret_cast<int64_t*>(ws + lay.off_ctarow);
     a.I = L->inter;
     a.grid = lay.grid;
-    const size_t smem = sizeof(float) * bsz * L->n_experts;  // <= 32 KB
+    // scores and their experts (the fast selection sorts both in place)
+    const size_t smem = 2 * sizeof(float) * bsz * L->n_experts;  // <= 64 KB
     static DeviceOnce attr;
     const fp9_status ast = attr.run([] {
         FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
+                                          static_cast<int>(2 * sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
         return FP9_OK;
     });
     if (ast != FP9_OK) return ast;
