@@ -624,14 +624,30 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
     const int c = blockIdx.x * kCombineCols + q * 4;
     const float* base = a.partial + static_cast<int64_t>(t) * a.grid * a.H + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int b = sl; b < a.grid; b += kCombineLanes) {
-        if (!((__ldcg(a.mask + b) >> t) & 1u)) continue;
-        const float4 p = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(b) * a.H));
-        acc.x += p.x;
-        acc.y += p.y;
-        acc.z += p.z;
-        acc.w += p.w;
+    // the written-masks and the partial rows are loaded together (one round
+    // trip to L2); rows a CTA never wrote are loaded but not added
+    constexpr int kPer = 4;
+    for (int b0 = sl; b0 < a.grid; b0 += kCombineLanes * kPer) {
+        uint32_t m[kPer];
+        float4 p[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int b = b0 + k * kCombineLanes;
+            m[k] = 0u;
+            if (b < a.grid) {
+                m[k] = __ldcg(a.mask + b);
+                p[k] = __ldcs(reinterpret_cast<const float4*>(base + static_cast<int64_t>(b) * a.H));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            if ((m[k] >> t) & 1u) {
+                acc.x += p[k].x;
+                acc.y += p[k].y;
+                acc.z += p[k].z;
+                acc.w += p[k].w;
+            }
+        }
     }
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) {  // the warp's 8 partial lanes of this float4
