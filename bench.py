@@ -45,7 +45,7 @@ def _args():
                    help="routed experts per layer (smaller layers for profiling captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the bsz-2 / dense side runs")
-    p.add_argument("--leg", choices=["fp8_to_fp9", "prefill", "moe_prefill"], default=None,
+    p.add_argument("--leg", choices=["fp8_to_fp9", "prefill", "moe_prefill", "stack"], default=None,
                    help="run one side measurement alone and print its record (profiling captures)")
     p.add_argument("--tokens", type=int, nargs="+", default=[1481, 4096],
                    help="prompt lengths of the moe_prefill leg")
@@ -206,6 +206,8 @@ def _native(args):
         return {"leg": args.leg, **_convert_run(dev, _peaks()[0])}
     if args.leg == "prefill":
         return {"leg": args.leg, **_prefill_run(dev, _tensor_peak())}
+    if args.leg == "stack":
+        return {"leg": args.leg, **_stack_run(dev, shape)}
 
     def make_layer(l):
         L = layers.MoELayer(H, I, shape.n_experts, shape.n_groups, shape.topk_groups, shape.topk,
