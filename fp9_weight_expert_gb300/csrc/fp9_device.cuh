@@ -188,4 +188,41 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// ------------------------------------------------------------ stack glue ---
+//
+// RMSNorm of the residual stream of a stack, x = v / sqrt(mean(v^2) + eps)
+// with v = h + y (unit gain), in one fixed order: 256 threads, thread t
+// adds the squares of the float4s t, t + 256, ... of the row (x, y, z, w of
+// each by fmaf), each warp sums its threads (warp_sum), and the 8 warp sums
+// are added in warp order.
+constexpr int kNormThreads = 256;
+
+// v = h + y of float4 c, read through L2 (both were written by earlier kernels).
+__device__ __forceinline__ float4 residual4(const float4* h4, const float4* y4, int64_t c) {
+    float4 v = __ldcg(h4 + c);
+    if (y4 != nullptr) {
+        const float4 d = __ldcg(y4 + c);
+        v.x += d.x;
+        v.y += d.y;
+        v.z += d.z;
+        v.w += d.w;
+    }
+    return v;
+}
+
+__device__ __forceinline__ float sumsq4(float4 v, float ss) {
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    return fmaf(v.w, v.w, ss);
+}
+
+// 1 / sqrt(mean + eps) from the 8 warp sums.
+__device__ __forceinline__ float rms_scale(const float* warp_sums, int64_t H, float eps) {
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) tot += warp_sums[w];
+    return 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+}
+
 }  // namespace fp9

@@ -14,8 +14,6 @@
 
 namespace fp9 {
 
-constexpr int kNormThreads = 256;
-
 // One CTA per token; each thread keeps its float4 columns in a fixed order,
 // and the block sum of squares is added in a fixed order.
 __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(float* h, const float* y, float* x_out,
@@ -31,28 +29,14 @@ __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(float* h
     const int64_t H4 = H / 4;
     float ss = 0.0f;
     for (int64_t c = threadIdx.x; c < H4; c += kNormThreads) {
-        float4 v = h4[c];
-        if (y4) {
-            const float4 d = y4[c];
-            v.x += d.x;
-            v.y += d.y;
-            v.z += d.z;
-            v.w += d.w;
-            h4[c] = v;
-        }
-        ss = fmaf(v.x, v.x, ss);
-        ss = fmaf(v.y, v.y, ss);
-        ss = fmaf(v.z, v.z, ss);
-        ss = fmaf(v.w, v.w, ss);
+        const float4 v = residual4(h4, y4, c);
+        if (y4) h4[c] = v;
+        ss = sumsq4(v, ss);
     }
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float tot = 0.0f;
-        for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
-        s_scale = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
-    }
+    if (threadIdx.x == 0) s_scale = rms_scale(red, H, eps);
     __syncthreads();
     const float scale = s_scale;
     for (int64_t c = threadIdx.x; c < H4; c += kNormThreads) {
