@@ -78,6 +78,7 @@ struct ExpertArgs {
     int32_t impl_jobs;       // phase 0: jobs that need no routing
     int32_t impl_nexp;       // phase 0: experts of the bank (shared experts, or 1 for the dense FFN)
     int32_t impl_bank;       // phase 0: 1 (shared experts) or 0 (dense FFN)
+    int32_t tpj;             // phase 0: tokens per job (1 or 2)
     int32_t routed;          // 1: phase 1 runs on the router's plan (MoE call)
     int32_t bsz;
     int32_t H;
@@ -121,7 +122,7 @@ struct Walk {
     Job job;
 
     __device__ __forceinline__ void load_job(const ExpertArgs& a) {
-        job = phase == 0 ? implicit_job(j, a.impl_nexp, a.impl_bank, a.bsz) : a.jobs[j];
+        job = phase == 0 ? implicit_job(j, a.impl_nexp, a.impl_bank, a.bsz, a.tpj) : a.jobs[j];
     }
     __device__ __forceinline__ void set_phase(const ExpertArgs& a, int ph) {
         phase = ph;
@@ -750,7 +751,10 @@ struct FfnCall {
 static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int32_t bsz, int32_t H, int64_t I,
                              uint8_t* ws, const WsLayout& lay, int32_t* status, cudaStream_t stream,
                              uint64_t timeout_ns, bool no_copy, bool combine) {
-    const int MT = bsz == 1 ? 1 : 2;  // jobs hold two tokens only when bsz >= 2
+    // An MoE call plans one token per job (see the plan) and runs the
+    // one-token kernel; a dense call pairs its tokens when bsz >= 2.
+    const int tpj = (call.moe || bsz == 1) ? 1 : 2;
+    const int MT = tpj;
     LaunchShape shp;
     fp9_status st = expert_shape(H, MT, shp);
     if (st != FP9_OK) return st;
@@ -766,7 +770,8 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     a.ctl = reinterpret_cast<const Control*>(ws);
     a.cta_row = reinterpret_cast<const int64_t*>(ws + lay.off_ctarow);
     a.impl_nexp = call.impl_nexp > 0 ? call.impl_nexp : 1;
-    a.impl_jobs = call.impl_nexp * token_pairs(bsz);
+    a.impl_jobs = call.impl_nexp * token_groups(bsz, tpj);
+    a.tpj = tpj;
     a.impl_bank = call.impl_bank;
     a.routed = call.moe ? 1 : 0;
     a.bsz = bsz;

@@ -3,7 +3,13 @@
 //
 // A job is one FFN streamed for a group of up to two tokens (the pages' bsz =
 // 2 pair hits nearly disjoint expert sets, so most jobs hold one token of a
-// pair; a shared expert holds both) [MTP-9.2]. The jobs' intermediate rows
+// pair; a shared expert holds both) [MTP-9.2]. An MoE call plans one token
+// per job instead (tpj = 1): the jobs of an expert chosen by several tokens
+// sit next to each other in the row sequence, so CTAs running side by side
+// stream the same rows and all but the first read of each row hit in L2 (HBM
+// bytes stay those of the union of experts), and every CTA runs the
+// one-token kernel, the fastest per weight. The dense FFN keeps token pairs
+// (each of its rows is streamed for both tokens at once). The jobs' intermediate rows
 // are concatenated and split over the CTAs of the fused kernel: each CTA
 // owns one contiguous range of (job, row) pairs, keeps y of the job's tokens
 // in registers and adds it into its own fp32 partial output of each token;
@@ -56,24 +62,24 @@ struct Control {
     int32_t pad;
 };
 
-// Jobs of phase 0 (no routing): nexp experts of one bank for every pair of
-// tokens, pair-major (job j: token pair j / nexp, expert j % nexp), so that
-// consecutive jobs hold the same tokens.
-__host__ __device__ inline Job implicit_job(int32_t j, int32_t nexp, int32_t bank, int32_t bsz) {
+// Jobs of phase 0 (no routing): nexp experts of one bank for every group of
+// tpj tokens (1 or 2), group-major (job j: token group j / nexp, expert
+// j % nexp), so that consecutive jobs hold the same tokens.
+__host__ __device__ inline Job implicit_job(int32_t j, int32_t nexp, int32_t bank, int32_t bsz, int32_t tpj) {
     Job jb;
     const int32_t p = j / nexp;
     jb.bank = bank;
     jb.expert = j - p * nexp;
     jb.pad = 0;
-    jb.tok[0] = kTokensPerJob * p;
-    jb.ntok = (kTokensPerJob * p + 1 < bsz) ? 2 : 1;
+    jb.tok[0] = tpj * p;
+    jb.ntok = (tpj == 2 && tpj * p + 1 < bsz) ? 2 : 1;
     jb.tok[1] = jb.ntok == 2 ? jb.tok[0] + 1 : jb.tok[0];
     jb.w[0] = 1.0f;
     jb.w[1] = jb.ntok == 2 ? 1.0f : 0.0f;
     return jb;
 }
 
-__host__ __device__ inline int32_t token_pairs(int32_t bsz) { return (bsz + kTokensPerJob - 1) / kTokensPerJob; }
+__host__ __device__ inline int32_t token_groups(int32_t bsz, int32_t tpj) { return (bsz + tpj - 1) / tpj; }
 
 constexpr size_t kAlign = 256;
 

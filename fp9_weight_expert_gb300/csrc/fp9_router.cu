@@ -42,6 +42,7 @@ struct RouterArgs {
     float* w_out;        // optional
     Job* jobs;           // [jmax]
     int64_t* cta_row;    // [grid + 1] first row of each CTA of the fused kernel
+    int32_t tpj;         // tokens per job: 1 (an MoE call) or 2
 };
 
 static_assert(kMaxJobs <= kRouterThreads && kMaxEntries <= kRouterThreads, "one thread per job in the plan scan");
@@ -237,7 +238,7 @@ __device__ void select_g32(const RouterArgs& a, float* s, int* s_idx, int tid, i
 }
 
 // Routed job list: experts in ascending id, each with its tokens in
-// ascending order, in groups of up to two (the shared experts need no
+// ascending order, in groups of up to tpj (the shared experts need no
 // routing: the fused kernel streams them on its own, before these). Then
 // the cost-weighted split of the jobs' rows over the fused kernel's CTAs:
 // each CTA's first row.
@@ -271,7 +272,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         e = s_key[tid] / FP9_MAX_BSZ;
         int pos = 0;
         for (int q = tid - 1; q >= 0 && s_key[q] / FP9_MAX_BSZ == e; --q) ++pos;
-        is_start = (pos % kTokensPerJob == 0) ? 1 : 0;
+        is_start = (pos % a.tpj == 0) ? 1 : 0;
     }
     int32_t J = 0;
     const int32_t before = block_exclusive_scan(is_start, tid, J);
@@ -282,7 +283,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         j.pad = 0;
         j.tok[0] = s_key[tid] % FP9_MAX_BSZ;
         j.w[0] = s_w[tid];
-        const bool two = (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
+        const bool two = a.tpj == 2 && (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
         j.ntok = two ? 2 : 1;
         j.tok[1] = two ? s_key[tid + 1] % FP9_MAX_BSZ : j.tok[0];
         j.w[1] = two ? s_w[tid + 1] : 0.0f;
@@ -297,7 +298,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
     int32_t ctot = 0;
     const int32_t cpre = block_exclusive_scan(cj, tid, ctot);
     const int64_t U = a.I * ctot;
-    const int32_t cmax = a.bsz >= 2 ? kRowCost2 : kRowCost1;
+    const int32_t cmax = (a.bsz >= 2 && a.tpj == 2) ? kRowCost2 : kRowCost1;
     int64_t G = U / cmax;
     G = G > a.grid ? a.grid : (G < 1 ? 1 : G);
     if (tid < J) {
@@ -468,6 +469,7 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.cta_row = reinterpret_cast<int64_t*>(ws + lay.off_ctarow);
     a.I = L->inter;
     a.grid = lay.grid;
+    a.tpj = 1;  // an MoE call plans one token per job
     // scores and their experts (the fast selection sorts both in place)
     const size_t smem = 2 * sizeof(float) * bsz * L->n_experts;  // <= 64 KB
     static DeviceOnce attr;
