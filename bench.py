@@ -384,20 +384,11 @@ def _native(args):
     return out
 
 
-def _streamed_units(ids_step, n_shared: int, bsz: int) -> int:
-    """Expert FFNs the fused kernel streams for one step: each routed expert
-    once per group of up to two of its tokens, each shared expert once per
-    pair of tokens."""
-    from collections import Counter
-    per_expert = Counter(ids_step)
-    return sum((n + 1) // 2 for n in per_expert.values()) + n_shared * ((bsz + 1) // 2)
-
-
 def _side_runs(Ls, ws, status, dev, shape):
     """The same layers at bsz 2, 5 and 8 (the pair and verify row counts):
-    weight-stream GB/s of the union of touched experts, and the bytes the
-    kernel actually streams (experts with three or more tokens, and the
-    shared expert, are streamed once per pair of tokens)."""
+    weight-stream GB/s of the union of touched experts, and the fused
+    kernel's (expert, token) passes per step (an MoE call plans one token
+    per job; the repeated passes of an expert read its rows from L2)."""
     import torch
 
     from fp9_weight_expert_gb300 import Workspace, binding, synth
@@ -421,12 +412,10 @@ def _side_runs(Ls, ws, status, dev, shape):
         ms = a.elapsed_time(b)
         idc = ids.cpu()
         units = sum(len(set(idc[i].flatten().tolist())) + shape.n_shared for i in range(K))
-        streamed = sum(_streamed_units(idc[i].flatten().tolist(), shape.n_shared, bsz) for i in range(K))
         gbs = units * unit / (ms / 1e3) / 1e9
         res[f"bsz{bsz}"] = {"tok_s": round(bsz * K / (ms / 1e3), 1), "us_per_layer": round(ms / K * 1e3, 2),
                             "weight_stream_gbs": round(gbs, 1), "mean_experts": round(units / K, 2),
-                            "streamed_experts": round(streamed / K, 2),
-                            "streamed_gbs": round(streamed * unit / (ms / 1e3) / 1e9, 1), "steps": K}
+                            "passes": bsz * (shape.topk + shape.n_shared), "steps": K}
         del w2
     res.update(_moe_prefill_run(Ls, status, dev, shape, (1481, 4096)))
     if int(status.item()) != 0:
@@ -550,10 +539,13 @@ def _moe_prefill_run(Ls, status, dev, shape, lengths):
 
 def _stack_run(dev, shape, n_layers=12, K=1000):
     """The 12-layer stack of the workload (config 5): 12 distinct resident
-    DeepSeek-V3 MoE layers (153 GB) with the residual + RMSNorm glue between
+    DeepSeek-V3 MoE layers (153 GB) with the residual + RMSNorm between
     them, h <- h + MoE_l(RMSNorm(h)); the whole stack step is captured once
     in a CUDA graph and replayed K = 1000 times (the workload's steady
-    state over 1000 steps). Tokens/s through all 12 layers."""
+    state over 1000 steps). Tokens/s through all 12 layers, for the layer
+    step with the glue folded in (fp9_moe_forward_residual: three kernels a
+    layer) and, under "glue", for the separate glue kernel between
+    fp9_moe_forward calls (four kernels a layer)."""
     import torch
 
     from fp9_weight_expert_gb300 import Workspace, binding, layers, synth
@@ -572,19 +564,23 @@ def _stack_run(dev, shape, n_layers=12, K=1000):
                                                     * FP9_BYTES_PER_WEIGHT / 1e9, 1)}
     # bsz 2: an MTP pair (confirmed + draft token) in lockstep; bsz 5: a
     # speculative verify block of 5 rows
-    for bsz in (1, 2, 5):
+    for mode, bsz in (("residual", 1), ("residual", 2), ("residual", 5), ("glue", 1), ("glue", 2), ("glue", 5)):
         h0 = synth.tokens(bsz, H, synth.seed_for(7100, bsz, synth.TOKENS), dev) * 2.0
         h = h0.clone()
         x = torch.empty_like(h)
         y = torch.empty_like(h)
+        ss = torch.empty((bsz, H // 16), dtype=torch.float32, device=dev)
         ids = torch.empty((n_layers, bsz, shape.topk), dtype=torch.int32, device=dev)
         ws = Workspace.for_moe(Ls[0], bsz, dev)
 
         def step():
             binding.fp9_residual_rmsnorm(h, None, x)
             for l, L in enumerate(Ls):
-                binding.fp9_moe_forward(L, x, y, ws.tensor, status, ids[l])
-                binding.fp9_residual_rmsnorm(h, y, x)
+                if mode == "residual":
+                    binding.fp9_moe_forward_residual(L, x if l == 0 else None, h, ss, ws.tensor, status, ids[l])
+                else:
+                    binding.fp9_moe_forward(L, x, y, ws.tensor, status, ids[l])
+                    binding.fp9_residual_rmsnorm(h, y, x)
 
         step()
         torch.cuda.synchronize()
@@ -612,10 +608,14 @@ def _stack_run(dev, shape, n_layers=12, K=1000):
         idc = ids.cpu()
         experts = sum(len(set(idc[l].flatten().tolist())) + shape.n_shared for l in range(n_layers))
         wbytes = experts * 3 * I * H * FP9_BYTES_PER_WEIGHT
-        out[f"bsz{bsz}"] = {"tok_s": round(bsz / (ms / 1e3), 1), "us_per_stack_step": round(ms * 1e3, 1),
-                            "us_per_layer": round(ms * 1e3 / n_layers, 2),
-                            "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
-                            "experts_streamed": experts, "steps": K}
+        rec = {"tok_s": round(bsz / (ms / 1e3), 1), "us_per_stack_step": round(ms * 1e3, 1),
+               "us_per_layer": round(ms * 1e3 / n_layers, 2),
+               "weight_stream_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+               "experts_streamed": experts, "steps": K}
+        if mode == "residual":
+            out[f"bsz{bsz}"] = rec
+        else:
+            out.setdefault("glue", {})[f"bsz{bsz}"] = rec
     del Ls
     torch.cuda.empty_cache()
     return out

@@ -159,6 +159,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk copy global -> shared (no tensor map), completing `bytes` of
 // transaction count on `bar`. dst, src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
@@ -196,6 +202,27 @@ __device__ __forceinline__ float warp_sum(float v) {
 // each by fmaf), each warp sums its threads (warp_sum), and the 8 warp sums
 // are added in warp order.
 constexpr int kNormThreads = 256;
+
+// The same scale, 1 / sqrt(mean(v^2) + eps), from a row's sum of squares
+// held as n <= FP9_MAX_HIDDEN / 16 partial sums (ss[0 .. n), column
+// order), added by one warp in a fixed order: lane l adds parts l, l + 32,
+// ... in turn (all its loads issued first), then the xor butterfly of
+// warp_sum (each step adds the same two values on both lanes). Every lane
+// of every warp that calls it gets the same bits.
+__device__ __forceinline__ float rms_scale_parts(const float* ss, int n, int64_t H, float eps, int lane) {
+    constexpr int kPer = (FP9_MAX_HIDDEN / 16 + 31) / 32;
+    float v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = lane + 32 * k;
+        v[k] = i < n ? __ldcg(ss + i) : 0.0f;
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) s += v[k];
+    s = warp_sum(s);
+    return 1.0f / sqrtf(s / static_cast<float>(H) + eps);
+}
 
 // v = h + y of float4 c, read through L2 (both were written by earlier kernels).
 __device__ __forceinline__ float4 residual4(const float4* h4, const float4* y4, int64_t c) {

@@ -69,7 +69,9 @@ struct BankPtrs {
 
 struct ExpertArgs {
     BankPtrs bank[2];        // 0: routed experts / dense FFN, 1: shared experts
-    const float* x;          // [bsz, H]
+    const float* x;          // [bsz, H]: x, or h in stack mode
+    const float* ss;         // stack mode: partial sums of squares of h (x = RMSNorm(h)), else NULL
+    float eps;
     float* partial;          // token-major: [bsz * gridDim.x, H]
     uint32_t* mask;          // [gridDim.x]: bit t = partial of token t written
     const Job* jobs;         // phase 1: the router's jobs
@@ -195,7 +197,7 @@ __device__ __forceinline__ bool reads_stages(int w, int R) { return w < 2 * R; }
 // ------------------------------------------------------------- producer ---
 
 __device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring) {
-    const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol_once = l2_evict_first_policy(), pol_reread = l2_evict_normal_policy();
     const int H = a.H, R = a.rows;
     const uint32_t sbytes = stage_bytes(H, R);
     uint32_t use[kSlots] = {0u, 0u, 0u};
@@ -209,6 +211,7 @@ __device__ void producer(const ExpertArgs& a, SmemCtl& ctl, uint8_t* ring) {
         const uint32_t bb = static_cast<uint32_t>(rows * H), sb = static_cast<uint32_t>(rows * (H / 8));
         const uint32_t full = smem_addr(&ctl.full[m]);
         const uint32_t dst = smem_addr(ring + m * sbytes);
+        const uint64_t pol = (job.flags & kJobReread) ? pol_reread : pol_once;
         if (!a.no_copy) {
             mbar_arrive_expect_tx(full, bb + sb);
             bulk_g2s(dst, bp.body[m] + row * H, bb, full, pol);
@@ -411,8 +414,10 @@ __device__ __forceinline__ void flush_y(const ExpertArgs& a, int ntok, int tok0,
 // columns 16 c + 4 q + (0, 2, 1, 3) of token t), then waits until every
 // consumer warp has written its share. x is read from L2 (ld.global.cg):
 // in an MoE call the fused kernel reads it before its own grid-dependency
-// wait, once the kernel that wrote it has completed.
-template <int MT>
+// wait, once the kernel that wrote it has completed. In stack mode x = h *
+// scale, the scale formed by each warp from the partial sums of squares
+// (the router's bits).
+template <int MT, bool kNorm>
 __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const Job& job, int nch,
                                         int tid, int NT, uint32_t& xuse, int lane) {
     const int H4 = a.H / 4;
@@ -420,9 +425,18 @@ __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float
         if (t >= job.ntok) break;
         const int tok = t == 0 ? job.tok[0] : job.tok[1];
         const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H);
-        for (int j = tid; j < H4; j += NT) {
-            const float4 v = __ldcg(src + j);
-            xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x, v.z, v.y, v.w);
+        if constexpr (kNorm) {
+            const int nparts = a.H / kNormPartCols;
+            const float sc = rms_scale_parts(a.ss + static_cast<int64_t>(tok) * nparts, nparts, a.H, a.eps, lane);
+            for (int j = tid; j < H4; j += NT) {
+                const float4 v = __ldcg(src + j);
+                xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x * sc, v.z * sc, v.y * sc, v.w * sc);
+            }
+        } else {
+            for (int j = tid; j < H4; j += NT) {
+                const float4 v = __ldcg(src + j);
+                xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x, v.z, v.y, v.w);
+            }
         }
     }
     __syncwarp();
@@ -447,7 +461,7 @@ struct Shape {
     static constexpr int kRows = HC > 0 ? (kNW / 2 > 4 ? kNW / 2 : 4) : 0;
 };
 
-template <int MT, int HC>
+template <int MT, int HC, bool kNorm>
 __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const uint8_t* ring, int NW, int warp,
                          int lane) {
     using S = Shape<MT, HC>;
@@ -466,7 +480,7 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
     w.begin(a, R);
     uint32_t xuse = 0;
     bool ok = true;
-    if (!w.done()) ok = stage_x<MT>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
+    if (!w.done()) ok = stage_x<MT, kNorm>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
     uint32_t c = 0;  // chunk index: uses of the gate and up slots, and the publish parity
     // the chunk whose down rows are pending (chunk c - 1) and its tokens
     bool pending = false, p_flush = false;
@@ -529,7 +543,7 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
             // new tokens: y is flushed after this chunk's down rows; every
             // warp is past this chunk's gate/up rows, so x may change now
             p_flush = true;
-            ok = stage_x<MT>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
+            ok = stage_x<MT, kNorm>(a, ctl, xs, w.job, nch, warp * 32 + lane, NW * 32, xuse, lane);
         }
         ++c;
     }
@@ -553,7 +567,8 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
 
 // MT: most tokens a job can hold (1 when bsz == 1). HC: the hidden size
 // the kernel is specialised for (0: any).
-template <int MT, int HC>
+// kNorm: stack mode (x = RMSNorm(h) formed while staging; MT == 1 only).
+template <int MT, int HC, bool kNorm>
 __global__ void __launch_bounds__(MT == 1 ? kMaxThreads1 : kMaxThreads, 1) expert_kernel(const ExpertArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem);
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(MT == 1 ? kMaxThreads1 : kMaxThreads, 1) exper
         if (lane == 0) producer(a, ctl, ring);
         return;
     }
-    consumer<MT, HC>(a, ctl, xs, ring, NW, warp, lane);
+    consumer<MT, HC, kNorm>(a, ctl, xs, ring, NW, warp, lane);
 }
 
 // ------------------------------------------------------------- combine ----
@@ -603,10 +618,13 @@ struct CombineArgs {
     const uint32_t* mask;  // [grid]
     int32_t H;
     int32_t grid;          // CTAs of the expert kernel
-    float* y;
+    float* y;              // [bsz, H], or NULL (stack mode)
+    float* h;              // stack mode: [bsz, H] residual stream, h += y; else NULL
+    float* ss;             // stack mode: [bsz, H / 16] partial sums of squares of the new h
 };
 
 constexpr int kCombineCols = 16;    // columns per CTA: 4 float4
+static_assert(kCombineCols == kNormPartCols, "a combine CTA writes one partial sum of squares");
 constexpr int kCombineThreads = 256;
 constexpr int kCombineLanes = kCombineThreads / 4;  // partial lanes per column: 64
 
@@ -614,7 +632,9 @@ constexpr int kCombineLanes = kCombineThreads / 4;  // partial lanes per column:
 // order. Thread (lane s, float4 q) adds the partials of CTAs s, s + 64, ...
 // that hold token t (all their loads in flight at once); the 64 lane sums
 // are added by a fixed shuffle tree inside each warp (8 lanes per warp),
-// then the 8 warps' sums in warp order.
+// then the 8 warps' sums in warp order. Stack mode: h += y over the CTA's
+// 16 columns, and their sum of squares (float4 q = 0..3 in order) is the
+// CTA's partial for the next layer's RMSNorm.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
     __shared__ float4 red[kCombineThreads / 32][4];
     grid_dependency_wait();  // all partials are written
@@ -668,7 +688,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
             sum.z += o.z;
             sum.w += o.w;
         }
-        reinterpret_cast<float4*>(a.y + static_cast<int64_t>(t) * a.H)[c / 4] = sum;
+        const int64_t o4 = (static_cast<int64_t>(t) * a.H + c) / 4;
+        if (a.y != nullptr) reinterpret_cast<float4*>(a.y)[o4] = sum;
+        if (a.h != nullptr) {
+            float4 v = __ldcg(reinterpret_cast<const float4*>(a.h) + o4);
+            v.x += sum.x;
+            v.y += sum.y;
+            v.z += sum.z;
+            v.w += sum.w;
+            reinterpret_cast<float4*>(a.h)[o4] = v;
+            const float s = sumsq4(v, 0.0f);
+            const float s1 = __shfl_sync(0xFu, s, 1), s2 = __shfl_sync(0xFu, s, 2), s3 = __shfl_sync(0xFu, s, 3);
+            if (q == 0) a.ss[static_cast<int64_t>(t) * gridDim.x + blockIdx.x] = ((s + s1) + s2) + s3;
+        }
     }
 }
 
@@ -716,9 +748,9 @@ static fp9_status expert_shape(int32_t H, int MT, LaunchShape& s) {
     return FP9_OK;
 }
 
-template <int MT, int HC>
+template <int MT, int HC, bool kNorm>
 static cudaError_t set_smem(int optin) {
-    return cudaFuncSetAttribute(expert_kernel<MT, HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    return cudaFuncSetAttribute(expert_kernel<MT, HC, kNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 static fp9_status ensure_smem_attr() {
@@ -726,10 +758,12 @@ static fp9_status ensure_smem_attr() {
     return attr.run([] {
         const int32_t optin = device_max_smem_optin();
         if (optin <= 0) return FP9_ERR_CUDA;
-        FP9_CUDA_TRY((set_smem<1, 0>(optin)));
-        FP9_CUDA_TRY((set_smem<2, 0>(optin)));
-        FP9_CUDA_TRY((set_smem<1, kDsv3Hidden>(optin)));
-        FP9_CUDA_TRY((set_smem<2, kDsv3Hidden>(optin)));
+        FP9_CUDA_TRY((set_smem<1, 0, false>(optin)));
+        FP9_CUDA_TRY((set_smem<2, 0, false>(optin)));
+        FP9_CUDA_TRY((set_smem<1, kDsv3Hidden, false>(optin)));
+        FP9_CUDA_TRY((set_smem<2, kDsv3Hidden, false>(optin)));
+        FP9_CUDA_TRY((set_smem<1, 0, true>(optin)));
+        FP9_CUDA_TRY((set_smem<1, kDsv3Hidden, true>(optin)));
         return FP9_OK;
     });
 }
@@ -747,10 +781,19 @@ struct FfnCall {
     bool moe;            // phase 1 runs on the router's plan
 };
 
+// Stack mode of a call: the input is RMSNorm(h) (norm.ss set; x points at
+// h) and the combine adds y into h and writes the next partial sums of
+// squares (h, ss_out set; y NULL).
+struct Residual {
+    NormIn norm{nullptr, 0.0f};
+    float* h = nullptr;
+    float* ss_out = nullptr;
+};
+
 // Queues the fused expert kernel and (when `combine`) the combine kernel.
 static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int32_t bsz, int32_t H, int64_t I,
                              uint8_t* ws, const WsLayout& lay, int32_t* status, cudaStream_t stream,
-                             uint64_t timeout_ns, bool no_copy, bool combine) {
+                             uint64_t timeout_ns, bool no_copy, bool combine, const Residual& res = Residual()) {
     // An MoE call plans one token per job (see the plan) and runs the
     // one-token kernel; a dense call pairs its tokens when bsz >= 2.
     const int tpj = (call.moe || bsz == 1) ? 1 : 2;
@@ -764,6 +807,8 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     a.bank[0] = call.routed;
     a.bank[1] = call.implicit;
     a.x = x;
+    a.ss = res.norm.ss;
+    a.eps = res.norm.eps;
     a.partial = reinterpret_cast<float*>(ws + lay.off_partial);
     a.mask = reinterpret_cast<uint32_t*>(ws + lay.off_mask);
     a.jobs = reinterpret_cast<const Job*>(ws + lay.off_jobs);
@@ -786,8 +831,13 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     // the DeepSeek-V3 hidden size has its own kernel with every loop bound fixed
     const bool special = H == kDsv3Hidden && shp.rows == (MT == 1 ? Shape<1, kDsv3Hidden>::kRows
                                                                    : Shape<2, kDsv3Hidden>::kRows);
-    void (*kern)(const ExpertArgs) = special ? (MT == 1 ? expert_kernel<1, kDsv3Hidden> : expert_kernel<2, kDsv3Hidden>)
-                                             : (MT == 1 ? expert_kernel<1, 0> : expert_kernel<2, 0>);
+    // stack mode runs only in MoE calls (MT == 1)
+    const bool norm = a.ss != nullptr;
+    if (norm && MT != 1) return FP9_ERR_INVALID_ARG;
+    void (*kern)(const ExpertArgs) =
+        special ? (norm ? expert_kernel<1, kDsv3Hidden, true>
+                        : (MT == 1 ? expert_kernel<1, kDsv3Hidden, false> : expert_kernel<2, kDsv3Hidden, false>))
+                : (norm ? expert_kernel<1, 0, true> : (MT == 1 ? expert_kernel<1, 0, false> : expert_kernel<2, 0, false>));
     FP9_CUDA_TRY(launch_pdl(kern, dim3(lay.grid), dim3(shp.threads), shp.smem, stream, a));
     if (prof) FP9_CUDA_TRY(cudaEventRecord(g_prof_stop, stream));
     if (!combine) return FP9_OK;
@@ -797,13 +847,15 @@ static fp9_status launch_ffn(const FfnCall& call, const float* x, float* y, int3
     c.H = H;
     c.grid = lay.grid;
     c.y = y;
+    c.h = res.h;
+    c.ss = res.ss_out;
     FP9_CUDA_TRY(launch_pdl(combine_kernel, dim3(H / kCombineCols, bsz), dim3(kCombineThreads), 0, stream, c));
     return FP9_OK;
 }
 
 fp9_status check_layer(const fp9_moe_layer* L, int32_t bsz);
 fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, int32_t* ids_out, float* w_out,
-                         uint8_t* ws, const WsLayout& lay, bool build, cudaStream_t stream);
+                         uint8_t* ws, const WsLayout& lay, bool build, cudaStream_t stream, const NormIn& norm);
 
 static fp9_status check_dense(const fp9_ffn_bank* f, int32_t bsz) {
     FP9_CHECK_ARG(f != nullptr, FP9_ERR_INVALID_ARG);
@@ -848,10 +900,36 @@ extern "C" fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x
     FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
-    st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s);
+    st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s, NormIn{nullptr, 0.0f});
     if (st != FP9_OK) return st;
     return launch_ffn(moe_call(layer), x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, d_status,
                       s, kDefaultTimeoutNs, false, true);
+}
+
+extern "C" fp9_status fp9_moe_forward_residual(const fp9_moe_layer* layer, const float* x, float* h, float* ss,
+                                               int32_t bsz, float eps, int32_t* ids, float* weights, void* ws,
+                                               size_t ws_bytes, int32_t* d_status, void* stream) {
+    fp9_status st = check_layer(layer, bsz);
+    if (st != FP9_OK) return st;
+    FP9_CHECK_ARG(h != nullptr && ss != nullptr && ws != nullptr && x != h, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(eps >= 0.0f && eps <= 1.0f, FP9_ERR_INVALID_ARG);
+    FP9_CHECK_ARG(aligned(h, 16) && aligned(ss, 16) && (x == nullptr || aligned(x, 16)), FP9_ERR_ALIGN);
+    FP9_CHECK_ARG(aligned(ws, kAlign), FP9_ERR_ALIGN);
+    const int32_t sms = device_sm_count();
+    FP9_CHECK_ARG(sms > 0, FP9_ERR_CUDA);
+    const WsLayout lay = moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true));
+    FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    Residual res;
+    res.norm = NormIn{x == nullptr ? ss : nullptr, eps};
+    res.h = h;
+    res.ss_out = ss;
+    const float* in = x == nullptr ? h : x;
+    st = launch_router(layer, in, bsz, ids, weights, w, lay, true, s, res.norm);
+    if (st != FP9_OK) return st;
+    return launch_ffn(moe_call(layer), in, nullptr, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay,
+                      d_status, s, kDefaultTimeoutNs, false, true, res);
 }
 
 extern "C" fp9_status fp9_dense_ffn(const fp9_ffn_bank* ffn, const float* x, int32_t bsz, float* y, void* ws,
@@ -999,7 +1077,7 @@ extern "C" fp9_status fp9_moe_forward_noalloc(const fp9_moe_layer* layer, const 
     FP9_CHECK_ARG(w != nullptr, FP9_ERR_CUDA);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     FP9_CUDA_TRY(cudaMemsetAsync(w, 0, sizeof(Control), s));
-    st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s);
+    st = launch_router(layer, x, bsz, ids, weights, w, lay, true, s, NormIn{nullptr, 0.0f});
     if (st != FP9_OK) return st;
     return launch_ffn(moe_call(layer), x, y, bsz, static_cast<int32_t>(layer->hidden), layer->inter, w, lay, d_status,
                       s, kDefaultTimeoutNs, false, true);

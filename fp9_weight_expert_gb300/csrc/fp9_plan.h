@@ -42,6 +42,26 @@ constexpr int kTokensPerJob = 2;
 constexpr int32_t kRowCost1 = 8, kRowCost2 = 11;
 __host__ __device__ inline int32_t row_cost(int32_t ntok) { return ntok == 2 ? kRowCost2 : kRowCost1; }
 
+// Job flags. kJobReread: another job of the same call streams these rows
+// too (an expert chosen by several tokens, a shared expert at bsz >= 2);
+// the fused kernel then reads them with the L2 evict-normal priority, so
+// that the other job's reads find them in L2 although its CTAs reach the
+// rows some microseconds earlier or later, while the rest of the weight
+// stream is read evict-first.
+constexpr int32_t kJobReread = 1;
+
+// Stack mode of an MoE call (fp9_moe_forward_residual). The layer's input
+// is x = RMSNorm(h) (unit gain), formed where it is read: the router and the
+// fused kernel read h and the row's sum of squares, which the previous
+// call's combine left as partial sums, one per kNormPartCols columns of each
+// token's row (ss[t * H / kNormPartCols + b]); the combine adds y into h
+// and writes the new partial sums.
+constexpr int kNormPartCols = 16;
+struct NormIn {
+    const float* ss;  // partial sums of squares of h, or NULL (x is the input as given)
+    float eps;
+};
+
 // the router keeps one thread per routed job
 constexpr int kMaxJobs = FP9_MAX_BSZ * FP9_MAX_TOPK;  // 128
 
@@ -49,7 +69,7 @@ struct __align__(16) Job {
     int32_t bank;      // 0 = routed experts (or the dense FFN), 1 = shared
     int32_t expert;    // index inside the bank
     int32_t ntok;      // 1 or 2
-    int32_t pad;
+    int32_t flags;     // kJobReread
     int32_t tok[kTokensPerJob];
     float w[kTokensPerJob];  // routing weight per token (1 for shared / dense)
 };
@@ -62,6 +82,8 @@ struct Control {
     int32_t pad;
 };
 
+__host__ __device__ inline int32_t token_groups(int32_t bsz, int32_t tpj) { return (bsz + tpj - 1) / tpj; }
+
 // Jobs of phase 0 (no routing): nexp experts of one bank for every group of
 // tpj tokens (1 or 2), group-major (job j: token group j / nexp, expert
 // j % nexp), so that consecutive jobs hold the same tokens.
@@ -70,7 +92,7 @@ __host__ __device__ inline Job implicit_job(int32_t j, int32_t nexp, int32_t ban
     const int32_t p = j / nexp;
     jb.bank = bank;
     jb.expert = j - p * nexp;
-    jb.pad = 0;
+    jb.flags = token_groups(bsz, tpj) > 1 ? kJobReread : 0;
     jb.tok[0] = tpj * p;
     jb.ntok = (tpj == 2 && tpj * p + 1 < bsz) ? 2 : 1;
     jb.tok[1] = jb.ntok == 2 ? jb.tok[0] + 1 : jb.tok[0];
@@ -78,8 +100,6 @@ __host__ __device__ inline Job implicit_job(int32_t j, int32_t nexp, int32_t ban
     jb.w[1] = jb.ntok == 2 ? 1.0f : 0.0f;
     return jb;
 }
-
-__host__ __device__ inline int32_t token_groups(int32_t bsz, int32_t tpj) { return (bsz + tpj - 1) / tpj; }
 
 constexpr size_t kAlign = 256;
 

@@ -28,7 +28,9 @@ constexpr int kMaxEntries = FP9_MAX_BSZ * FP9_MAX_TOPK;  // 128 (token, expert) 
 static_assert(kMaxEntries <= kRouterThreads, "one thread per routed pair");
 
 struct RouterArgs {
-    const float* x;      // [bsz, H]
+    const float* x;      // [bsz, H]: x, or h in stack mode
+    const float* ss;     // stack mode: partial sums of squares of h (x = RMSNorm(h)), else NULL
+    float eps;
     const float* wr;     // [E, H]
     int32_t bsz, E, H, n_groups, topk_groups, topk;
     float scale;
@@ -266,12 +268,14 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         s_w[rank] = w;
     }
     __syncthreads();
-    int32_t is_start = 0;
+    int32_t is_start = 0, run = 0;
     int e = 0;
-    if (tid < P) {  // a job starts at every other key of an expert's run
+    if (tid < P) {  // a job starts at every tpj-th key of an expert's run
         e = s_key[tid] / FP9_MAX_BSZ;
         int pos = 0;
         for (int q = tid - 1; q >= 0 && s_key[q] / FP9_MAX_BSZ == e; --q) ++pos;
+        run = pos + 1;
+        for (int q = tid + 1; q < P && s_key[q] / FP9_MAX_BSZ == e; ++q) ++run;
         is_start = (pos % a.tpj == 0) ? 1 : 0;
     }
     int32_t J = 0;
@@ -280,7 +284,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         Job j;
         j.bank = 0;
         j.expert = e;
-        j.pad = 0;
+        j.flags = run > a.tpj ? kJobReread : 0;  // the expert's tokens fill more than one job
         j.tok[0] = s_key[tid] % FP9_MAX_BSZ;
         j.w[0] = s_w[tid];
         const bool two = a.tpj == 2 && (tid + 1 < P) && (s_key[tid + 1] / FP9_MAX_BSZ == e);
@@ -326,6 +330,9 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
     }
 }
 
+// kNorm: stack mode (a.ss set), a separate instance so that the plain
+// call's code is not burdened by it.
+template <bool kNorm>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
     extern __shared__ float s_scores[];  // [bsz, E] scores, then [bsz, E] experts, in the last CTA
     __shared__ float s_red[kRouterThreads / 32][FP9_MAX_BSZ];
@@ -352,6 +359,23 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
         wv[i] = in ? ld_global_hint(w4 + c, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
         x0[i] = in ? __ldg(x4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // stack mode: x = h * (1 / sqrt(mean(h^2) + eps)) of each token, the
+    // scale of token t formed by warp t from the partial sums of squares
+    // (the same bits as any other warp would form)
+    __shared__ float s_norm[FP9_MAX_BSZ];
+    static_assert(kRouterThreads / 32 >= FP9_MAX_BSZ, "a warp per token");
+    constexpr bool norm = kNorm;
+    if (norm) {
+        const int nparts = a.H / kNormPartCols;
+        if (warp < a.bsz) {
+            const float sc = rms_scale_parts(a.ss + warp * nparts, nparts, a.H, a.eps, lane);
+            if (lane == 0) s_norm[warp] = sc;
+        }
+        __syncthreads();
+        const float sc = s_norm[0];
+#pragma unroll
+        for (int i = 0; i < kRouterVec; ++i) x0[i] = make_float4(x0[i].x * sc, x0[i].y * sc, x0[i].z * sc, x0[i].w * sc);
+    }
 
     float acc[FP9_MAX_BSZ];
 #pragma unroll
@@ -368,11 +392,13 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
 #pragma unroll
     for (int t = 1; t < FP9_MAX_BSZ; ++t) {
         if (t < a.bsz) {
+            const float sc = norm ? s_norm[t] : 1.0f;
 #pragma unroll
             for (int i = 0; i < kRouterVec; ++i) {
                 const int c = tid + i * kRouterThreads;
                 if (c < H4) {
-                    const float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
+                    float4 xv = __ldg(x4 + static_cast<int64_t>(t) * H4 + c);
+                    if (norm) xv = make_float4(xv.x * sc, xv.y * sc, xv.z * sc, xv.w * sc);
                     float v = acc[t];
                     v = fmaf(wv[i].x, xv.x, v);
                     v = fmaf(wv[i].y, xv.y, v);
@@ -446,11 +472,15 @@ fp9_status check_layer(const fp9_moe_layer* L, int32_t bsz) {
     return FP9_OK;
 }
 
-// Queues the router kernel; writes the job list when `build` is set.
+// Queues the router kernel; writes the job list when `build` is set. With
+// norm.ss set, x holds h and the router routes RMSNorm(h) (stack mode).
 fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, int32_t* ids_out,
-                         float* w_out, uint8_t* ws, const WsLayout& lay, bool build, cudaStream_t stream) {
+                         float* w_out, uint8_t* ws, const WsLayout& lay, bool build, cudaStream_t stream,
+                         const NormIn& norm) {
     RouterArgs a;
     a.x = x;
+    a.ss = norm.ss;
+    a.eps = norm.eps;
     a.wr = L->w_router;
     a.bsz = bsz;
     a.E = L->n_experts;
@@ -474,12 +504,17 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     const size_t smem = 2 * sizeof(float) * bsz * L->n_experts;  // <= 64 KB
     static DeviceOnce attr;
     const fp9_status ast = attr.run([] {
-        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(2 * sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
+        FP9_CUDA_TRY(cudaFuncSetAttribute(router_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(2 * sizeof(float) * FP9_MAX_BSZ * FP9_MAX_EXPERTS)));
         return FP9_OK;
     });
     if (ast != FP9_OK) return ast;
-    FP9_CUDA_TRY(launch_pdl(router_kernel, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
+    if (norm.ss != nullptr)
+        FP9_CUDA_TRY(launch_pdl(router_kernel<true>, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
+    else
+        FP9_CUDA_TRY(launch_pdl(router_kernel<false>, dim3(L->n_experts), dim3(kRouterThreads), smem, stream, a));
     return FP9_OK;
 }
 
@@ -541,5 +576,5 @@ extern "C" fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int
     const WsLayout lay = moe_layout(bsz, layer->n_experts, layer->topk, layer->hidden, expert_grid(sms, true));
     FP9_CHECK_ARG(ws_bytes >= lay.total, FP9_ERR_WORKSPACE);
     return launch_router(layer, x, bsz, ids, weights, static_cast<uint8_t*>(ws), lay, false,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), NormIn{nullptr, 0.0f});
 }

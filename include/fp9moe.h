@@ -193,15 +193,49 @@ fp9_status moe_router(const fp9_moe_layer* layer, const float* x, int32_t bsz,
  * fp9_moe_forward: y = MoE(x) for one layer, at 1 <= bsz <= FP9_MAX_BSZ.
  *   x, y device fp32 [bsz, hidden], 16-byte aligned (y may not alias x).
  *   ids / weights: optional device outputs of the routing (NULL to skip).
- *   Weights are streamed once per call for each group of up to two tokens
- *   that share an expert; partial sums over intermediate slices stay fp32
- *   and are added in a fixed order, so results are deterministic for a
- *   given device ([MEMOIR-COMM], [MEMOIR-16], [DS4-TP]).
+ *   An expert chosen by several tokens is one job per token; its rows are
+ *   read with the L2 evict-normal priority, so the repeated reads mostly
+ *   hit in L2 (every other weight is read once, evict-first); partial sums over intermediate slices stay fp32 and
+ *   are added in a fixed order, so results are deterministic for a given
+ *   device ([MEMOIR-COMM], [MEMOIR-16], [DS4-TP]).
  */
 fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x,
                            int32_t bsz, float* y, int32_t* ids, float* weights,
                            void* ws, size_t ws_bytes, int32_t* d_status,
                            void* stream);
+
+/*
+ * fp9_moe_forward_residual: one layer step of a stack of MoE layers with the
+ * glue between layers folded into the layer's own kernels ("第 9 章 MTP1
+ * dual-lane overlap", section 9.5: stage 0 of a decode layer holds the
+ * layernorm and the residual add). Per token t:
+ *   in[t] = x[t] if x is given, else h[t] / sqrt(mean(h[t]^2) + eps)
+ *           (RMSNorm with unit gain, mean(h[t]^2) from the partial sums
+ *           in ss[t]);
+ *   h[t] += MoE(in[t]) of `layer`, as fp9_moe_forward computes it;
+ *   ss[t, b] = the sum of the squares of the new h[t, 16 b .. 16 b + 15],
+ *           b = 0 .. hidden / 16 - 1 (the next call's norm).
+ * A stack calls it once per layer: the first layer with x = RMSNorm(h)
+ * (fp9_residual_rmsnorm(h, NULL, x)), the others with x = NULL; after the
+ * last, fp9_residual_rmsnorm(h, NULL, x_out) gives the normed output. No x
+ * is stored between layers: the router and the fused kernel scale h where
+ * they read it, and the combine kernel writes h and ss, so a layer step is
+ * three kernels instead of four. The partial sums and their total are added
+ * in fixed orders (deterministic for a device); the router and the fused
+ * kernel form the same scale bit for bit.
+ *   x      device fp32 [bsz, hidden] or NULL; may not alias h.
+ *   h      device fp32 [bsz, hidden], updated in place.
+ *   ss     device fp32 [bsz, hidden / 16]: read when x is NULL, rewritten.
+ *   eps    0 <= eps <= 1.
+ *   layer, bsz, ids, weights, ws, ws_bytes (fp9_moe_workspace_bytes),
+ *   d_status, stream: as fp9_moe_forward. x, h, ss 16-byte aligned.
+ *   Errors: as fp9_moe_forward.
+ */
+fp9_status fp9_moe_forward_residual(const fp9_moe_layer* layer, const float* x,
+                                    float* h, float* ss, int32_t bsz, float eps,
+                                    int32_t* ids, float* weights, void* ws,
+                                    size_t ws_bytes, int32_t* d_status,
+                                    void* stream);
 
 /*
  * fp9_moe_forward_host: fp9_moe_forward with x and y in host memory, for a

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
               "fp9_moe_workspace_bytes", "fp9_dense_workspace_bytes", "fp9_residual_rmsnorm",
               "fp9_selftest_timeout", "fp9_status_str", "fp9_from_fp8", "fp9_ffn_prefill",
               "fp9_prefill_workspace_bytes", "fp9_moe_prefill", "fp9_moe_prefill_workspace_bytes",
-              "fp9_prefill_selftest_timeout", "fp9_moe_forward_host", "fp9_moe_host_workspace_bytes"]:
+              "fp9_prefill_selftest_timeout", "fp9_moe_forward_host", "fp9_moe_host_workspace_bytes",
+              "fp9_moe_forward_residual"]:
         assert n in names, n
 
 
@@ -95,6 +96,29 @@ def test_moe_forward_argument_checks(lib):
     assert _fwd(lib, _layer(), y=P) == binding.FP9_ERR_INVALID_ARG       # y aliases x
     assert _fwd(lib, _layer(), ws=P + 16) == binding.FP9_ERR_ALIGN
     assert lib.fp9_moe_workspace_bytes(ctypes.byref(_layer(topk=17)), 1) == 0
+
+
+def test_moe_forward_residual_argument_checks(lib):
+    L = _layer()
+    H, SS, WS = P, P + 0x10000, P + 0x20000
+
+    def call(layer=L, x=None, h=H, ss=SS, bsz=1, eps=1e-6, ws=WS):
+        return lib.fp9_moe_forward_residual(ctypes.byref(layer) if layer is not None else None, x, h, ss, bsz,
+                                            ctypes.c_float(eps), None, None, ws, 1 << 30, None, None)
+    assert call(layer=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(bsz=0) == binding.FP9_ERR_INVALID_ARG
+    assert call(bsz=9) == binding.FP9_ERR_INVALID_ARG
+    assert call(h=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(ss=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(ws=None) == binding.FP9_ERR_INVALID_ARG
+    assert call(x=H) == binding.FP9_ERR_INVALID_ARG           # x aliases h
+    assert call(eps=-1.0) == binding.FP9_ERR_INVALID_ARG
+    assert call(eps=2.0) == binding.FP9_ERR_INVALID_ARG
+    assert call(h=H + 4) == binding.FP9_ERR_ALIGN
+    assert call(ss=SS + 8) == binding.FP9_ERR_ALIGN
+    assert call(x=P + 0x30004) == binding.FP9_ERR_ALIGN
+    assert call(ws=WS + 16) == binding.FP9_ERR_ALIGN
+    assert call(layer=_layer(topk=17)) == binding.FP9_ERR_SHAPE
 
 
 def test_moe_forward_host_argument_checks(lib):
