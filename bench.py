@@ -339,16 +339,7 @@ def _native(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded N(0,0.02) weights packed to fp9 on the GPU, N(0,1) tokens)",
-        "config": {
-            "workload": f"one DeepSeek-V3 MoE layer, bsz {bsz}: hidden 7168, {shape.n_experts} routed experts "
-                        f"(8 groups x {shape.n_experts // 8}, top-4 groups, top-8) + 1 shared, "
-                        "intermediate 2048, fp9 weights",
-            "bsz": bsz,
-            "resident_layers": len(Ls),
-            "l2": "inputs larger than L2: 4 resident layers (12.7 GB each) rotate, each step streams "
-                  f"{sum(weight_bytes) / K / 1e6:.1f} MB of fp9 weights",
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "config": _workload_config(shape, bsz, len(Ls), sum(weight_bytes) / K, world),
         "roofline": {
             "bound": "hbm",
             "kernel": "fp9::expert_kernel",
@@ -957,10 +948,25 @@ def _cpu_sample_worker(spec: str):
                   f"one core = the same FFNs one at a time (one pass)"}))
 
 
+def _workload_config(shape, bsz, n_layers, bytes_per_step, world):
+    """The bench line's config (both arms print the same one)."""
+    return {
+        "workload": f"one DeepSeek-V3 MoE layer, bsz {bsz}: hidden 7168, {shape.n_experts} routed experts "
+                    f"(8 groups x {shape.n_experts // 8}, top-4 groups, top-8) + 1 shared, "
+                    "intermediate 2048, fp9 weights",
+        "bsz": bsz,
+        "resident_layers": n_layers,
+        "l2": f"inputs larger than L2: {n_layers} resident layers (12.7 GB each) rotate, each step streams "
+              f"{bytes_per_step / 1e6:.1f} MB of fp9 weights",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
+
+
 def _reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
+    from fp9_weight_expert_gb300 import synth
     rec = _cpu_baseline(mode="ref", steps=args.steps, warmup=args.warmup)
     if "error" in rec:
         return {"impl": "reference", "unavailable": "oracle run failed: " + rec["error"][-200:]}
@@ -979,7 +985,9 @@ def _reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "one DeepSeek-V3 MoE layer, bsz 1 (CPU oracle on the host cores)", "bsz": 1},
+        # the native arm's workload at bsz 1 (9 experts of 49.5 MB a step)
+        "config": _workload_config(synth.DSV3, 1, args.layers,
+                                   9 * 3 * 2048 * 7168 * FP9_BYTES_PER_WEIGHT, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": rec,
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

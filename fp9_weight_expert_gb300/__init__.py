@@ -8,13 +8,13 @@ in HBM, and seeded synthetic input generators.
 
 from . import binding, build_lib, layers, synth  # noqa: F401
 from .binding import (  # noqa: F401
-    Fp9Error, fp9_decode, fp9_dense_ffn, fp9_ffn_prefill, fp9_from_fp8, fp9_moe_forward, fp9_moe_prefill, fp9_pack,
+    Fp9Error, fp9_decode, fp9_dense_ffn, fp9_ffn_prefill, fp9_from_fp8, fp9_moe_forward, fp9_moe_forward_residual, fp9_moe_prefill, fp9_pack,
     fp9_residual_rmsnorm, fp9_selftest_timeout, moe_router, status_str,
 )
 from .layers import FFNBank, MoELayer, Workspace  # noqa: F401
 
 __all__ = [
     "binding", "build_lib", "layers", "synth", "Fp9Error", "fp9_pack", "fp9_decode", "moe_router",
-    "fp9_moe_forward", "fp9_dense_ffn", "fp9_ffn_prefill", "fp9_moe_prefill", "fp9_from_fp8", "fp9_residual_rmsnorm", "fp9_selftest_timeout",
+    "fp9_moe_forward", "fp9_moe_forward_residual", "fp9_dense_ffn", "fp9_ffn_prefill", "fp9_moe_prefill", "fp9_from_fp8", "fp9_residual_rmsnorm", "fp9_selftest_timeout",
     "status_str", "FFNBank", "MoELayer", "Workspace",
 ]
