@@ -426,11 +426,17 @@ __device__ __forceinline__ bool stage_x(const ExpertArgs& a, SmemCtl& ctl, float
         const int tok = t == 0 ? job.tok[0] : job.tok[1];
         const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(tok) * a.H);
         if constexpr (kNorm) {
+            // h is staged as it is and scaled in place once the warp has the
+            // scale, so the loads of h and of the partial sums overlap
+            for (int j = tid; j < H4; j += NT) {
+                const float4 v = __ldcg(src + j);
+                xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x, v.z, v.y, v.w);
+            }
             const int nparts = a.H / kNormPartCols;
             const float sc = rms_scale_parts(a.ss + static_cast<int64_t>(tok) * nparts, nparts, a.H, a.eps, lane);
             for (int j = tid; j < H4; j += NT) {
-                const float4 v = __ldcg(src + j);
-                xs[(t * 4 + (j & 3)) * nch + (j >> 2)] = make_float4(v.x * sc, v.z * sc, v.y * sc, v.w * sc);
+                float4& v = xs[(t * 4 + (j & 3)) * nch + (j >> 2)];
+                v = make_float4(v.x * sc, v.y * sc, v.z * sc, v.w * sc);
             }
         } else {
             for (int j = tid; j < H4; j += NT) {
