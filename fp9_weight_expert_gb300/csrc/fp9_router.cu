@@ -239,11 +239,81 @@ __device__ void select_g32(const RouterArgs& a, float* s, int* s_idx, int tid, i
     __syncthreads();
 }
 
+// Position of one-token job `tid` (sorted by expert, then token) in a job
+// order that spaces the jobs of an expert chosen by several tokens k jobs
+// apart, k in 1..8 chosen so that k jobs are close to a whole number of the
+// fused kernel's CTA shares (J / G jobs each): then the CTAs that stream an
+// expert's rows for its tokens reach each row at about the same time, and
+// all but the first read of it hit in L2. The order is a k-column grid
+// (position = slot * k + column): the repeated experts' groups go to the
+// columns in turn, each group down one column, and the single-token jobs
+// fill the other slots in order. `pos`: the job's index in its expert's
+// group; `run`: the group's size. Returns -1 (keep the sorted order) when a
+// group does not fit in its column. Every thread of the CTA calls it.
+__device__ int32_t spaced_position(int tid, int J, int64_t G, int pos, int run) {
+    __shared__ int32_t s_rsize[kMaxEntries];
+    __shared__ int32_t s_grank[kMaxEntries];
+    __shared__ int s_fail;
+    int k = 1, best = J;
+    for (int c = 1; c <= 8 && c <= J; ++c) {  // the same choice in every thread
+        const int r = static_cast<int>((c * G) % J);
+        const int d = r < J - r ? r : J - r;
+        if (d < best) {
+            best = d;
+            k = c;
+        }
+    }
+    const bool in = tid < J;
+    const int rep_start = (in && pos == 0 && run >= 2) ? 1 : 0;
+    const int single = (in && run == 1) ? 1 : 0;
+    int32_t nrep = 0, nsingle = 0;
+    const int32_t rrank = block_exclusive_scan(rep_start, tid, nrep);
+    const int32_t srank = block_exclusive_scan(single, tid, nsingle);
+    if (tid == 0) s_fail = 0;
+    if (rep_start) {
+        s_rsize[rrank] = run;
+        s_grank[tid] = rrank;
+    }
+    __syncthreads();
+    int32_t dest = -1;
+    if (in) {
+        auto height = [&](int c) { return (J - c + k - 1) / k; };
+        auto used = [&](int c, int upto) {  // slots of column c that repeated groups of rank < upto hold
+            int u = 0;
+            for (int r = c; r < upto; r += k) u += s_rsize[r];
+            return u;
+        };
+        int col = 0, slot = 0;
+        if (run >= 2) {
+            const int r = s_grank[tid - pos];
+            col = r % k;
+            slot = used(col, r) + pos;
+            if (slot >= height(col)) s_fail = 1;
+        } else {
+            int left = srank;
+            for (col = 0; col < k; ++col) {
+                const int u = used(col, nrep);
+                const int free = height(col) - u;
+                if (left < free) {
+                    slot = u + left;
+                    break;
+                }
+                left -= free;
+            }
+            if (col == k) s_fail = 1;
+        }
+        dest = slot * k + col;
+    }
+    __syncthreads();
+    return s_fail ? -1 : dest;
+}
+
 // Routed job list: experts in ascending id, each with its tokens in
 // ascending order, in groups of up to tpj (the shared experts need no
-// routing: the fused kernel streams them on its own, before these). Then
-// the cost-weighted split of the jobs' rows over the fused kernel's CTAs:
-// each CTA's first row.
+// routing: the fused kernel streams them on its own, before these); for
+// one-token jobs at bsz >= 3, re-spaced by spaced_position. Then the
+// cost-weighted split of the jobs' rows over the fused kernel's CTAs: each
+// CTA's first row.
 __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, const float* s_wts) {
     __shared__ int32_t s_in[kMaxEntries];
     __shared__ int32_t s_key[kMaxEntries];
@@ -268,18 +338,23 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         s_w[rank] = w;
     }
     __syncthreads();
-    int32_t is_start = 0, run = 0;
+    int32_t is_start = 0, run = 0, pos = 0;
     int e = 0;
     if (tid < P) {  // a job starts at every tpj-th key of an expert's run
         e = s_key[tid] / FP9_MAX_BSZ;
-        int pos = 0;
         for (int q = tid - 1; q >= 0 && s_key[q] / FP9_MAX_BSZ == e; --q) ++pos;
         run = pos + 1;
         for (int q = tid + 1; q < P && s_key[q] / FP9_MAX_BSZ == e; ++q) ++run;
         is_start = (pos % a.tpj == 0) ? 1 : 0;
     }
     int32_t J = 0;
-    const int32_t before = block_exclusive_scan(is_start, tid, J);
+    int32_t before = block_exclusive_scan(is_start, tid, J);
+    if (a.tpj == 1 && a.bsz >= 3) {  // J == P: job tid is key tid
+        int64_t G = a.I * J;
+        G = G > a.grid ? a.grid : G;
+        const int32_t d = spaced_position(tid, J, G, pos, run);
+        if (d >= 0) before = d;
+    }
     if (is_start) {
         Job j;
         j.bank = 0;
