@@ -568,7 +568,10 @@ def _stack_run(dev, shape, n_layers=12, K=1000):
             binding.fp9_residual_rmsnorm(h, None, x)
             for l, L in enumerate(Ls):
                 if mode == "residual":
-                    binding.fp9_moe_forward_residual(L, x if l == 0 else None, h, ss, ws.tensor, status, ids[l])
+                    # the next layer's router weights are read into L2 meanwhile
+                    # (after the last layer: the first one, the next replay's)
+                    binding.fp9_moe_forward_residual(L, x if l == 0 else None, h, ss, ws.tensor, status, ids[l],
+                                                     next_layer=Ls[(l + 1) % len(Ls)])
                 else:
                     binding.fp9_moe_forward(L, x, y, ws.tensor, status, ids[l])
                     binding.fp9_residual_rmsnorm(h, y, x)

@@ -89,9 +89,9 @@ _SIGS = {
                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                        ctypes.c_void_p]),
     "fp9_moe_forward_residual": (ctypes.c_int, [ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_void_p,
-                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
-                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
-                                                ctypes.c_void_p]),
+                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
+                                                ctypes.POINTER(MoELayerC), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "fp9_dense_ffn": (ctypes.c_int, [ctypes.POINTER(FFNBankC), ctypes.c_void_p, ctypes.c_int32,
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.c_void_p, ctypes.c_void_p]),
@@ -228,12 +228,15 @@ def fp9_moe_forward(layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
 
 def fp9_moe_forward_residual(layer, x: torch.Tensor | None, h: torch.Tensor, ss: torch.Tensor, ws: torch.Tensor,
                              status: torch.Tensor | None = None, ids: torch.Tensor | None = None,
-                             weights: torch.Tensor | None = None, eps: float = 1e-6, stream=None) -> None:
+                             weights: torch.Tensor | None = None, eps: float = 1e-6, next_layer=None,
+                             stream=None) -> None:
     """One layer step of a stack: h += MoE(x), or h += MoE(RMSNorm(h))
     when x is None (the norm's sums of squares come from ss, which the call
-    then rewrites for the new h: [bsz, hidden / 16] fp32)."""
+    then rewrites for the new h: [bsz, hidden / 16] fp32). next_layer: the
+    stack's next layer, whose router weights are read into L2."""
+    nxt = ctypes.byref(next_layer.c_struct()) if next_layer is not None else None
     _check(load().fp9_moe_forward_residual(ctypes.byref(layer.c_struct()), _ptr(x), _ptr(h), _ptr(ss), h.shape[0],
-                                           ctypes.c_float(eps), _ptr(ids), _ptr(weights), _ptr(ws),
+                                           ctypes.c_float(eps), nxt, _ptr(ids), _ptr(weights), _ptr(ws),
                                            ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
            "fp9_moe_forward_residual")
 

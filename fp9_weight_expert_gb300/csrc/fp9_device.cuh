@@ -165,6 +165,14 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
     return pol;
 }
 
+// L2 prefetch of `bytes` at `src` with an L2 cache-eviction policy (a
+// hint: nothing is written and nothing waits for it). src 16-byte aligned,
+// bytes % 16 == 0.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 // Bulk copy global -> shared (no tensor map), completing `bytes` of
 // transaction count on `bar`. dst, src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,

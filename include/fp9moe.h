@@ -227,15 +227,20 @@ fp9_status fp9_moe_forward(const fp9_moe_layer* layer, const float* x,
  *   h      device fp32 [bsz, hidden], updated in place.
  *   ss     device fp32 [bsz, hidden / 16]: read when x is NULL, rewritten.
  *   eps    0 <= eps <= 1.
+ *   next   the stack's next layer, or NULL: its router weights are read
+ *          into L2 (a prefetch hint, issued by the expert kernel's CTAs
+ *          once they have issued their last weight copies), so that the
+ *          next call's router finds them there even when many layers are
+ *          resident. Checked like `layer`.
  *   layer, bsz, ids, weights, ws, ws_bytes (fp9_moe_workspace_bytes),
  *   d_status, stream: as fp9_moe_forward. x, h, ss 16-byte aligned.
  *   Errors: as fp9_moe_forward.
  */
 fp9_status fp9_moe_forward_residual(const fp9_moe_layer* layer, const float* x,
                                     float* h, float* ss, int32_t bsz, float eps,
-                                    int32_t* ids, float* weights, void* ws,
-                                    size_t ws_bytes, int32_t* d_status,
-                                    void* stream);
+                                    const fp9_moe_layer* next, int32_t* ids,
+                                    float* weights, void* ws, size_t ws_bytes,
+                                    int32_t* d_status, void* stream);
 
 /*
  * fp9_moe_forward_host: fp9_moe_forward with x and y in host memory, for a

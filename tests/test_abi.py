@@ -102,9 +102,10 @@ def test_moe_forward_residual_argument_checks(lib):
     L = _layer()
     H, SS, WS = P, P + 0x10000, P + 0x20000
 
-    def call(layer=L, x=None, h=H, ss=SS, bsz=1, eps=1e-6, ws=WS):
+    def call(layer=L, x=None, h=H, ss=SS, bsz=1, eps=1e-6, ws=WS, nxt=None):
         return lib.fp9_moe_forward_residual(ctypes.byref(layer) if layer is not None else None, x, h, ss, bsz,
-                                            ctypes.c_float(eps), None, None, ws, 1 << 30, None, None)
+                                            ctypes.c_float(eps), ctypes.byref(nxt) if nxt is not None else None,
+                                            None, None, ws, 1 << 30, None, None)
     assert call(layer=None) == binding.FP9_ERR_INVALID_ARG
     assert call(bsz=0) == binding.FP9_ERR_INVALID_ARG
     assert call(bsz=9) == binding.FP9_ERR_INVALID_ARG
@@ -119,6 +120,8 @@ def test_moe_forward_residual_argument_checks(lib):
     assert call(x=P + 0x30004) == binding.FP9_ERR_ALIGN
     assert call(ws=WS + 16) == binding.FP9_ERR_ALIGN
     assert call(layer=_layer(topk=17)) == binding.FP9_ERR_SHAPE
+    assert call(nxt=_layer(topk=17)) == binding.FP9_ERR_SHAPE       # the next layer is checked too
+    assert call(nxt=_layer(w_router=P + 4)) == binding.FP9_ERR_ALIGN
 
 
 def test_moe_forward_host_argument_checks(lib):

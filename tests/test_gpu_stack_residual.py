@@ -46,7 +46,8 @@ def test_residual_steps_match_oracle(bsz):
     for l in range(3):
         hb = h.cpu().numpy().astype(np.float64)
         ids = torch.empty((bsz, shape.topk), dtype=torch.int32, device="cuda")
-        binding.fp9_moe_forward_residual(Ls[l], x if l == 0 else None, h, ss, ws.tensor, status, ids, eps=EPS)
+        binding.fp9_moe_forward_residual(Ls[l], x if l == 0 else None, h, ss, ws.tensor, status, ids, eps=EPS,
+                                         next_layer=Ls[l + 1] if l + 1 < 3 else None)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         _check_parts(h, ss)
@@ -112,7 +113,8 @@ def test_residual_stack_in_a_cuda_graph_matches_eager():
     def run():
         binding.fp9_residual_rmsnorm(h, None, x, EPS)
         for l, L in enumerate(Ls):
-            binding.fp9_moe_forward_residual(L, x if l == 0 else None, h, ss, ws.tensor, eps=EPS)
+            binding.fp9_moe_forward_residual(L, x if l == 0 else None, h, ss, ws.tensor, eps=EPS,
+                                             next_layer=Ls[(l + 1) % 3])
 
     run()
     torch.cuda.synchronize()
