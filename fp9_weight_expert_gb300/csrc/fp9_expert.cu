@@ -53,6 +53,7 @@ namespace fp9 {
 constexpr int kMaxRows = 16;                                    // rows per chunk
 constexpr int kSlots = 3;                                       // gate, up, down
 constexpr int kDownCols = 16;                                   // down columns per thread
+constexpr int kDsv3Hidden = 7168;  // the DeepSeek-V3 hidden size: specialised kernels
 constexpr int kMaxConsumerWarps = FP9_MAX_HIDDEN / kDownCols / 32;  // 14
 constexpr int kMaxThreads = kMaxConsumerWarps * 32 + 32;        // 480
 // One-token kernels round the consumer warps up to a multiple of 4, so that
@@ -98,6 +99,8 @@ struct SmemCtl {
     uint64_t empty[kSlots];
     uint64_t pub[2];         // gate/up sums of a chunk published (double-buffered by chunk parity)
     uint64_t xbar;           // a job's x staged in shared memory
+    uint64_t hfull[2];       // down helper pairs: the helper's y is in shared memory
+    uint64_t hfree[2];       // ... and has been added by the owner
     int abort;
     int never;               // stays 0: a flag nobody raises
     float gu[2][2][kMaxRows][2][kTokensPerJob];  // [chunk parity][gate, up][row][half][token]
@@ -365,20 +368,29 @@ __device__ __forceinline__ void down_row(const uint8_t* st, int H, int R, int rr
     }
 }
 
-// The down rows of a chunk. RC > 0: a full chunk of RC rows is unrolled
-// (no guards) when every lane of the warp owns columns; a warp with lanes
-// past the last column (the one-token kernel's extra warps) takes the
-// guarded loop, whose inactive lanes only join the shuffles.
+// The down rows of a chunk: all of them (half < 0), or its first (half 0)
+// or second (half 1) half, split at (rows + 1) / 2. RC > 0: a full chunk of
+// RC rows is unrolled (no guards) when every lane of the warp owns columns;
+// a warp with lanes past the last column takes the guarded loop, whose
+// inactive lanes only join the shuffles.
 template <int T, int MT, int RC>
 __device__ __forceinline__ void down_stage(const uint8_t* st, int H, int R, int rows, int cc, bool active, float hv,
-                                           Cols<MT>& y) {
+                                           Cols<MT>& y, int half = -1) {
     if (RC > 0 && rows == RC && __all_sync(0xFFFFFFFFu, active)) {
+        if (half < 0) {
 #pragma unroll
-        for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, cc, hv, y);
+            for (int rr = 0; rr < RC; ++rr) down_row<T, MT>(st, H, R, rr, cc, hv, y);
+        } else {
+            const int r0 = half * ((RC + 1) / 2);
+#pragma unroll
+            for (int k = 0; k < RC / 2; ++k) down_row<T, MT>(st, H, R, r0 + k, cc, hv, y);
+        }
         return;
     }
+    const int sp = (rows + 1) / 2;
+    const int lo = half == 1 ? sp : 0, hi = half == 0 ? sp : rows;
 #pragma unroll 1
-    for (int rr = 0; rr < rows; ++rr) {
+    for (int rr = lo; rr < hi; ++rr) {
         if (active) {
             down_row<T, MT>(st, H, R, rr, cc, hv, y);
         } else {
@@ -487,13 +499,55 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
     const int R = S::kRows > 0 ? S::kRows : a.rows;
     if (S::kNW > 0) NW = S::kNW;
     const int nch = H / 16;
-    const int cc = warp * 32 + lane;
+    // Down helpers (the one-token kernel at hidden 7168): 14 warps own the
+    // 448 16-column chunks of y, and the two warps that only exist for the
+    // gate/up balance take the second half of the down rows of warps 0 and
+    // 1 (warp 14 + i helps warp i), adding their y into the owner's when it
+    // is flushed. Warp w issues on scheduler w mod 4, so each scheduler then
+    // issues 28 row units of down work per chunk instead of 32, 32, 24, 24.
+    constexpr bool kHelp = MT == 1 && HC == kDsv3Hidden && S::kNW == S::kNW0 + 2 && S::kRows % 2 == 0;
+    const bool helper = kHelp && warp >= S::kNW0;
+    const bool helped = kHelp && warp < S::kNW - S::kNW0;
+    const int cw = helper ? warp - S::kNW0 : warp;
+    const int half = helper ? 1 : (helped ? 0 : -1);
+    const int cc = cw * 32 + lane;
     const bool active = cc < H / kDownCols;
     const uint32_t sbytes = stage_bytes(H, R);
     const bool rd_gate = reads_stages(warp, R), rd_up = rd_gate;
     Cols<MT> y;
     zero_cols(y);
     uint32_t written = 0;  // tokens whose partial row this CTA has written
+    float* hy = reinterpret_cast<float*>(const_cast<uint8_t*>(ring) + kSlots * sbytes) + (cw * 32 + lane) * 16;
+    uint32_t hn = 0;  // flushes of this pair so far
+    // Flushes y into the CTA's partial rows; in a helper pair the helper
+    // hands its y to the owner through shared memory and the owner adds it
+    // (owner rows + helper rows, a fixed order) before writing.
+    auto flush = [&](int ntok, int tok0, int tok1) -> bool {
+        if (helper || helped) {
+            const uint32_t full = smem_addr(&ctl.hfull[cw]), free = smem_addr(&ctl.hfree[cw]);
+            if (helper) {
+                if (hn > 0 && !mbar_wait_bounded(free, (hn - 1) & 1u, a.timeout_ns, &ctl.abort)) return false;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) reinterpret_cast<float2*>(hy)[k] = y.p[0][k];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full);
+                ++hn;
+                return true;
+            }
+            if (!mbar_wait_bounded(full, hn & 1u, a.timeout_ns, &ctl.abort)) return false;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 o = reinterpret_cast<const float2*>(hy)[k];
+                y.p[0][k].x += o.x;
+                y.p[0][k].y += o.y;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(free);
+            ++hn;
+        }
+        flush_y(a, ntok, tok0, tok1, cc, active, written, y);
+        return true;
+    };
     Walk w;
     w.begin(a, R);
     uint32_t xuse = 0;
@@ -530,10 +584,13 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
             if (p_T == 2)
                 down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             else
-                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y, half);
             release(ctl, kDown, lane);
             if (p_flush) {
-                flush_y(a, p_ntok, p_tok0, p_tok1, cc, active, written, y);
+                if (!flush(p_ntok, p_tok0, p_tok1)) {
+                    ok = false;
+                    break;
+                }
                 zero_cols(y);
             }
         }
@@ -571,9 +628,9 @@ __device__ void consumer(const ExpertArgs& a, SmemCtl& ctl, float4* xs, const ui
             if (p_T == 2)
                 down_stage<MT, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
             else
-                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y);
+                down_stage<1, MT, S::kRows>(ring + kDown * sbytes, H, R, p_rows, cc, active, p_hv, y, half);
             release(ctl, kDown, lane);
-            flush_y(a, p_ntok, p_tok0, p_tok1, cc, active, written, y);
+            ok = flush(p_ntok, p_tok0, p_tok1);
         }
     }
     if (warp == 0 && lane == 0) a.mask[blockIdx.x] = written;
@@ -616,6 +673,10 @@ __global__ void __launch_bounds__(MT == 1 ? kMaxThreads1 : kMaxThreads, 1) exper
         mbar_init(smem_addr(&ctl.pub[0]), NW);
         mbar_init(smem_addr(&ctl.pub[1]), NW);
         mbar_init(smem_addr(&ctl.xbar), NW);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&ctl.hfull[i]), 1);
+            mbar_init(smem_addr(&ctl.hfree[i]), 1);
+        }
         ctl.abort = 0;
         ctl.never = 0;
         fence_mbar_init();
@@ -741,7 +802,6 @@ struct LaunchShape {
     size_t smem;
 };
 
-constexpr int kDsv3Hidden = 7168;
 
 // Consumer warps: one thread per 16 hidden columns, rounded up to a
 // multiple of 4 in the one-token kernel (16 for hidden 7168: each of the
@@ -758,7 +818,9 @@ static fp9_status expert_shape(int32_t H, int MT, LaunchShape& s) {
     if (optin <= 0) return FP9_ERR_CUDA;
     int R = nw / 2 > 4 ? nw / 2 : 4;
     if (R > kMaxRows) R = kMaxRows;
-    const size_t fixed = kCtlBytes + (x_bytes(H, MT) + 127u) / 128u * 128u;
+    // the down helpers' y hand-over (one-token kernel at hidden 7168): 2 x 32 lanes x 16 floats
+    const size_t helpers = (MT == 1 && H == kDsv3Hidden) ? 2 * 32 * kDownCols * sizeof(float) : 0;
+    const size_t fixed = kCtlBytes + (x_bytes(H, MT) + 127u) / 128u * 128u + helpers;
     while (R > 1 && fixed + kSlots * static_cast<size_t>(stage_bytes(H, R)) > static_cast<size_t>(optin)) --R;
     if (fixed + kSlots * static_cast<size_t>(stage_bytes(H, R)) > static_cast<size_t>(optin)) return FP9_ERR_SHAPE;
     s.rows = R;
