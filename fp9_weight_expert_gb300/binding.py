@@ -253,6 +253,23 @@ def fp9_moe_forward_host(layer, x_host: torch.Tensor, y_host: torch.Tensor, ws: 
                                        _stream(stream)), "fp9_moe_forward_host")
 
 
+def host_forward_fn(layer, ws: torch.Tensor, status: torch.Tensor | None = None, stream=None):
+    """fp9_moe_forward_host with the layer, the workspace, the status word and
+    the stream marshalled once: returns f(x_host, y_host) for a per-step
+    loop, which passes only the two host buffers' addresses per call (the
+    generic wrapper spends some microseconds of Python per call on
+    argument conversion). x_host, y_host: pinned CPU tensors [bsz, hidden]."""
+    fn = load().fp9_moe_forward_host
+    lp = ctypes.byref(layer.c_struct())
+    wp, wn, sp, st = _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)
+
+    def call(x_host: torch.Tensor, y_host: torch.Tensor) -> None:
+        code = fn(lp, x_host.data_ptr(), x_host.shape[0], y_host.data_ptr(), wp, wn, sp, st)
+        if code != FP9_OK:
+            raise Fp9Error(code, "fp9_moe_forward_host")
+    return call
+
+
 def fp9_dense_ffn(ffn, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
                   status: torch.Tensor | None = None, stream=None) -> None:
     _check(load().fp9_dense_ffn(ctypes.byref(ffn.c_struct()), _ptr(x), x.shape[0], _ptr(y),

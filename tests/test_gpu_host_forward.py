@@ -50,3 +50,28 @@ def test_host_forward_rejects_a_short_workspace_and_device_tensors():
     assert e.value.code == binding.FP9_ERR_WORKSPACE
     with pytest.raises(ValueError):
         binding.fp9_moe_forward_host(L, xh.cuda(), yh, Workspace.for_moe_host(L, 1).tensor, status)
+
+
+def test_prepared_host_forward_equals_the_generic_call():
+    """binding.host_forward_fn (arguments marshalled once, for per-step
+    loops) runs the same call: y equal bit for bit over several steps, and
+    the same error for a short workspace."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = synth.TINY
+    L = support.build_layer(shape, base=995, status=status)
+    wsh = Workspace.for_moe_host(L, 2)
+    f = binding.host_forward_fn(L, wsh.tensor, status)
+    wr = L.w_router.cpu().numpy()
+    for step in range(3):
+        xh = support.safe_tokens(shape, wr, 2, 996 + step).pin_memory()
+        y1 = torch.empty((2, shape.hidden), dtype=torch.float32).pin_memory()
+        y2 = torch.empty_like(y1).pin_memory()
+        f(xh, y1)
+        binding.fp9_moe_forward_host(L, xh, y2, wsh.tensor, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(y1, y2)
+    g = binding.host_forward_fn(L, Workspace.for_moe(L, 2).tensor, status)
+    with pytest.raises(binding.Fp9Error) as e:
+        g(xh, y1)
+    assert e.value.code == binding.FP9_ERR_WORKSPACE
