@@ -366,8 +366,8 @@ def _native(args):
             "h2d_bytes_per_step": bsz * H * 4,
             "d2h_bytes_per_step": bsz * H * 4,
             "steps": Ke,
-            "api": "fp9_moe_forward_host (pinned host x and y, through binding.host_forward_fn) + stream "
-                   "synchronise, per step",
+            "api": "fp9_moe_forward_host (pinned host x and y, through binding.host_forward_fn: x copied in, "
+                   "y written to host memory by the last kernel) + stream synchronise, per step",
         },
         "gpu_launches": 3 * K,
         "clocks": clocks,

@@ -632,10 +632,22 @@ extern "C" fp9_status fp9_moe_forward_host(const fp9_moe_layer* layer, const flo
     float* yd = reinterpret_cast<float*>(w + align_up(base) + stage);
     const size_t bytes = sizeof(float) * static_cast<size_t>(bsz) * static_cast<size_t>(layer->hidden);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A page-locked y_host that the device can address (its device address
+    // from cudaPointerGetAttributes, 16-byte aligned) is written by the
+    // combine kernel itself: no copy back is queued after it.
+    float* y_direct = nullptr;
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess) {
+        if (pa.type == cudaMemoryTypeHost && pa.devicePointer != nullptr && aligned(pa.devicePointer, 16))
+            y_direct = static_cast<float*>(pa.devicePointer);
+    } else {
+        (void)cudaGetLastError();  // an address the runtime does not know: copy back
+    }
     FP9_CUDA_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
-    st = fp9_moe_forward(layer, xd, bsz, yd, nullptr, nullptr, ws, base, d_status, stream);
+    st = fp9_moe_forward(layer, xd, bsz, y_direct != nullptr ? y_direct : yd, nullptr, nullptr, ws, base, d_status,
+                         stream);
     if (st != FP9_OK) return st;
-    FP9_CUDA_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    if (y_direct == nullptr) FP9_CUDA_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
     return FP9_OK;
 }
 

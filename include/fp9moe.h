@@ -248,13 +248,16 @@ fp9_status fp9_moe_forward_residual(const fp9_moe_layer* layer, const float* x,
  * instead of a copy, the forward and a copy). This is an interface of this
  * library only; the pages have no counterpart.
  *   x_host, y_host: host fp32 [bsz, hidden]. With page-locked memory both
- *   copies are asynchronous and the call returns at once. With a pageable
+ *   transfers are asynchronous and the call returns at once. With a pageable
  *   y_host the call is synchronous: the copy of y back to pageable memory
  *   returns only once it is done, i.e. after the whole forward (a pageable
- *   x_host only makes the copy of x finish before the call returns). Queued on `stream`: the copy
- *   of x into the workspace, the forward, the copy of y back. y_host holds
- *   the result once the stream has reached that point (synchronise the
- *   stream, or wait on an event recorded after the call).
+ *   x_host only makes the copy of x finish before the call returns). Queued
+ *   on `stream`: the copy of x into the workspace, the forward, and the copy
+ *   of y back, except for a page-locked y_host that the device can address
+ *   (cudaPointerGetAttributes gives it a device address, 16-byte aligned),
+ *   which the forward's last kernel writes directly. y_host holds the result
+ *   once the stream has reached that point (synchronise the stream, or wait
+ *   on an event recorded after the call).
  *   ws: device, >= fp9_moe_host_workspace_bytes(layer, bsz), 256-byte
  *   aligned: fp9_moe_forward's workspace followed by two staging rows.
  *   Errors: as fp9_moe_forward; FP9_ERR_CUDA if a copy cannot be queued.
