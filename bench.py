@@ -534,7 +534,7 @@ def _moe_prefill_run(Ls, status, dev, shape, lengths):
 
 
 def _stack_run(dev, shape, n_layers=12, K=1000):
-    """The 12-layer stack of the workload (config 5): 12 distinct resident
+    """The 12-layer stack of the workload: 12 distinct resident
     DeepSeek-V3 MoE layers (153 GB) with the residual + RMSNorm between
     them, h <- h + MoE_l(RMSNorm(h)); the whole stack step is captured once
     in a CUDA graph and replayed K = 1000 times (the workload's steady
@@ -819,7 +819,7 @@ class _ExpertPool:
 
 
 def _oracle_layer_setup():
-    """Config 2 (one DeepSeek-V3 MoE layer, bsz 1): the router weight, one
+    """One DeepSeek-V3 MoE layer at bsz 1: the router weight, one
     token, its routing (oracle) and the experts it needs."""
     import oracle as O
     from fp9_weight_expert_gb300 import synth
@@ -845,11 +845,12 @@ def _layer_all_cores(pool, x, wr, shape, w, one_core=False):
 def _cpu_sample_worker(spec: str):
     """Oracle timing, CPU only (see _cpu_baseline).
 
-    mode 'layer' (the bench's cpu_baseline): config 2 on one core (the
-    oracle's moe() on one token, two passes) and on all cores (the layer's 9
-    expert FFNs on 9 worker processes); then configs 1, 3 and 4 from the
-    measured per-expert times, scaled to each config's expert count.
-    mode 'ref' (the reference arm): `steps` timed layer steps of config 2 on
+    mode 'layer' (the bench's cpu_baseline): the DeepSeek-V3 layer at bsz 1
+    on one core (the oracle's moe() on one token, two passes) and on all
+    cores (the layer's 9 expert FFNs on 9 worker processes); then the tiny
+    layer (measured), the layer at bsz 2, 5 and 8 and the dense FFN (from the
+    measured per-expert times, scaled to each workload's expert count).
+    mode 'ref' (the reference arm): `steps` timed steps of that layer on
     all cores after `warmup` untimed ones.
     """
     import numpy as np
@@ -882,7 +883,7 @@ def _cpu_sample_worker(spec: str):
                           f"8 routed + 1 shared expert FFNs (fp64 numpy, one BLAS thread each) on {workers} worker "
                           f"processes side by side ({used} of {ncores} host cores busy), added as moe() adds them"}))
             return
-        # all cores: config 2, two timed passes after one untimed
+        # all cores: the DeepSeek-V3 layer at bsz 1, two timed passes after one untimed
         _layer_all_cores(pool, x, wr, shape, w)
         t0 = time.perf_counter()
         for _ in range(2):
@@ -901,7 +902,7 @@ def _cpu_sample_worker(spec: str):
     ids8, _ = O.route(xs8, wr, shape.n_groups, shape.topk_groups, shape.topk, shape.route_scale)
     t_route8 = time.perf_counter() - t0
     configs = {}
-    # config 1: the tiny layer, measured directly (L2-sized, one core)
+    # the tiny layer (hidden 256, 8 experts), measured directly (one core)
     tiny = synth.TINY
 
     def tiny_planes(kind, k):
@@ -923,7 +924,7 @@ def _cpu_sample_worker(spec: str):
     configs["tiny_bsz1"] = {"tok_s_1core": round(1.0 / t_tiny, 2), "measured": "directly (moe(), 50 passes)"}
     configs["dsv3_bsz1"] = {"tok_s_1core": round(1.0 / t_one, 5), "tok_s_all_cores": round(1.0 / t_all, 5),
                             "measured": "directly"}
-    # config 3: bsz 2, 5, 8 tokens drawn independently; the oracle decodes
+    # the DeepSeek-V3 layer at bsz 2, 5, 8 (tokens drawn independently); the oracle decodes
     # each distinct expert once and runs one FFN per (token, expert) pair
     for bsz in (2, 5, 8):
         U = len(set(ids8[:bsz].flatten().tolist())) + shape.n_shared
@@ -936,14 +937,14 @@ def _cpu_sample_worker(spec: str):
                                      "measured": "scaled from the per-expert times (decode once per expert, one "
                                                  "FFN per token and expert; all cores: one expert per core, "
                                                  "rounds of the measured all-core layer time)"}
-    # config 4: the dense FFN (18432 = 9 x 2048 rows) costs 9 expert FFNs
+    # the dense FFN 7168 / 18432 (18432 = 9 x 2048 rows) costs 9 expert FFNs
     for bsz in (1, 2):
         t1 = 9 * t_dec + 9 * bsz * t_tok
         configs[f"dense_bsz{bsz}"] = {"tok_s_1core": round(bsz / t1, 5),
                                       "tok_s_all_cores": round(bsz / (t_all + (bsz - 1) * t_tok), 5),
                                       "measured": "scaled: 9 x one expert's decode + FFN (one core); all cores: "
                                                   "its 9 row blocks of 2048 side by side, as the 9 expert FFNs "
-                                                  "of config 2, plus one more token's FFN per extra token"}
+                                                  "of the bsz-1 layer, plus one more token's FFN per extra token"}
     print(json.dumps({
         "value": round(1.0 / t_all, 5), "unit": "tok/s", "cores": used, "host_cores": ncores, "kind": "oracle",
         "seconds_all_cores": round(t_all, 4), "one_core": {"value": round(1.0 / t_one, 5), "cores": 1,
