@@ -292,6 +292,10 @@ def _native(args):
     mean_kern_s = sum(kern_ms) / Kk / 1e3
     kernel_gbs = (sum(weight_bytes[:Kk]) / Kk) / mean_kern_s / 1e9
     step_gbs = sum(weight_bytes) / (elapsed_ms / 1e3) / 1e9
+    # all algorithmic bytes of a step: the fp9 weights, the fp32 router
+    # weights (4 E H) and x and y (8 bsz H)
+    other_bytes = 4 * shape.n_experts * H + 8 * bsz * H
+    total_gbs = (sum(weight_bytes) + K * other_bytes) / (elapsed_ms / 1e3) / 1e9
     peak, peak_kind = _peaks()
 
     # end to end through the C ABI with host buffers: one fp9_moe_forward_host
@@ -359,6 +363,7 @@ def _native(args):
                              "same steps (value comes from the pass with no events between launches)",
         },
         "weight_stream_gbs_per_step": round(step_gbs, 1),
+        "total_gbs_per_step": round(total_gbs, 1),
         "us_per_layer": round(elapsed_ms / K * 1e3, 2),
         "e2e": {
             "value": round(replica_throughput(world, bsz, Ke, e2e_s), 2),
