@@ -41,6 +41,9 @@ constexpr int kTokensPerJob = 2;
 // work units of one intermediate row of a job holding 1 or 2 tokens
 constexpr int32_t kRowCost1 = 8, kRowCost2 = 11;
 __host__ __device__ inline int32_t row_cost(int32_t ntok) { return ntok == 2 ? kRowCost2 : kRowCost1; }
+// the router's split charges a CTA whose range crosses a job boundary this
+// many one-token rows (the extra part-filled chunk it walks)
+constexpr int32_t kJobGapRows = 4;
 
 // Job flags. kJobReread: another job of the same call streams these rows
 // too (an expert chosen by several tokens, a shared expert at bsz >= 2);

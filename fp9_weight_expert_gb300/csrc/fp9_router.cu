@@ -369,19 +369,25 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         s_jobs[before] = j;
     }
     __syncthreads();
-    // Work units: job j's rows start at unit I * C_j, C_j the summed row
-    // costs of the jobs before it; each CTA gets U / G units. G is capped so
-    // that a CTA's share is at least one row of the dearest job, which
+    // Work units: job j's rows start at unit I * C_j + j * gap, C_j the
+    // summed row costs of the jobs before it; each CTA gets U / G units. The
+    // gap between two jobs is the cost of kJobGapRows one-token rows: a CTA
+    // whose range crosses a job boundary walks one more part-filled chunk
+    // (a chunk never spans two jobs), and every chunk costs a hand-off
+    // whatever its rows (measured: such CTAs ended 2-3 us after the median,
+    // about four rows of work), so it gets that many rows fewer. G is capped
+    // so that a CTA's share is at least one row of the dearest job, which
     // leaves no CTA without a row.
     const int32_t cj = tid < J ? row_cost(s_jobs[tid].ntok) : 0;
     int32_t ctot = 0;
     const int32_t cpre = block_exclusive_scan(cj, tid, ctot);
-    const int64_t U = a.I * ctot;
+    const int64_t gap = static_cast<int64_t>(kJobGapRows) * kRowCost1;
+    const int64_t U = a.I * ctot + (J - 1) * gap;
     const int32_t cmax = (a.bsz >= 2 && a.tpj == 2) ? kRowCost2 : kRowCost1;
     int64_t G = U / cmax;
     G = G > a.grid ? a.grid : (G < 1 ? 1 : G);
     if (tid < J) {
-        s_u0[tid] = a.I * cpre;
+        s_u0[tid] = a.I * cpre + tid * gap;
         s_cost[tid] = cj;
         a.jobs[tid] = s_jobs[tid];
     }
@@ -396,7 +402,8 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
             if (s_u0[mid] <= us) lo = mid;
             else hi = mid - 1;
         }
-        const int64_t r = (us - s_u0[lo] + s_cost[lo] - 1) / s_cost[lo];
+        int64_t r = (us - s_u0[lo] + s_cost[lo] - 1) / s_cost[lo];
+        if (r > a.I) r = a.I;  // in the gap after job lo: the next job's first row
         a.cta_row[b] = static_cast<int64_t>(lo) * a.I + r;
     }
     if (tid == 0) {
