@@ -42,8 +42,9 @@ constexpr int kTokensPerJob = 2;
 constexpr int32_t kRowCost1 = 8, kRowCost2 = 11;
 __host__ __device__ inline int32_t row_cost(int32_t ntok) { return ntok == 2 ? kRowCost2 : kRowCost1; }
 // the router's split charges a CTA whose range crosses a job boundary this
-// many one-token rows (the extra part-filled chunk it walks)
-constexpr int32_t kJobGapRows = 4;
+// many one-token rows (the extra part-filled chunk it walks; 0, 4, 8 and 12
+// were measured: 8 gave the shortest DeepSeek-V3 layer steps at bsz 1 to 8)
+constexpr int32_t kJobGapRows = 8;
 
 // Job flags. kJobReread: another job of the same call streams these rows
 // too (an expert chosen by several tokens, a shared expert at bsz >= 2);

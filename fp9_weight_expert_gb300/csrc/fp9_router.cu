@@ -373,9 +373,10 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
     // summed row costs of the jobs before it; each CTA gets U / G units. The
     // gap between two jobs is the cost of kJobGapRows one-token rows: a CTA
     // whose range crosses a job boundary walks one more part-filled chunk
-    // (a chunk never spans two jobs), and every chunk costs a hand-off
-    // whatever its rows (measured: such CTAs ended 2-3 us after the median,
-    // about four rows of work), so it gets that many rows fewer. G is capped
+    // (a chunk never spans two jobs, and at bsz >= 2 the tokens may change
+    // there: y is flushed and x staged again), and every chunk costs a
+    // hand-off whatever its rows (measured: such CTAs ended 2-3 us after the
+    // median), so it gets that many rows fewer. G is capped
     // so that a CTA's share is at least one row of the dearest job, which
     // leaves no CTA without a row.
     const int32_t cj = tid < J ? row_cost(s_jobs[tid].ntok) : 0;
