@@ -119,17 +119,18 @@ __device__ __forceinline__ uint32_t encode_product(float x, float s, uint32_t& s
 // 再让 Qwen3.5 充当高压试炼场"). Every weight of a block is its e4m3 value times
 // the block's scale s, rounded once to fp9 (encode_product), so the body
 // depends only on the code's magnitude: per block the CTA encodes the 128
-// magnitudes |e4m3(c)| * |s| into a table indexed by the whole code byte
-// (256 bytes, each body stored for both signs, so no mask is needed before
-// a lookup), then each weight is one shared-memory byte read. Rounding to
-// nearest is symmetric, so the product's sign is the code's sign xor the
-// scale's sign; a NaN product (a NaN code, 0 * Inf, a NaN scale) is the
-// canonical NaN of the multiply, sign 0.
+// magnitudes |e4m3(c)| * |s| into a table indexed by the code's 7
+// magnitude bits (128 bytes), then each weight is one shared-memory byte
+// read. Rounding to nearest is symmetric, so the product's sign is the
+// code's sign xor the scale's sign; a NaN product (a NaN code, 0 * Inf, a
+// NaN scale) is the canonical NaN of the multiply, sign 0.
 //
-// Grid: x = block column, y = block row (a CTA walks the block rows
-// blockIdx.y, + gridDim.y, ... so any row count fits the 65535 limit).
-// 256 threads; a thread converts kUnits units of G consecutive weights of
-// a row (G = 16, or 8 when cols % 16 != 0).
+// Matrices with a ragged block (rows or cols not a multiple of 128) take
+// fp8_to_fp9_kernel: grid x = block column, y = block row (a CTA walks the
+// block rows blockIdx.y, + gridDim.y, ... so any row count fits the 65535
+// limit), 256 threads, a thread converting kUnits units of G consecutive
+// weights of a row (G = 16, or 8 when cols % 16 != 0). Matrices of whole
+// blocks take fp8_to_fp9_full_kernel (below).
 template <int G>
 struct Fp8Block {
     static constexpr int kUnits = 128 * 128 / G / 256;  // units of G weights per thread
@@ -187,13 +188,15 @@ __device__ __forceinline__ uint32_t gather_signs8(uint32_t v0, uint32_t v1) {
     return ((v1 & 0x80808080u) | ((v0 >> 4) & 0x08080808u)) * 0x00204081u;
 }
 
-// Encodes the block's table (threads 0..127) and converts the block's units
-// of this thread; returns whether any weight landed on an Inf or NaN body.
-template <int G>
-__device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t* tab, uint8_t* __restrict__ body,
-                                                  uint8_t* __restrict__ sign) {
+// Threads 0..127 write the table of a block of scale `scale`: entry c holds
+// the fp9 body of |e4m3(c)| * |scale|, c < 128 (a code's magnitude bits).
+// 128 bytes are one word per shared-memory bank, so a warp's lookups never
+// conflict: lanes reading one magnitude (of either sign) read one word.
+// Returns whether this thread's entry is an Inf or NaN body for a finite
+// code: the NaN code's entry (c = 0x7F) is the NaN body whatever the scale,
+// so NaN codes are looked for in the codes themselves (fp8_nan_bits).
+__device__ __forceinline__ bool fp8_table_entry(uint8_t* tab, float scale) {
     bool range = false;
-    __syncthreads();  // the previous block's lookups are done
     if (threadIdx.x < 128) {
         // |e4m3(c)| for c < 128: the hardware conversion of the code pair
         // (c, c) to fp16, then fp32
@@ -201,54 +204,81 @@ __device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t*
             __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(threadIdx.x * 0x101u), __NV_E4M3);
         const float x = __low2float(*reinterpret_cast<const __half2*>(&hr));
         uint32_t sb;
-        const uint8_t e = static_cast<uint8_t>(encode_product(x, fabsf(B.scale), sb, range));
+        const uint8_t e = static_cast<uint8_t>(encode_product(x, fabsf(scale), sb, range));
         tab[threadIdx.x] = e;
-        tab[threadIdx.x + 128] = e;
     }
-    // a block whose table holds an Inf or NaN body checks its weights
-    const int special = __syncthreads_or(range ? 1 : 0);
-    // all-ones over the unit's sign bits when the scale is negative
+    return range && threadIdx.x != 0x7Fu;
+}
+
+// For m = the magnitude bits of four e4m3 codes (a word & 0x7F7F7F7F):
+// bit 7 of a byte is set when that code is a NaN code (magnitude bits all
+// ones): a byte's 7 bits plus one reach its bit 7 only then, and never
+// carry into the next byte.
+__device__ __forceinline__ uint32_t fp8_nan_bits(uint32_t m) { return (m + 0x01010101u) & 0x80808080u; }
+
+// One unit of G codes (words in[0 .. G/4)) through the block's table:
+// writes unit g of the body and sign planes. `sflip` is all-ones over the
+// unit's sign bits when the scale is negative; `special` says a finite
+// code's product overflows in this block. When that holds or the unit has
+// a NaN code, each body is checked, and `hit` is set if one is Inf or NaN.
+template <int G>
+__device__ __forceinline__ void fp8_unit_convert(const uint32_t (&in)[G / 4], const uint8_t* tab, uint32_t sflip,
+                                                 bool special, int64_t g, uint8_t* __restrict__ body,
+                                                 uint8_t* __restrict__ sign, bool& hit) {
+    uint32_t out[G / 4];
+    uint32_t nan = 0;
+#pragma unroll
+    for (int w = 0; w < G / 4; ++w) {
+        const uint32_t m = in[w] & 0x7F7F7F7Fu;
+        nan |= fp8_nan_bits(m);
+        const uint32_t b0 = tab[m & 0xFFu], b1 = tab[__byte_perm(m, 0u, 0x4441u)];
+        const uint32_t b2 = tab[__byte_perm(m, 0u, 0x4442u)], b3 = tab[m >> 24];
+        // the bytes do not overlap, so the adds are ors; written as
+        // multiply-adds they can share the integer multiply pipe
+        out[w] = (b3 * 256u + b2) * 65536u + (b1 * 256u + b0);
+    }
+    uint32_t sb;
+    if constexpr (G == 16)
+        sb = __byte_perm(gather_signs8(in[0], in[1]), gather_signs8(in[2], in[3]), 0x0073u);
+    else
+        sb = gather_signs8(in[0], in[1]) >> 24;
+    sb ^= sflip;
+    if (special || nan != 0) {
+        // bytes 0xF8..0xFF (Inf 0xF8, NaN 0xFC): flag them; NaN is unsigned
+#pragma unroll
+        for (int w = 0; w < G / 4; ++w) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t bk = (out[w] >> (8 * k)) & 0xFFu;
+                if ((bk & 0xF8u) == 0xF8u) hit = true;
+                if (bk == 0xFCu) sb &= ~(1u << (4 * w + k));
+            }
+        }
+    }
+    if constexpr (G == 16) {
+        __stcs(reinterpret_cast<uint4*>(body) + g, make_uint4(out[0], out[1], out[2], out[3]));
+        reinterpret_cast<uint16_t*>(sign)[g] = static_cast<uint16_t>(sb);
+    } else {
+        __stcs(reinterpret_cast<uint2*>(body) + g, make_uint2(out[0], out[1]));
+        sign[g] = static_cast<uint8_t>(sb);
+    }
+}
+
+// Encodes the block's table (threads 0..127) and converts the block's units
+// of this thread; returns whether any weight landed on an Inf or NaN body.
+template <int G>
+__device__ __forceinline__ bool fp8_block_convert(const Fp8Block<G>& B, uint8_t* tab, uint8_t* __restrict__ body,
+                                                  uint8_t* __restrict__ sign) {
+    __syncthreads();  // the previous block's lookups are done
+    const bool range = fp8_table_entry(tab, B.scale);
+    // a block with an overflowing product checks all its weights
+    const bool special = __syncthreads_or(range ? 1 : 0) != 0;
     const uint32_t sflip = (__float_as_uint(B.scale) >> 31) ? (1u << G) - 1u : 0u;
     bool hit = false;
 #pragma unroll
     for (int j = 0; j < Fp8Block<G>::kUnits; ++j) {
         if (B.g[j] < 0) continue;
-        const int64_t g = B.g[j];
-        uint32_t out[G / 4];
-#pragma unroll
-        for (int w = 0; w < G / 4; ++w) {
-            const uint32_t v = B.in[j][w];
-            const uint32_t b0 = tab[v & 0xFFu], b1 = tab[__byte_perm(v, 0u, 0x4441u)];
-            const uint32_t b2 = tab[__byte_perm(v, 0u, 0x4442u)], b3 = tab[__umulhi(v, 256u)];
-            // the bytes do not overlap, so the adds are ors; written as
-            // multiply-adds they can share the integer multiply pipe
-            out[w] = (b3 * 256u + b2) * 65536u + (b1 * 256u + b0);
-        }
-        uint32_t sb;
-        if constexpr (G == 16)
-            sb = __byte_perm(gather_signs8(B.in[j][0], B.in[j][1]), gather_signs8(B.in[j][2], B.in[j][3]), 0x0073u);
-        else
-            sb = gather_signs8(B.in[j][0], B.in[j][1]) >> 24;
-        sb ^= sflip;
-        if (special) {
-            // bytes 0xF8..0xFF (Inf 0xF8, NaN 0xFC): flag them; NaN is unsigned
-#pragma unroll
-            for (int w = 0; w < G / 4; ++w) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t bk = (out[w] >> (8 * k)) & 0xFFu;
-                    if ((bk & 0xF8u) == 0xF8u) hit = true;
-                    if (bk == 0xFCu) sb &= ~(1u << (4 * w + k));
-                }
-            }
-        }
-        if constexpr (G == 16) {
-            __stcs(reinterpret_cast<uint4*>(body) + g, make_uint4(out[0], out[1], out[2], out[3]));
-            reinterpret_cast<uint16_t*>(sign)[g] = static_cast<uint16_t>(sb);
-        } else {
-            __stcs(reinterpret_cast<uint2*>(body) + g, make_uint2(out[0], out[1]));
-            sign[g] = static_cast<uint8_t>(sb);
-        }
+        fp8_unit_convert<G>(B.in[j], tab, sflip, special, B.g[j], body, sign, hit);
     }
     return hit;
 }
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restri
                                                          int64_t cols, int64_t nbx, int64_t nby,
                                                          uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
                                                          int32_t* status) {
-    __shared__ uint8_t tab[256];
+    __shared__ uint8_t tab[128];
     bool hit = false;
     // a block's codes are loaded before its table is built, so they are in
     // flight meanwhile
@@ -268,6 +298,79 @@ __global__ void __launch_bounds__(256) fp8_to_fp9_kernel(const uint8_t* __restri
         fp8_block_load<G>(w8, scale, rows, cols, nbx, by, A);
         hit |= fp8_block_convert<G>(A, tab, body, sign);
     }
+    if (hit) record_status(status, FP9_ERR_RANGE);
+}
+
+// Matrices of whole 128 x 128 blocks (rows and cols multiples of 128, such
+// as every DeepSeek-V3 expert matrix): a persistent grid of a few CTAs per
+// SM, CTA k converting blocks k, k + gridDim.x, ... in row-major block
+// order. Thread t owns the units of 16 codes at rows (t >> 3) + 32 j,
+// j = 0..3, columns 16 (t & 7) .. + 15 of each block it visits. Per block:
+// one barrier publishes the block's table (built during the previous
+// block); the codes of the CTA's next block are loaded and its table is
+// built, from a scale loaded a block earlier, before this block's lookups,
+// so the loads are in flight and no warp idles at the barrier while the
+// table is encoded. The table is double-buffered: the barrier that
+// publishes one buffer also orders every lookup into the other (the
+// previous block's) before that buffer is written again.
+// Three CTAs per SM: with four, 64 registers a thread held the kernel at
+// 132 against 127 us on 24 DeepSeek-V3 expert matrices; two were slower.
+constexpr int kFp8FullCtasPerSm = 3;
+
+struct Fp8Full {
+    uint32_t in[4][4];  // unit j: rows (t >> 3) + 32 j
+    int64_t base;       // index of unit 0's first code
+    float scale;
+};
+
+__device__ __forceinline__ void fp8_full_load(const uint8_t* __restrict__ w8, int64_t cols, int64_t nbx,
+                                              int64_t b, int64_t toff, Fp8Full& B) {
+    const int64_t by = b / nbx, bx = b - by * nbx;
+    B.base = by * 128 * cols + bx * 128 + toff;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w8 + B.base + j * 32 * cols));
+        B.in[j][0] = q.x, B.in[j][1] = q.y, B.in[j][2] = q.z, B.in[j][3] = q.w;
+    }
+}
+
+__global__ void __launch_bounds__(256, kFp8FullCtasPerSm)
+    fp8_to_fp9_full_kernel(const uint8_t* __restrict__ w8, const float* __restrict__ scale, int64_t cols,
+                           int64_t nbx, int64_t nblocks, uint8_t* __restrict__ body, uint8_t* __restrict__ sign,
+                           int32_t* status) {
+    __shared__ uint8_t tab[2][128];
+    const int64_t G = gridDim.x;
+    const int64_t toff = static_cast<int64_t>(threadIdx.x >> 3) * cols + (threadIdx.x & 7) * 16;
+    int64_t b = blockIdx.x;
+    if (b >= nblocks) return;  // (the grid holds at most nblocks CTAs)
+    bool hit = false;
+    Fp8Full A, B;
+    fp8_full_load(w8, cols, nbx, b, toff, A);
+    A.scale = __ldg(scale + b);  // scales are [nby, nbx]: block b's is at b
+    float s_next = b + G < nblocks ? __ldg(scale + b + G) : 0.0f;
+    bool range = fp8_table_entry(tab[0], A.scale);  // the table of the block about to be published
+    int p = 0;
+    // block bc (codes in C) with table p; loads the next block into N
+    auto step = [&](const Fp8Full& C, Fp8Full& N, int64_t bc) -> bool {
+        const int64_t bn = bc + G;
+        const bool more = bn < nblocks;
+        if (more) {
+            fp8_full_load(w8, cols, nbx, bn, toff, N);
+            N.scale = s_next;
+            if (bn + G < nblocks) s_next = __ldg(scale + bn + G);
+        }
+        // a block with an overflowing product checks all its weights
+        const bool special = __syncthreads_or(range ? 1 : 0) != 0;
+        if (more) range = fp8_table_entry(tab[p ^ 1], N.scale);
+        const uint32_t sflip = (__float_as_uint(C.scale) >> 31) ? 0xFFFFu : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            fp8_unit_convert<16>(C.in[j], tab[p], sflip, special, (C.base + j * 32 * cols) >> 4, body, sign, hit);
+        p ^= 1;
+        return more;
+    };
+    // two blocks per trip, A then B, so that neither is copied
+    while (step(A, B, b) && step(B, A, b + G)) b += 2 * G;
     if (hit) record_status(status, FP9_ERR_RANGE);
 }
 
@@ -335,8 +438,18 @@ extern "C" fp9_status fp9_from_fp8(const uint8_t* w8, const float* scale_inv, in
     const bool wide = cols % 16 == 0 && aligned(w8, 16) && aligned(body, 16) && aligned(sign, 2);
     const int64_t nbx = (cols + 127) / 128, nby = (rows + 127) / 128;
     FP9_CHECK_ARG(nbx <= 0x7FFFFFFF, FP9_ERR_SHAPE);  // one grid column per block column
-    const dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(nby < 65535 ? nby : 65535));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (wide && rows % 128 == 0 && cols % 128 == 0) {
+        const int64_t nblocks = nbx * nby;
+        int32_t sms = device_sm_count();
+        if (sms <= 0) sms = 148;
+        const int64_t cap = static_cast<int64_t>(sms) * kFp8FullCtasPerSm;
+        fp8_to_fp9_full_kernel<<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), 256, 0, st>>>(
+            w8, scale_inv, cols, nbx, nblocks, body, sign, d_status);
+        FP9_CUDA_TRY(cudaGetLastError());
+        return FP9_OK;
+    }
+    const dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(nby < 65535 ? nby : 65535));
     if (wide)
         fp8_to_fp9_kernel<16><<<grid, 256, 0, st>>>(w8, scale_inv, rows, cols, nbx, nby, body, sign, d_status);
     else

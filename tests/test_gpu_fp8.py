@@ -2,7 +2,8 @@
 against the oracle: bit-exact body and sign planes, the range status, on
 random codes and scales, ragged shapes (partial scale blocks, one group),
 the hand-derived worked examples, products whose fp32 rounding lands on an
-fp9 midpoint, and a full DeepSeek-V3 expert matrix."""
+fp9 midpoint, and a full DeepSeek-V3 expert matrix. Ragged matrices take
+the one-block-per-CTA kernel, matrices of whole blocks the persistent one."""
 
 import numpy as np
 import pytest
@@ -92,6 +93,64 @@ def test_full_dsv3_expert_matrix():
     w8[(w8 & 0x7F) == 0x7F] = 0x3C
     # checkpoint-like scales: weight magnitudes around 1e-2 after scaling
     scale = (np.exp2(rng.uniform(-14, -10, size=(rows // 128, cols // 128)))).astype(np.float32)
+    _check(w8, scale)
+
+
+def _midpoint_witnesses():
+    """(code, scale) pairs whose fp32 product is an fp9 midpoint while the
+    exact product is not (the oracle's rounding is decided by the latter)."""
+    out = []
+    for code in range(256):
+        x = float(O.e4m3_value(code))
+        if not np.isfinite(x) or x == 0:
+            continue
+        for mid in [1.0625 + 0.125 * j for j in range(8)]:
+            s0 = np.float32(mid / abs(x))
+            for step in (-1, 1):
+                sc = np.nextafter(s0, np.float32(np.inf) if step > 0 else np.float32(-np.inf))
+                if abs(float(np.float32(x) * sc)) == mid and abs(x * float(sc)) != mid:
+                    out.append((code, sc))
+    return out
+
+
+@pytest.mark.parametrize("case", ["random", "nan", "overflow", "midpoints"])
+def test_whole_blocks(case):
+    """Matrices of whole 128 x 128 blocks run the persistent kernel, whose
+    CTAs walk several blocks (here 45): bit-exact planes and the range
+    status without NaN codes, with a NaN code in two blocks, with one block
+    whose products overflow, and with blocks whose scale puts the fp32
+    product of one code on an fp9 midpoint."""
+    rows, cols = 640, 1152
+    rng = np.random.default_rng(["random", "nan", "overflow", "midpoints"].index(case) + 40)
+    w8 = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3C
+    scale = (np.exp2(rng.uniform(-14, 6, size=(5, 9))) * rng.choice([1, -1], size=(5, 9))).astype(np.float32)
+    if case == "nan":
+        w8[130, 700] = 0x7F
+        w8[639, 5] = 0xFF
+    elif case == "overflow":
+        scale[2, 3] = np.float32(2.0 ** 14)  # 448 * 2^14 is past the fp9 range
+    elif case == "midpoints":
+        wit = _midpoint_witnesses()
+        assert len(wit) >= 45
+        pick = rng.choice(len(wit), size=45, replace=False)
+        for k, i in enumerate(pick):
+            code, sc = wit[i]
+            by, bx = divmod(k, 9)
+            blk = w8[by * 128:(by + 1) * 128, bx * 128:(bx + 1) * 128]
+            blk[rng.random(blk.shape) < 0.5] = code
+            scale[by, bx] = sc
+    _check(w8, scale)
+
+
+def test_whole_blocks_several_per_cta():
+    # 32 x 56 = 1792 blocks: more than the persistent grid holds at once
+    rng = np.random.default_rng(23)
+    rows, cols = 4096, 7168
+    w8 = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3C
+    scale = (np.exp2(rng.uniform(-14, -10, size=(rows // 128, cols // 128))) *
+             rng.choice([1, -1], size=(rows // 128, cols // 128))).astype(np.float32)
     _check(w8, scale)
 
 
