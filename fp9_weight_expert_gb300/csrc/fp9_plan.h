@@ -45,6 +45,13 @@ __host__ __device__ inline int32_t row_cost(int32_t ntok) { return ntok == 2 ? k
 // many one-token rows (the extra part-filled chunk it walks; 0, 4, 8 and 12
 // were measured: 8 gave the shortest DeepSeek-V3 layer steps at bsz 1 to 8)
 constexpr int32_t kJobGapRows = 8;
+// the router's split evens out each CTA's total of phase-0 and phase-1 rows
+// when phase 0 gives every CTA at least this many rows; with fewer, a CTA is
+// done with phase 0 before the router's plan is ready, so only equal
+// phase-1 shares matter (DeepSeek-V3 layer, evened against equal shares:
+// bsz 1, 14 phase-0 rows, 82.3 against 81.4 us per stacked layer; bsz 2,
+// 27 rows, 148.9 against 149.2; bsz 5 339.3 against 340.6)
+constexpr int32_t kEvenPhase0Rows = 24;
 
 // Job flags. kJobReread: another job of the same call streams these rows
 // too (an expert chosen by several tokens, a shared expert at bsz >= 2);
@@ -161,10 +168,19 @@ inline WsLayout dense_layout(int32_t bsz, int64_t hidden, int32_t grid) {
 // up, so none of them waits for the router to finish.
 inline int32_t expert_grid(int32_t sms, bool moe) { return moe && sms > 1 ? sms - 1 : sms; }
 
+// a / d for a >= 0, d > 0: a 32-bit division when both fit (a 64-bit
+// division is a long emulated sequence on the GPU, and the router's plan,
+// which waits on these, is on the step's critical path)
+__host__ __device__ inline int64_t div_nonneg(int64_t a, int64_t d) {
+    if ((static_cast<uint64_t>(a) >> 32) == 0 && (static_cast<uint64_t>(d) >> 32) == 0)
+        return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(d));
+    return a / d;
+}
+
 // First unit of CTA b, and the CTA that owns unit p, for n units over g
 // CTAs (CTA b owns units [b*n/g, (b+1)*n/g)). With one unit per row and
 // g <= n no CTA is empty.
-__host__ __device__ inline int64_t cta_start(int64_t b, int64_t n, int64_t g) { return b * n / g; }
+__host__ __device__ inline int64_t cta_start(int64_t b, int64_t n, int64_t g) { return div_nonneg(b * n, g); }
 __host__ __device__ inline int64_t cta_of_row(int64_t p, int64_t n, int64_t g) {
     return ((p + 1) * g - 1) / n;
 }

@@ -45,6 +45,7 @@ struct RouterArgs {
     Job* jobs;           // [jmax]
     int64_t* cta_row;    // [grid + 1] first row of each CTA of the fused kernel
     int32_t tpj;         // tokens per job: 1 (an MoE call) or 2
+    int64_t impl_rows;   // the fused kernel's phase-0 rows (shared experts, one token per job)
 };
 
 static_assert(kMaxJobs <= kRouterThreads && kMaxEntries <= kRouterThreads, "one thread per job in the plan scan");
@@ -256,7 +257,7 @@ __device__ int32_t spaced_position(int tid, int J, int64_t G, int pos, int run) 
     __shared__ int s_fail;
     int k = 1, best = J;
     for (int c = 1; c <= 8 && c <= J; ++c) {  // the same choice in every thread
-        const int r = static_cast<int>((c * G) % J);
+        const int r = (c * static_cast<int>(G)) % J;  // G <= the grid: 32-bit arithmetic
         const int d = r < J - r ? r : J - r;
         if (d < best) {
             best = d;
@@ -385,7 +386,7 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
     const int64_t gap = static_cast<int64_t>(kJobGapRows) * kRowCost1;
     const int64_t U = a.I * ctot + (J - 1) * gap;
     const int32_t cmax = (a.bsz >= 2 && a.tpj == 2) ? kRowCost2 : kRowCost1;
-    int64_t G = U / cmax;
+    int64_t G = div_nonneg(U, cmax);
     G = G > a.grid ? a.grid : (G < 1 ? 1 : G);
     if (tid < J) {
         s_u0[tid] = a.I * cpre + tid * gap;
@@ -393,17 +394,34 @@ __device__ void build_jobs(const RouterArgs& a, int tid, const int32_t* s_ids, c
         a.jobs[tid] = s_jobs[tid];
     }
     __syncthreads();
+    // The fused kernel splits phase 0 evenly by rows over min(n0, grid)
+    // CTAs, so they hold one row more or less of it (27 or 28 rows of the
+    // DeepSeek-V3 shared expert at bsz 2). When phase 0 gives every CTA at
+    // least kEvenPhase0Rows rows, phase 1 evens out the totals: CTA b's
+    // first unit is its equal share of both phases less the phase-0 units
+    // of the CTAs before it (taken when every CTA's share exceeds its
+    // phase-0 units by a row: the first units then rise with b and end at
+    // U). Otherwise each CTA gets an equal share of phase 1.
+    const int64_t n0 = a.impl_rows;
+    const int64_t g0 = n0 < a.grid ? n0 : a.grid;
+    const int64_t T = U + n0 * kRowCost1;
+    const bool even = G == a.grid && n0 >= static_cast<int64_t>(kEvenPhase0Rows) * g0 &&
+                      div_nonneg(T, G) >= (div_nonneg(n0 + g0 - 1, g0) + 1) * kRowCost1;
     for (int b = tid; b <= G; b += blockDim.x) {
         // CTA b's first row: the first row whose first unit is at or past
         // the CTA's first unit (b == G: one past the last row)
-        const int64_t us = cta_start(b, U, G);
+        int64_t us = cta_start(b, U, G);
+        if (even) {
+            us = cta_start(b, T, G) - (b < g0 ? cta_start(b, n0, g0) : n0) * kRowCost1;
+            us = us < 0 ? 0 : (us > U ? U : us);
+        }
         int lo = 0, hi = J - 1;  // the last job starting at or before us
         while (lo < hi) {
             const int mid = (lo + hi + 1) / 2;
             if (s_u0[mid] <= us) lo = mid;
             else hi = mid - 1;
         }
-        int64_t r = (us - s_u0[lo] + s_cost[lo] - 1) / s_cost[lo];
+        int64_t r = div_nonneg(us - s_u0[lo] + s_cost[lo] - 1, s_cost[lo]);
         if (r > a.I) r = a.I;  // in the gap after job lo: the next job's first row
         a.cta_row[b] = static_cast<int64_t>(lo) * a.I + r;
     }
@@ -583,6 +601,7 @@ fp9_status launch_router(const fp9_moe_layer* L, const float* x, int32_t bsz, in
     a.I = L->inter;
     a.grid = lay.grid;
     a.tpj = 1;  // an MoE call plans one token per job
+    a.impl_rows = static_cast<int64_t>(L->n_shared) * bsz * L->inter;  // one job per shared expert and token
     // scores and their experts (the fast selection sorts both in place)
     const size_t smem = 2 * sizeof(float) * bsz * L->n_experts;  // <= 64 KB
     static DeviceOnce attr;
