@@ -716,12 +716,19 @@ constexpr int kCombineLanes = kCombineThreads / 4;  // partial lanes per column:
 // CTA's partial for the next layer's RMSNorm.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
     __shared__ float4 red[kCombineThreads / 32][4];
-    grid_dependency_wait();  // all partials are written
-    grid_launch_dependents();
     const int q = threadIdx.x & 3, sl = threadIdx.x >> 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.y;
     const int c = blockIdx.x * kCombineCols + q * 4;
+    const int64_t o4 = (static_cast<int64_t>(t) * a.H + c) / 4;
+    // stack mode: h is read before the wait for the expert kernel, which
+    // does not write it (its last writer, the previous layer's combine, was
+    // complete before this layer's router passed its own wait), so that
+    // load is off the path from the last partial to the new h
+    float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.h != nullptr && threadIdx.x < 4) hv = __ldcg(reinterpret_cast<const float4*>(a.h) + o4);
+    grid_dependency_wait();  // all partials are written
+    grid_launch_dependents();
     const float* base = a.partial + static_cast<int64_t>(t) * a.grid * a.H + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     // the written-masks and the partial rows are loaded together (one round
@@ -767,10 +774,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
             sum.z += o.z;
             sum.w += o.w;
         }
-        const int64_t o4 = (static_cast<int64_t>(t) * a.H + c) / 4;
         if (a.y != nullptr) reinterpret_cast<float4*>(a.y)[o4] = sum;
         if (a.h != nullptr) {
-            float4 v = __ldcg(reinterpret_cast<const float4*>(a.h) + o4);
+            float4 v = hv;
             v.x += sum.x;
             v.y += sum.y;
             v.z += sum.z;

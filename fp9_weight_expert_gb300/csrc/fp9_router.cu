@@ -444,21 +444,35 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     const float4* x4 = reinterpret_cast<const float4*>(a.x);
     const float4* w4 = reinterpret_cast<const float4*>(a.wr) + static_cast<int64_t>(e) * H4;
 
-    // Nothing is read before the wait: the caller may have written x, W_g
-    // or the workspace with the kernel just before this one. W_g is read
-    // with the L2 evict-last hint: the router weights (7.3 MB a layer) stay
-    // in L2 from one step to the next while the expert weights stream
-    // through it evict-first. The first token's x is loaded with them.
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // W_g is read with the L2 evict-last hint: the router weights (7.3 MB a
+    // layer) stay in L2 from one step to the next while the expert weights
+    // stream through it evict-first. In stack mode, where the weights of
+    // many layers take turns and a row may have left L2, the CTA's row is
+    // read before the wait for the kernel queued before this one (the
+    // previous layer's combine), so that those loads overlap its tail: no
+    // kernel of this library writes W_g, and a kernel that does not signal
+    // its dependents early has completed before this one starts (the header
+    // states the one case left to the caller). A plain call reads W_g after
+    // the wait: with the row in L2 the early read gained nothing and
+    // slowed a bsz-2 layer step by 1.1 us (its loads meet the two-token
+    // combine's). x and the workspace are always read after the wait.
     const uint64_t keep = l2_evict_last_policy();
     float4 wv[kRouterVec], x0[kRouterVec];
+    auto load_w = [&] {
+#pragma unroll
+        for (int i = 0; i < kRouterVec; ++i) {
+            const int c = tid + i * kRouterThreads;
+            wv[i] = c < H4 ? ld_global_hint(w4 + c, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    if (kNorm) load_w();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!kNorm) load_w();
 #pragma unroll
     for (int i = 0; i < kRouterVec; ++i) {
         const int c = tid + i * kRouterThreads;
-        const bool in = c < H4;
-        wv[i] = in ? ld_global_hint(w4 + c, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x0[i] = in ? __ldg(x4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x0[i] = c < H4 ? __ldg(x4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     // stack mode: x = h * (1 / sqrt(mean(h^2) + eps)) of each token, the
     // scale of token t formed by warp t from the partial sums of squares

@@ -111,6 +111,12 @@ typedef struct fp9_ffn_bank {
  * Output: y = sum_k w_k FFN_{id_k}(x) + sum of the shared FFNs (weight 1).
  * routed.n must equal n_experts and shared.n must equal n_shared; both
  * banks share the layer's hidden and inter.
+ * In fp9_moe_forward_residual the router starts reading w_router before
+ * it waits for the kernel queued just before it on the stream, when that
+ * kernel lets dependents start early (programmatic dependent launch): no
+ * kernel of this library writes w_router, and any other kernel has
+ * completed first unless it signals its dependents early itself; such a
+ * kernel must not write w_router right before a call.
  */
 typedef struct fp9_moe_layer {
     int64_t hidden;
