@@ -74,6 +74,20 @@ def test_pack_decode_argument_checks(lib):
     assert lib.fp9_decode(P, P, 4, 8, P + 8, None) == binding.FP9_ERR_ALIGN
 
 
+def test_from_fp8_argument_checks(lib):
+    # (w8, scale, rows, cols, body, sign, status, stream): every case is
+    # refused on the host before a device query or launch
+    assert lib.fp9_from_fp8(P, P, 128, 12, P, P, None, None) == binding.FP9_ERR_SHAPE       # cols % 8
+    assert lib.fp9_from_fp8(P, P, -1, 8, P, P, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_from_fp8(None, P, 128, 128, P, P, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_from_fp8(P, None, 128, 128, P, P, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_from_fp8(P, P, 128, 128, P, None, None, None) == binding.FP9_ERR_INVALID_ARG
+    assert lib.fp9_from_fp8(P + 4, P, 128, 128, P, P, None, None) == binding.FP9_ERR_ALIGN   # w8: 8 bytes
+    assert lib.fp9_from_fp8(P, P + 2, 128, 128, P, P, None, None) == binding.FP9_ERR_ALIGN   # scales: 4
+    assert lib.fp9_from_fp8(P, P, 128, 128, P + 4, P, None, None) == binding.FP9_ERR_ALIGN   # body: 8
+    assert lib.fp9_from_fp8(None, None, 0, 128, None, None, None, None) == binding.FP9_OK     # empty: no-op
+
+
 def _fwd(lib, layer, bsz=1, x=P, y=P + 0x10000, ws=P + 0x20000, ws_bytes=1 << 30):
     return lib.fp9_moe_forward(ctypes.byref(layer), x, bsz, y, None, None, ws, ws_bytes, None, None)
 
